@@ -1,0 +1,199 @@
+"""fp64 CPU oracle for the row softmax and the attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product library never loads it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, IEEE double, OpenMP over rows);
+this module only compiles it with gcc and marshals numpy arrays through ctypes.
+Which page and section each function follows is stated in ``oracle.c``.
+
+Parity status of the functions below: every one is pinned by the
+``-m "not gpu"`` tests in ``tests/test_oracle.py`` (worked values printed on
+the pages, closed forms, invariants, independent library routines and brute
+force on tiny inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lib = None
+
+
+def compile_oracle(src_path: str = _SRC, out_path: str = _LIB_PATH) -> str:
+    """Compile an oracle source file into a shared library with gcc.
+
+    -O2 without -ffast-math keeps every double operation IEEE (no reassociation,
+    no contraction into FMA across statements that would change results in a
+    way a reader cannot see; -ffp-contract=off makes that explicit).
+    """
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+           "-shared", "-std=c11", src_path, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Build ``_build/liboracle.so`` if it is missing or older than the source."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_oracle()
+    return _LIB_PATH
+
+
+def _bind(lib):
+    c_i64, c_dbl, c_int = ctypes.c_int64, ctypes.c_double, ctypes.c_int
+    vp = ctypes.c_void_p
+    lib.oracle_softmax_rows.argtypes = [vp, vp, c_i64, c_i64]
+    lib.oracle_softmax_rows.restype = None
+    lib.oracle_online_softmax_state.argtypes = [vp, c_i64, vp, c_i64, vp, vp]
+    lib.oracle_online_softmax_state.restype = None
+    lib.oracle_attention_fwd.argtypes = [vp, vp, vp, vp, vp, c_i64, c_i64, c_i64, c_dbl,
+                                         c_int, vp]
+    lib.oracle_attention_fwd.restype = None
+    lib.oracle_attention_rows.argtypes = [vp, vp, vp, c_i64, c_i64, c_i64, c_dbl, c_int, vp,
+                                          vp, vp, c_i64, vp, vp]
+    lib.oracle_attention_rows.restype = None
+    lib.oracle_attention_fwd_online.argtypes = [vp, vp, vp, vp, vp, c_i64, c_i64, c_i64,
+                                                c_dbl, c_int, vp, c_i64]
+    lib.oracle_attention_fwd_online.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.
+
+    ``path`` loads another build of an oracle source (the mutation tests use
+    it); the default is the committed ``oracle.c``.
+    """
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _f32(a) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float32)
+    return np.ascontiguousarray(a)
+
+
+def num_threads(lib=None) -> int:
+    return (lib or load()).oracle_num_threads()
+
+
+def softmax_rows(x, lib=None) -> np.ndarray:
+    """Stable row softmax of a 2-D array (cast to fp32, as the GPU path sees it).
+
+    Returns float64 [rows, N].
+    """
+    x = _f32(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    rows, N = x.shape
+    y = np.empty((rows, N), dtype=np.float64)
+    (lib or load()).oracle_softmax_rows(_ptr(x), _ptr(y), rows, N)
+    return y
+
+
+def online_softmax_state(x, block_ends, lib=None):
+    """(m, l) of a 1-D row consumed block by block with the online merge rule."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    ends = np.ascontiguousarray(np.asarray(block_ends, dtype=np.int64))
+    m = np.zeros(1, dtype=np.float64)
+    l = np.zeros(1, dtype=np.float64)
+    (lib or load()).oracle_online_softmax_state(_ptr(x), x.size, _ptr(ends), ends.size,
+                                                 _ptr(m), _ptr(l))
+    return float(m[0]), float(l[0])
+
+
+def _cu(cu_seqlens) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+
+
+def attention_packed(Q, K, V, cu_seqlens, scale, causal, lib=None, online_tile=None):
+    """Exact attention over packed sequences.
+
+    Q, K, V: [total, H, d] (any float dtype; cast to fp32, exact for bf16 values).
+    cu_seqlens: [B+1] prefix sums.  Returns (O [total, H, d] f64, lse [H, total] f64).
+    ``online_tile`` selects the tiled online recurrence (cross-check only).
+    """
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    total, H, d = Q.shape
+    cu = _cu(cu_seqlens)
+    B = cu.size - 1
+    if int(cu[-1]) != total:
+        raise ValueError("cu_seqlens[-1] must equal the number of packed tokens")
+    O = np.zeros((total, H, d), dtype=np.float64)
+    lse = np.zeros((H, total), dtype=np.float64)
+    lib = lib or load()
+    if online_tile is None:
+        lib.oracle_attention_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, H, d,
+                                 float(scale), int(bool(causal)), _ptr(cu))
+    else:
+        lib.oracle_attention_fwd_online(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), B, H,
+                                        d, float(scale), int(bool(causal)), _ptr(cu),
+                                        int(online_tile))
+    return O, lse
+
+
+def attention_dense(Q, K, V, scale, causal, lib=None, online_tile=None):
+    """Exact attention on a dense batch.
+
+    Q, K, V: [B, N, H, d].  Returns (O [B, N, H, d] f64, lse [B, H, N] f64).
+    """
+    Q = np.asarray(Q)
+    B, N, H, d = Q.shape
+    cu = np.arange(B + 1, dtype=np.int32) * N
+    O, lse = attention_packed(np.reshape(Q, (B * N, H, d)), np.reshape(K, (B * N, H, d)),
+                              np.reshape(V, (B * N, H, d)), cu, scale, causal, lib=lib,
+                              online_tile=online_tile)
+    return O.reshape(B, N, H, d), lse.reshape(H, B, N).transpose(1, 0, 2).copy()
+
+
+def attention_rows(Q, K, V, cu_seqlens, scale, causal, tok, head, lib=None):
+    """The attention definition on sampled (token, head) pairs of a packed batch.
+
+    Returns (O_rows [n, d] f64, lse_rows [n] f64).
+    """
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    total, H, d = Q.shape
+    cu = _cu(cu_seqlens)
+    B = cu.size - 1
+    tok = np.ascontiguousarray(np.asarray(tok, dtype=np.int64))
+    head = np.ascontiguousarray(np.asarray(head, dtype=np.int64))
+    if tok.shape != head.shape:
+        raise ValueError("tok and head must have the same shape")
+    if tok.size and (tok.min() < 0 or tok.max() >= total or head.min() < 0 or head.max() >= H):
+        raise ValueError("sample index out of range")
+    n = tok.size
+    O = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    (lib or load()).oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, d, float(scale),
+                                          int(bool(causal)), _ptr(cu), _ptr(tok), _ptr(head),
+                                          n, _ptr(O), _ptr(lse))
+    return O, lse
+
+
+if __name__ == "__main__":  # pragma: no cover - manual rebuild
+    print(build(force="--force" in sys.argv))

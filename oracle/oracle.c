@@ -1,0 +1,323 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the row softmax and the
+ * attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA library and includes nothing from it.
+ *
+ * Sources (the pages the method is defined on):
+ *   [L22] "第二十二课：Softmax 为什么难以高效，以及 FlashAttention 如何减少显存访问"
+ *         (lincklin.cn, lesson 22)
+ *   [FG]  "少搬一趟：FlashAttention 四代进化史" (chengshu-blog, booklet)
+ *   [OF]  "从 FlashAttention 看懂算子融合：为什么融合、少读写了什么、又会错在哪里"
+ *         (jokeuncle.github.io notes)
+ *
+ * Every floating-point step runs in IEEE double.  Inputs arrive as float
+ * (fp32 values, or bf16 values widened to fp32, which is exact) and are widened
+ * to double before any arithmetic.
+ *
+ * Layouts (row-major, contiguous):
+ *   softmax:   x, y  [rows, N]
+ *   attention: Q, K, V, O  [total, H, d]  (token-major, heads, head dim)
+ *              lse         [H, total]
+ *              cu_seqlens  [B + 1], int32 prefix sums of the sequence lengths;
+ *              sequence b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ *   A dense [B, N, H, d] batch is the packed layout with
+ *   cu_seqlens = {0, N, 2N, ..., B*N}.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Row softmax                                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Numerically stable softmax of one row, in the three passes of [L22] §三
+ * ("稳定 Softmax 至少需要哪些步骤"), using the shift by the row maximum of
+ * [L22] §二 ("数值稳定 Softmax"):
+ *   pass 1  m = max_j x_j
+ *   pass 2  s = sum_j exp(x_j - m)
+ *   pass 3  y_j = exp(x_j - m) / s
+ */
+static void softmax_row(const float *x, double *y, int64_t N)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) {
+        double xj = (double)x[j];
+        if (xj > m)
+            m = xj;
+    }
+    double s = 0.0;
+    for (int64_t j = 0; j < N; ++j)
+        s += exp((double)x[j] - m);
+    for (int64_t j = 0; j < N; ++j)
+        y[j] = exp((double)x[j] - m) / s;
+}
+
+/* Row softmax over a [rows, N] matrix; rows are independent ([L22] §五). */
+void oracle_softmax_rows(const float *x, double *y, int64_t rows, int64_t N)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        softmax_row(x + r * N, y + r * N, N);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Online softmax: the block merge, used only to cross-check the oracle     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Running (m, l) of a row whose entries arrive in blocks.  Block k covers
+ * x[block_ends[k-1] .. block_ends[k]-1] (block_ends[-1] = 0, the last entry of
+ * block_ends is n).  Each block yields its own (m_B, l_B) by the stable form;
+ * the running state absorbs it with the merge rule of [L22] §十九
+ * ("Online Softmax 的最大值更新"):
+ *   m = max(m_A, m_B)
+ *   l = exp(m_A - m) * l_A + exp(m_B - m) * l_B
+ * starting from m = -inf, l = 0 ([L22] §三十二).  A block of one entry is the
+ * per-element update of [L22] §二十.  The first merge would compute
+ * exp(-inf - (-inf)); since l_A = 0 there, the empty running state is simply
+ * replaced by the first block.
+ */
+void oracle_online_softmax_state(const double *x, int64_t n, const int64_t *block_ends,
+                                 int64_t nblocks, double *m_out, double *l_out)
+{
+    double m = -INFINITY, l = 0.0;
+    int64_t begin = 0;
+    for (int64_t k = 0; k < nblocks; ++k) {
+        int64_t end = block_ends[k];
+        if (end > n)
+            end = n;
+        if (end <= begin)
+            continue;
+        double mb = -INFINITY;
+        for (int64_t j = begin; j < end; ++j)
+            if (x[j] > mb)
+                mb = x[j];
+        double lb = 0.0;
+        for (int64_t j = begin; j < end; ++j)
+            lb += exp(x[j] - mb);
+        if (l == 0.0 && m == -INFINITY) {
+            m = mb;
+            l = lb;
+        } else {
+            double mn = m > mb ? m : mb;
+            l = exp(m - mn) * l + exp(mb - mn) * lb;
+            m = mn;
+        }
+        begin = end;
+    }
+    *m_out = m;
+    *l_out = l;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention forward                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Index of the sequence that owns token t (cu_seqlens is non-decreasing). */
+static int64_t owner_sequence(const int32_t *cu_seqlens, int64_t B, int64_t t)
+{
+    int64_t lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int64_t mid = (lo + hi + 1) / 2;
+        if ((int64_t)cu_seqlens[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+/*
+ * One query row of exact attention, straight from the definition
+ * ([L22] §十二–§十三, [FG] §1.2):
+ *   s_j  = scale * (q . k_j)                 for every visible key j
+ *   p_j  = exp(s_j - m) / l,  m = max_j s_j,  l = sum_j exp(s_j - m)
+ *   o    = sum_j p_j v_j
+ *   lse  = m + ln(l) = ln sum_j exp(s_j)     ([FG] §2.4)
+ * Visible keys: the keys of the query's own sequence, and, when causal,
+ * only those at positions j <= i ([L22] §三十四; masked scores are -inf and
+ * contribute exp(-inf) = 0, so they are simply left out of the sums).
+ *
+ * start: first token of the sequence; L: its length; i: query position in it.
+ * s: scratch of at least L doubles.
+ */
+static void attention_row(const float *Q, const float *K, const float *V, int64_t H,
+                          int64_t d, double scale, int causal, int64_t start, int64_t L,
+                          int64_t i, int64_t h, double *s, double *o, double *lse)
+{
+    const float *q = Q + ((start + i) * H + h) * d;
+    int64_t nvis = causal ? (i + 1 < L ? i + 1 : L) : L;
+
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const float *k = K + ((start + j) * H + h) * d;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            dot += (double)q[c] * (double)k[c];
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+    }
+    /* pass 2: normaliser */
+    double l = 0.0;
+    for (int64_t j = 0; j < nvis; ++j)
+        l += exp(s[j] - m);
+    /* pass 3: probabilities times values */
+    for (int64_t c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - m) / l;
+        const float *v = V + ((start + j) * H + h) * d;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] += p * (double)v[c];
+    }
+    *lse = nvis > 0 ? m + log(l) : -INFINITY;
+}
+
+/*
+ * Full attention forward over all sequences, heads and query rows.
+ * O: [total, H, d] doubles; lse: [H, total] doubles.
+ */
+void oracle_attention_fwd(const float *Q, const float *K, const float *V, double *O,
+                          double *lse, int64_t B, int64_t H, int64_t d, double scale,
+                          int causal, const int32_t *cu_seqlens)
+{
+    int64_t total = cu_seqlens[B];
+    /* scratch for one row of scores; no sequence is longer than the packed total */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(total > 0 ? total : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t w = 0; w < total * H; ++w) {
+            int64_t t = w / H, h = w % H;
+            int64_t b = owner_sequence(cu_seqlens, B, t);
+            int64_t start = cu_seqlens[b];
+            int64_t L = (int64_t)cu_seqlens[b + 1] - start;
+            attention_row(Q, K, V, H, d, scale, causal, start, L, t - start, h, s,
+                          O + (t * H + h) * d, lse + h * total + t);
+        }
+        free(s);
+    }
+}
+
+/*
+ * The same definition evaluated only on n sampled (token, head) pairs.
+ * O_rows: [n, d]; lse_rows: [n].  Used where the full problem is too large for
+ * the CPU within a test's time.
+ */
+void oracle_attention_rows(const float *Q, const float *K, const float *V, int64_t B,
+                           int64_t H, int64_t d, double scale, int causal,
+                           const int32_t *cu_seqlens, const int64_t *tok, const int64_t *head,
+                           int64_t n, double *O_rows, double *lse_rows)
+{
+    int64_t total = cu_seqlens[B];
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(total > 0 ? total : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n; ++r) {
+            int64_t t = tok[r], h = head[r];
+            int64_t b = owner_sequence(cu_seqlens, B, t);
+            int64_t start = cu_seqlens[b];
+            int64_t L = (int64_t)cu_seqlens[b + 1] - start;
+            attention_row(Q, K, V, H, d, scale, causal, start, L, t - start, h, s,
+                          O_rows + r * d, lse_rows + r);
+        }
+        free(s);
+    }
+}
+
+/*
+ * Cross-check only (not what the GPU path is compared with): the tiled
+ * online recurrence of [L22] §三十二 ("FlashAttention 的伪代码") and
+ * [FG] §2.2, evaluated in fp64 with key tiles of T entries.  Per query row:
+ *   m = -inf, l = 0, acc = 0
+ *   for each key tile:  new_m = max(m, max_j s_j)
+ *                       p_j   = exp(s_j - new_m)
+ *                       c     = exp(m - new_m)
+ *                       l     = c * l + sum_j p_j
+ *                       acc   = c * acc + sum_j p_j v_j
+ *                       m     = new_m
+ *   o = acc / l,  lse = m + ln l
+ * The first tile has m = -inf; its correction factor is taken as 0 (l and acc
+ * are still 0 there), which avoids the undefined exp(-inf - (-inf)).
+ */
+void oracle_attention_fwd_online(const float *Q, const float *K, const float *V, double *O,
+                                 double *lse, int64_t B, int64_t H, int64_t d, double scale,
+                                 int causal, const int32_t *cu_seqlens, int64_t T)
+{
+    int64_t total = cu_seqlens[B];
+    if (T < 1)
+        T = 1;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)T * sizeof(double));
+        double *acc = (double *)malloc((size_t)(d > 0 ? d : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t w = 0; w < total * H; ++w) {
+            int64_t t = w / H, h = w % H;
+            int64_t b = owner_sequence(cu_seqlens, B, t);
+            int64_t start = cu_seqlens[b];
+            int64_t L = (int64_t)cu_seqlens[b + 1] - start;
+            int64_t i = t - start;
+            int64_t nvis = causal ? (i + 1 < L ? i + 1 : L) : L;
+            const float *q = Q + (t * H + h) * d;
+            double m = -INFINITY, l = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                acc[c] = 0.0;
+            for (int64_t j0 = 0; j0 < nvis; j0 += T) {
+                int64_t j1 = j0 + T < nvis ? j0 + T : nvis;
+                double bmax = -INFINITY;
+                for (int64_t j = j0; j < j1; ++j) {
+                    const float *k = K + ((start + j) * H + h) * d;
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += (double)q[c] * (double)k[c];
+                    s[j - j0] = scale * dot;
+                    if (s[j - j0] > bmax)
+                        bmax = s[j - j0];
+                }
+                double new_m = m > bmax ? m : bmax;
+                double corr = (m == -INFINITY) ? 0.0 : exp(m - new_m);
+                l *= corr;
+                for (int64_t c = 0; c < d; ++c)
+                    acc[c] *= corr;
+                for (int64_t j = j0; j < j1; ++j) {
+                    double p = exp(s[j - j0] - new_m);
+                    const float *v = V + ((start + j) * H + h) * d;
+                    l += p;
+                    for (int64_t c = 0; c < d; ++c)
+                        acc[c] += p * (double)v[c];
+                }
+                m = new_m;
+            }
+            double *o = O + (t * H + h) * d;
+            for (int64_t c = 0; c < d; ++c)
+                o[c] = nvis > 0 ? acc[c] / l : 0.0;
+            lse[h * total + t] = nvis > 0 ? m + log(l) : -INFINITY;
+        }
+        free(acc);
+        free(s);
+    }
+}
+
+/* Threads the OpenMP runtime will use for the parallel loops above. */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

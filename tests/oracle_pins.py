@@ -1,0 +1,315 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes a loaded oracle library (``oracle.load()`` or a
+deliberately broken build of ``oracle.c``) and raises ``AssertionError`` when
+the oracle disagrees with:
+  * a value printed on a page (``tests/golden/worked_examples.json``),
+  * a closed form,
+  * an invariant of the definition (rows sum to 1, shift invariance, causal
+    rows blind to later keys, packed sequences independent of each other),
+  * an independent library routine (scipy.special.softmax / logsumexp,
+    torch's CPU scaled-dot-product attention in float64),
+  * a different algorithm for the same quantity (the online block merge).
+
+``tests/test_oracle.py`` runs every pin on the committed oracle;
+``tests/test_oracle_mutants.py`` checks that each planted mistake in a copy of
+the oracle fails at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "worked_examples.json")
+
+
+def golden():
+    with open(GOLDEN, encoding="utf-8") as f:
+        return json.load(f)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape:
+        raise AssertionError(f"{what}: shape {a.shape} vs {b.shape}")
+    if not np.all(np.isfinite(a)):
+        raise AssertionError(f"{what}: non-finite values")
+    err = float(np.max(np.abs(a - b))) if a.size else 0.0
+    if not err <= tol:
+        raise AssertionError(f"{what}: max abs error {err:.3e} > {tol:.1e}")
+
+
+# --------------------------------------------------------------------------
+# Row softmax
+# --------------------------------------------------------------------------
+
+def pin_softmax_worked_example(lib):
+    g = golden()["softmax_2_1_0"]
+    y = oracle.softmax_rows([g["x"]], lib=lib)[0]
+    _close(y, g["y"], g["tol"], "softmax [2,1,0] vs page")
+    e = np.array([math.exp(2), math.exp(1), 1.0])
+    _close(y, e / e.sum(), 1e-15, "softmax [2,1,0] vs closed form")
+
+
+def pin_softmax_overflow_row(lib):
+    g = golden()["overflow_1000_999_998"]
+    y = oracle.softmax_rows([g["x"]], lib=lib)[0]
+    y0 = oracle.softmax_rows([[2, 1, 0]], lib=lib)[0]
+    _close(y, y0, 1e-15, "[1000,999,998] vs [2,1,0] (shift invariance)")
+    # rows whose spread exceeds the double exponent range still work: only the
+    # shift by the maximum keeps every exp(x - m) in (0, 1]
+    y = oracle.softmax_rows([[1000.0, -1000.0, 0.0, 999.0]], lib=lib)[0]
+    _close(y, [1 / (1 + math.exp(-1)), 0.0, 0.0, math.exp(-1) / (1 + math.exp(-1))], 1e-15,
+           "wide-spread row")
+
+
+def pin_softmax_rows_sum_to_one(lib):
+    rng = np.random.default_rng(7)
+    for N in (1, 2, 3, 31, 33, 1000):
+        x = (rng.standard_normal((5, N)) * 5).astype(np.float32)
+        y = oracle.softmax_rows(x, lib=lib)
+        _close(y.sum(axis=1), np.ones(5), 1e-12, f"row sums N={N}")
+        if not (np.all(y > 0) and np.all(y <= 1)):
+            raise AssertionError("softmax outside (0, 1]")
+    _close(oracle.softmax_rows([[3.5]], lib=lib), [[1.0]], 0.0, "N=1")
+
+
+def pin_softmax_shift_invariance(lib):
+    rng = np.random.default_rng(8)
+    # multiples of 1/8 with |x| <= 30: x + c is exact in fp32 for the shifts below
+    x = (rng.integers(-240, 241, size=(6, 50)) / 8.0).astype(np.float32)
+    y = oracle.softmax_rows(x, lib=lib)
+    for c in (-1000.0, 7.0, 1000.0):
+        xs = (x.astype(np.float64) + c).astype(np.float32)
+        if not np.array_equal(xs.astype(np.float64), x.astype(np.float64) + c):
+            raise AssertionError("test setup: shift not exact")
+        _close(oracle.softmax_rows(xs, lib=lib), y, 1e-14, f"shift {c}")
+
+
+def pin_softmax_vs_scipy(lib):
+    from scipy.special import softmax as sp_softmax
+    rng = np.random.default_rng(9)
+    for N in (1, 7, 64, 4097):
+        x = (rng.standard_normal((4, N)) * 3).astype(np.float32)
+        x[0] += 1000.0
+        ref = sp_softmax(x.astype(np.float64), axis=1)
+        _close(oracle.softmax_rows(x, lib=lib), ref, 1e-14, f"scipy softmax N={N}")
+
+
+def pin_softmax_brute_force(lib):
+    rng = np.random.default_rng(10)
+    x = (rng.uniform(-30, 30, size=(8, 9))).astype(np.float32)
+    e = np.exp(x.astype(np.float64))
+    ref = e / e.sum(axis=1, keepdims=True)
+    _close(oracle.softmax_rows(x, lib=lib), ref, 1e-13, "naive softmax on |x| <= 30")
+
+
+# --------------------------------------------------------------------------
+# Online merge
+# --------------------------------------------------------------------------
+
+def pin_online_worked_examples(lib):
+    g = golden()
+    e = g["online_1_3_then_2_5"]
+    m, l = oracle.online_softmax_state(e["x"][:2], [2], lib=lib)
+    _close([m, l], [e["first_block_m"], e["first_block_l"]], e["tol"], "[1,3] vs page")
+    _close([m, l], [3.0, 1 + math.exp(-2)], 1e-15, "[1,3] closed form")
+    m, l = oracle.online_softmax_state(e["x"], e["block_ends"], lib=lib)
+    _close([m, l], [e["m"], e["l"]], e["tol"], "[1,3]+[2,5] vs page")
+    _close([m, l], [5.0, math.exp(-4) + math.exp(-2) + math.exp(-3) + 1.0], 1e-15,
+           "[1,3]+[2,5] closed form")
+
+    e = g["online_2_1_then_4"]
+    m, l = oracle.online_softmax_state(e["x"][:2], [2], lib=lib)
+    _close(l, e["first_block_l"], e["tol"], "[2,1] vs page")
+    m, l = oracle.online_softmax_state(e["x"], e["block_ends"], lib=lib)
+    _close([m, l], [e["m"], e["l"]], e["tol"], "[2,1]+[4] vs page")
+    _close(l, 1 + math.exp(-2) * (1 + math.exp(-1)), 1e-15, "[2,1]+[4] closed form")
+
+    e = g["online_2_1_then_4_3"]
+    m, l = oracle.online_softmax_state(e["x"], e["block_ends"], lib=lib)
+    _close([m, l], [e["m"], sum(math.exp(t) for t in e["direct_sum_terms"])], 1e-15,
+           "[2,1]+[4,3] vs direct sum")
+
+
+def pin_online_equals_logsumexp(lib):
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(300) * 4
+    x[137] += 50
+    ref = logsumexp(x)
+    for T in (1, 2, 3, 128, 300):
+        ends = list(range(T, 300, T)) + [300]
+        m, l = oracle.online_softmax_state(x, ends, lib=lib)
+        _close(m + math.log(l), ref, 1e-12, f"online lse T={T}")
+        _close(m, x.max(), 0.0, f"online max T={T}")
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def pin_attention_weighted_sum_example(lib):
+    g = golden()["weighted_sum_10_20_30"]
+    # d = 1, scale 1: q0 = 1 and key entries = the scores, so s_0j = [2, 1, 0]
+    K = np.array(g["scores"], dtype=np.float32).reshape(3, 1, 1)
+    Q = np.array([1, 0, 0], dtype=np.float32).reshape(3, 1, 1)
+    V = np.array(g["values"], dtype=np.float32).reshape(3, 1, 1)
+    O, lse = oracle.attention_packed(Q, K, V, [0, 3], 1.0, False, lib=lib)
+    _close(O[0, 0, 0], g["o"], g["tol"], "14.25 vs page")
+    e = np.exp([2.0, 1.0, 0.0])
+    _close(O[0, 0, 0], (e * np.array([10, 20, 30])).sum() / e.sum(), 1e-13, "14.25 closed form")
+    _close(lse[0, 0], math.log(e.sum()), 1e-15, "lse of [2,1,0]")
+    # queries 1 and 2 are zero vectors: uniform weights, O = mean(values)
+    _close(O[1:, 0, 0], [20.0, 20.0], 1e-13, "zero query")
+
+
+def pin_attention_uniform_scores(lib):
+    rng = np.random.default_rng(12)
+    lens = [5, 1, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, H, d = int(cu[-1]), 2, 8
+    Q = np.zeros((total, H, d), np.float32)
+    K = rng.standard_normal((total, H, d)).astype(np.float32)
+    V = rng.standard_normal((total, H, d)).astype(np.float32)
+    for causal in (False, True):
+        O, lse = oracle.attention_packed(Q, K, V, cu, 0.3, causal, lib=lib)
+        for b, L in enumerate(lens):
+            s = int(cu[b])
+            for i in range(L):
+                n = i + 1 if causal else L
+                _close(O[s + i], V[s:s + n].astype(np.float64).mean(axis=0), 1e-14,
+                       f"uniform O causal={causal}")
+                _close(lse[:, s + i], [math.log(n)] * H, 1e-14, f"uniform lse causal={causal}")
+
+
+def pin_attention_one_hot_key(lib):
+    rng = np.random.default_rng(13)
+    total, H, d = 6, 1, 4
+    Q = np.zeros((total, H, d), np.float32)
+    Q[:, 0, 0] = 1.0
+    K = (rng.standard_normal((total, H, d)) * 0.01).astype(np.float32)
+    K[2, 0, 0] = 2000.0                      # score 1000 above the rest with scale 0.5
+    V = rng.standard_normal((total, H, d)).astype(np.float32)
+    O, lse = oracle.attention_packed(Q, K, V, [0, total], 0.5, False, lib=lib)
+    for t in range(total):
+        _close(O[t, 0], V[2, 0], 1e-12, "one-hot key")
+        _close(lse[0, t], 0.5 * 2000.0, 1e-9, "one-hot lse")
+
+
+def _sdpa(Q, K, V, scale, causal):
+    """torch CPU float64 scaled-dot-product attention on [B, N, H, d] arrays."""
+    import torch
+    import torch.nn.functional as F
+    q = torch.from_numpy(np.asarray(Q, np.float64)).permute(0, 2, 1, 3)
+    k = torch.from_numpy(np.asarray(K, np.float64)).permute(0, 2, 1, 3)
+    v = torch.from_numpy(np.asarray(V, np.float64)).permute(0, 2, 1, 3)
+    o = F.scaled_dot_product_attention(q, k, v, is_causal=bool(causal), scale=float(scale))
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+def pin_attention_vs_torch_sdpa(lib):
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(14)
+    for (B, N, H, d, causal) in [(2, 7, 3, 5, False), (1, 9, 2, 8, True), (2, 33, 1, 16, True)]:
+        Q = rng.standard_normal((B, N, H, d)).astype(np.float32)
+        K = rng.standard_normal((B, N, H, d)).astype(np.float32)
+        V = rng.standard_normal((B, N, H, d)).astype(np.float32)
+        scale = 1 / math.sqrt(d)
+        O, lse = oracle.attention_dense(Q, K, V, scale, causal, lib=lib)
+        _close(O, _sdpa(Q, K, V, scale, causal), 1e-12, f"sdpa B{B} N{N} causal={causal}")
+        # lse: library logsumexp over the scores of each (b, h, i)
+        S = np.einsum("bihc,bjhc->bhij", Q.astype(np.float64), K.astype(np.float64)) * scale
+        if causal:
+            S = np.where(np.tril(np.ones((N, N), bool)), S, -np.inf)
+        _close(lse, logsumexp(S, axis=-1), 1e-12, "lse vs scipy logsumexp")
+
+
+def pin_attention_causal_ignores_future(lib):
+    rng = np.random.default_rng(15)
+    B, N, H, d = 1, 12, 2, 4
+    Q, K, V = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(3))
+    O, lse = oracle.attention_dense(Q, K, V, 0.5, True, lib=lib)
+    for i in (0, 5, 10):
+        K2, V2 = K.copy(), V.copy()
+        K2[:, i + 1:] = rng.standard_normal(K2[:, i + 1:].shape) * 9
+        V2[:, i + 1:] = rng.standard_normal(V2[:, i + 1:].shape) * 9
+        O2, lse2 = oracle.attention_dense(Q, K2, V2, 0.5, True, lib=lib)
+        _close(O2[:, :i + 1], O[:, :i + 1], 0.0, f"causal row <= {i} changed")
+        _close(lse2[:, :, :i + 1], lse[:, :, :i + 1], 0.0, "causal lse changed")
+        if np.allclose(O2[:, i + 1:], O[:, i + 1:]):
+            raise AssertionError("later rows should see the perturbation")
+
+
+def pin_attention_varlen_independent(lib):
+    rng = np.random.default_rng(16)
+    lens = [3, 8, 1, 5]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, H, d = int(cu[-1]), 2, 6
+    Q, K, V = (rng.standard_normal((total, H, d)).astype(np.float32) for _ in range(3))
+    for causal in (False, True):
+        O, lse = oracle.attention_packed(Q, K, V, cu, 0.4, causal, lib=lib)
+        for b, L in enumerate(lens):
+            s, e = int(cu[b]), int(cu[b + 1])
+            Ob, lseb = oracle.attention_dense(Q[None, s:e], K[None, s:e], V[None, s:e], 0.4,
+                                              causal, lib=lib)
+            _close(O[s:e], Ob[0], 0.0, f"varlen seq {b} causal={causal}")
+            _close(lse[:, s:e], lseb[0], 0.0, f"varlen lse seq {b}")
+            ref = _sdpa(Q[None, s:e], K[None, s:e], V[None, s:e], 0.4, causal)
+            _close(O[s:e], ref[0], 1e-12, f"varlen seq {b} vs sdpa")
+
+
+def pin_attention_online_matches(lib):
+    rng = np.random.default_rng(17)
+    lens = [130, 7, 257]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, H, d = int(cu[-1]), 2, 16
+    Q, K, V = (rng.standard_normal((total, H, d)).astype(np.float32) * 2 for _ in range(3))
+    for causal in (False, True):
+        O, lse = oracle.attention_packed(Q, K, V, cu, 0.25, causal, lib=lib)
+        for T in (1, 2, 7, 128):
+            O2, lse2 = oracle.attention_packed(Q, K, V, cu, 0.25, causal, lib=lib, online_tile=T)
+            _close(O2, O, 1e-12, f"online T={T} causal={causal}")
+            _close(lse2, lse, 1e-12, f"online lse T={T}")
+
+
+def pin_attention_rows_match_full(lib):
+    rng = np.random.default_rng(18)
+    lens = [40, 3, 77]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, H, d = int(cu[-1]), 3, 8
+    Q, K, V = (rng.standard_normal((total, H, d)).astype(np.float32) for _ in range(3))
+    O, lse = oracle.attention_packed(Q, K, V, cu, 0.35, True, lib=lib)
+    tok = rng.integers(0, total, 50)
+    head = rng.integers(0, H, 50)
+    Or, lr = oracle.attention_rows(Q, K, V, cu, 0.35, True, tok, head, lib=lib)
+    _close(Or, O[tok, head], 0.0, "sampled rows O")
+    _close(lr, lse[head, tok], 0.0, "sampled rows lse")
+
+
+def pin_attention_brute_force_tiny(lib):
+    # materialised S, P and PV for every (b, h) of a tiny batch
+    rng = np.random.default_rng(19)
+    B, N, H, d = 2, 5, 2, 3
+    Q, K, V = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(3))
+    for causal in (False, True):
+        O, lse = oracle.attention_dense(Q, K, V, 0.7, causal, lib=lib)
+        for b in range(B):
+            for h in range(H):
+                q, k, v = (X[b, :, h].astype(np.float64) for X in (Q, K, V))
+                S = 0.7 * q @ k.T
+                if causal:
+                    S[np.triu_indices(N, 1)] = -np.inf
+                P = np.exp(S) / np.exp(S).sum(axis=1, keepdims=True)
+                _close(O[b, :, h], P @ v, 1e-13, "brute-force O")
+                _close(lse[b, h], np.log(np.exp(S).sum(axis=1)), 1e-13, "brute-force lse")
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -1,0 +1,86 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Each mutant is the committed ``oracle/oracle.c`` with one plausible mistake
+(a dropped term, a wrong sign, a wrong index, an off-by-one mask, a transposed
+operand).  It is compiled on the CPU into a temporary library and the pins of
+``tests/oracle_pins.py`` are run against it; a mutant that passes every pin
+would mean the pins cannot see that kind of mistake.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement, occurrence index to replace)
+MUTANTS = [
+    ("softmax_min_not_max", "        if (xj > m)\n", "        if (xj < m)\n", 0),
+    ("softmax_no_shift_in_sum", "        s += exp((double)x[j] - m);", "        s += exp((double)x[j]);", 0),
+    ("softmax_no_normalise", "        y[j] = exp((double)x[j] - m) / s;", "        y[j] = exp((double)x[j] - m);", 0),
+    ("merge_wrong_sign", "l = exp(m - mn) * l + exp(mb - mn) * lb;", "l = exp(mn - m) * l + exp(mb - mn) * lb;", 0),
+    ("merge_keeps_old_max", "            m = mn;\n", "            m = m;\n", 0),
+    ("causal_excludes_diagonal", "int64_t nvis = causal ? (i + 1 < L ? i + 1 : L) : L;", "int64_t nvis = causal ? (i < L ? i : L) : L;", 0),
+    ("causal_sees_one_future_key", "int64_t nvis = causal ? (i + 1 < L ? i + 1 : L) : L;", "int64_t nvis = causal ? (i + 2 < L ? i + 2 : L) : L;", 0),
+    ("scale_dropped", "        s[j] = scale * dot;", "        s[j] = dot;", 0),
+    ("key_indexed_by_query", "const float *k = K + ((start + j) * H + h) * d;", "const float *k = K + ((start + i) * H + h) * d;", 0),
+    ("value_indexed_by_query", "const float *v = V + ((start + j) * H + h) * d;", "const float *v = V + ((start + i) * H + h) * d;", 0),
+    ("query_ignores_head", "const float *q = Q + ((start + i) * H + h) * d;", "const float *q = Q + ((start + i) * H) * d;", 0),
+    ("q_and_k_swapped", "dot += (double)q[c] * (double)k[c];", "dot += (double)k[c] * (double)k[c];", 0),
+    ("lse_drops_max", "*lse = nvis > 0 ? m + log(l) : -INFINITY;", "*lse = nvis > 0 ? log(l) : -INFINITY;", 0),
+    ("lse_log2", "*lse = nvis > 0 ? m + log(l) : -INFINITY;", "*lse = nvis > 0 ? m + log2(l) : -INFINITY;", 0),
+    ("p_not_normalised", "double p = exp(s[j] - m) / l;", "double p = exp(s[j] - m);", 0),
+    ("p_unshifted", "double p = exp(s[j] - m) / l;", "double p = exp(s[j]) / l;", 0),
+    ("varlen_start_zero", "            int64_t start = cu_seqlens[b];\n", "            int64_t start = 0;\n", 0),
+    ("varlen_length_is_total", "            int64_t L = (int64_t)cu_seqlens[b + 1] - start;\n", "            int64_t L = (int64_t)cu_seqlens[B] - start;\n", 0),
+    ("owner_off_by_one", "if ((int64_t)cu_seqlens[mid] <= t)", "if ((int64_t)cu_seqlens[mid] < t)", 0),
+    ("online_no_correction", "                l *= corr;\n", "", 0),
+    ("online_acc_no_correction", "                    acc[c] *= corr;\n", "", 0),
+    ("rows_wrong_lse_slot", "O_rows + r * d, lse_rows + r);", "O_rows + r * d, lse_rows + (r > 0 ? r - 1 : 0));", 0),
+]
+
+
+def _mutate(src, old, new, occ):
+    idx = -1
+    for _ in range(occ + 1):
+        idx = src.find(old, idx + 1)
+        if idx < 0:
+            raise AssertionError(f"mutation target not found: {old!r}")
+    return src[:idx] + new + src[idx + len(old):]
+
+
+_RUNNER = r"""
+import sys
+sys.path[:0] = [sys.argv[1], sys.argv[2]]
+import oracle, oracle_pins
+lib = oracle.load(sys.argv[3])
+failed = []
+for pin in oracle_pins.PINS:
+    try:
+        pin(lib)
+    except Exception as e:
+        failed.append(pin.__name__)
+print("FAILED_PINS", ",".join(failed))
+sys.exit(0 if failed else 3)
+"""
+
+
+@pytest.mark.parametrize("name,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, occ):
+    """A mutant is caught when some pin fails, or when it crashes outright
+    (a wrong index may run past a buffer); it runs in a child process so a
+    crash cannot take the test session down."""
+    src = open(SRC, encoding="utf-8").read()
+    mutated = _mutate(src, old, new, occ)
+    c_path = tmp_path / f"{name}.c"
+    c_path.write_text(mutated, encoding="utf-8")
+    so = oracle.compile_oracle(str(c_path), str(tmp_path / f"lib{name}.so"))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    tests = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _RUNNER, root, tests, so],
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 3, f"mutant {name} passed every pin"
