@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark: attention forward TFLOP/s and row-softmax GB/s on GB300.
+
+One step = one call of the fused attention forward (the tensor-core kernel)
+on the causal bf16 workload B=2, H=32, N=4096, d=128 (Q, K, V ~ N(0,1) rounded
+to bf16; 192 MiB of Q/K/V, larger than the 129 MB L2), through the C ABI.
+The row softmax (fp32, 4096 x N, the HBM-resident lengths) is timed in the
+same run with L2 flushed before every repetition and reported under
+"softmax".  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica of
+the workload (weak scaling, no collective on the data path); the time is the
+max over ranks and the value counts the work of all ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = ("attention fwd TFLOP/s and % BF16 peak; softmax GB/s and % HBM peak (1×GB300)")
+HEADLINE = "attn_bf16_causal_b2h32n4096d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCE = os.path.join(ROOT, "online_softmax_06_gb300", "csrc", "attn_bf16.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_bf16_causal_b2h32n4096d128.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(
+        k for k, w in workloads.WORKLOADS.items() if w.dtype == "bf16"))
+    ap.add_argument("--softmax-n", default="4096,32768",
+                    help="comma-separated row lengths for the softmax leg ('' to skip)")
+    ap.add_argument("--softmax-reps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        text = open(TRAFFIC_FILE, encoding="utf-8").read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(kernel source sha256\[:16\]\s*"
+                  r"([0-9a-f]+)\)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.windows = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[4:8]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if any(a - 0.03 <= r[0] <= b + 0.03 for a, b in self.windows)]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, n_rows: int, seed: int):
+    """A bounded, deterministic sample of the workload's query rows for the
+    oracle, and the algorithmic flops of those rows (4 * visible keys * d)."""
+    tok, head = workloads.sample_rows(w.total, w.H, n_rows, seed=seed)
+    cu = w.cu_seqlens()
+    seq = np.searchsorted(cu, tok, side="right") - 1
+    pos = tok - cu[seq]
+    L = (cu[seq + 1] - cu[seq]).astype(np.int64)
+    vis = (pos + 1) if w.causal else L
+    return tok, head, float(np.sum(4.0 * vis * w.d))
+
+
+def time_oracle(w, Qp, Kp, Vp, n_rows: int, seed: int):
+    import oracle
+    tok, head, flops = oracle_sample(w, n_rows, seed)
+    t0 = time.perf_counter()
+    oracle.attention_rows(Qp, Kp, Vp, w.cu_seqlens(), w.scale, w.causal, tok, head)
+    return time.perf_counter() - t0, flops
+
+
+def packed_f32(w):
+    Q, K, V = w.inputs()
+    Q, K, V = (t.float().numpy().reshape(w.total, w.H, w.d) for t in (Q, K, V))
+    return Q, K, V
+
+
+def cpu_baseline(w, seconds: float):
+    import oracle
+    Qp, Kp, Vp = packed_f32(w)
+    dt, _ = time_oracle(w, Qp, Kp, Vp, 64, seed=1)          # calibration
+    per_row = max(dt / 64, 1e-6)
+    n = int(min(max(seconds / per_row, 256), w.total * w.H))
+    dt, flops = time_oracle(w, Qp, Kp, Vp, n, seed=2)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} (token, head) query rows of {w.name} drawn uniformly with seed 2 "
+                      f"(fp64, {dt:.1f} s); flops = 4 * visible keys * d per row"}
+
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return 0
+    import oracle
+    w = workloads.WORKLOADS[args.workload]
+    Qp, Kp, Vp = packed_f32(w)
+    dt, _ = time_oracle(w, Qp, Kp, Vp, 64, seed=1)
+    per_row = max(dt / 64, 1e-6)
+    # each step is a bounded sample sized so the whole run stays within minutes
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    n = int(min(max(budget / per_row, 64), w.total * w.H))
+    for s in range(args.warmup):
+        time_oracle(w, Qp, Kp, Vp, n, seed=100 + s)
+    tot_t, tot_f = 0.0, 0.0
+    for s in range(args.steps):
+        dt, fl = time_oracle(w, Qp, Kp, Vp, n, seed=1000 + s)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * tot_t / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"{n} sampled query rows of {w.name} per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "varlen_lengths": list(w.lengths) or None,
+            "flops_per_step": w.flops(),
+            "l2": "inputs larger than L2 (Q/K/V %.0f MiB vs 129 MB L2)" %
+                  (3 * w.total * w.H * w.d * 2 / 2**20),
+            "parallelism": "replicas (weak scaling, no collective)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU legs
+# ---------------------------------------------------------------------------
+def time_attention(fa, w, dev, steps, warmup, dist, clocks):
+    import torch
+    Q, K, V = w.inputs()
+    q, k, v = (t.to(dev) for t in (Q, K, V))
+    o = torch.empty_like(q)
+    lse_shape = (w.H, w.total) if w.varlen else (w.B, w.H, w.N)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev) if w.varlen else None
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+
+    def launch():
+        if w.varlen:
+            rc = fa.fa_attention_fwd_varlen(*args, w.B, w.H, w.N, w.total, w.d, w.scale,
+                                            int(w.causal), cu.data_ptr())
+        else:
+            rc = fa.fa_attention_fwd(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal), None)
+        if rc != 0:
+            raise RuntimeError(f"attention launch failed: {fa.strerror(rc)}")
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(steps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(t0, time.time())
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    dev_err = fa.fa_get_device_error()
+    if dev_err != 0:
+        raise RuntimeError(f"device error word {dev_err:#x}")
+    return ms, steps
+
+
+def time_e2e(fa, w, dev, steps, warmup):
+    """Same metric through the C ABI with host buffers: every step copies Q, K, V
+    from pinned host memory, runs the kernel and copies O and lse back."""
+    import torch
+    Q, K, V = w.inputs()
+    hq, hk, hv = (t.pin_memory() for t in (Q, K, V))
+    q, k, v = (torch.empty_like(t, device=dev) for t in (Q, K, V))
+    o = torch.empty_like(q)
+    lse_shape = (w.H, w.total) if w.varlen else (w.B, w.H, w.N)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    ho = torch.empty_like(Q).pin_memory()
+    hl = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
+    cu = torch.from_numpy(w.cu_seqlens()).to(dev) if w.varlen else None
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if w.varlen:
+            rc = fa.fa_attention_fwd_varlen(*args, w.B, w.H, w.N, w.total, w.d, w.scale,
+                                            int(w.causal), cu.data_ptr())
+        else:
+            rc = fa.fa_attention_fwd(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal), None)
+        if rc != 0:
+            raise RuntimeError(fa.strerror(rc))
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": w.flops() * steps / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps}
+
+
+def time_softmax(fa, dev, Ns, reps, peaks, clocks):
+    """Row softmax 4096 x N: L2 flushed (a 512 MiB write) before every rep; each
+    rep timed alone with CUDA events; median reported."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for N in Ns:
+        x = torch.from_numpy(workloads.softmax_workload(N)).to(dev)
+        y = torch.empty_like(x)
+        rows = x.shape[0]
+        for _ in range(3):
+            fa.fa_softmax_rows(x.data_ptr(), y.data_ptr(), rows, N)
+        times = []
+        t0 = time.time()
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            rc = fa.fa_softmax_rows(x.data_ptr(), y.data_ptr(), rows, N)
+            e1.record(stream)
+            if rc != 0:
+                raise RuntimeError(fa.strerror(rc))
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        clocks.mark(t0, time.time())
+        # warm (no flush) for context
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fa.fa_softmax_rows(x.data_ptr(), y.data_ptr(), rows, N)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        warm_ms = e0.elapsed_time(e1) / reps
+        ms = statistics.median(times)
+        nbytes = 8.0 * rows * N
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[str(N)] = {"rows": rows, "N": N, "ms": ms, "GB_per_s": gbs,
+                       "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                       "bytes_per_launch": nbytes, "l2": "flushed before each rep",
+                       "warm_GB_per_s": nbytes / (warm_ms / 1e3) / 1e9}
+        del x, y
+    return out
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import online_softmax_06_gb300 as fa
+    fa.build()
+    fa.lib()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        dist = tdist
+    peaks, peak_src = load_peaks()
+    w = workloads.WORKLOADS[args.workload]
+    clocks = ClockSampler(local_rank)
+    try:
+        ms, steps = time_attention(fa, w, dev, args.steps, args.warmup, dist, clocks)
+        ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        if dist:
+            dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+        ms_max = float(ms_t.item())
+        softmax = {}
+        if args.softmax_n and rank == 0:
+            Ns = [int(s) for s in args.softmax_n.split(",") if s]
+            softmax = time_softmax(fa, dev, Ns, args.softmax_reps, peaks, clocks)
+    finally:
+        clk = clocks.stop()
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e(fa, w, dev, max(3, min(args.steps, 50)), 2)
+    flops = w.flops()
+    value = world * flops * steps / (ms_max / 1e3) / 1e12
+    per_launch_s = (ms / 1e3) / steps
+    achieved = flops / per_launch_s / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(),
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "kernel": "attn_fwd_bf16_kernel<128>",
+                     "algorithmic_flops_per_launch": flops},
+        "gpu_launches": steps,
+        "clocks": clk,
+        "softmax": softmax,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

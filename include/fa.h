@@ -1,0 +1,153 @@
+/*
+ * fa.h -- C ABI of libfa.so: numerically stable row softmax and exact fused
+ * attention forward (online softmax, FlashAttention-style) for one NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The operations are defined on these pages:
+ *   [L22] "第二十二课：Softmax 为什么难以高效，以及 FlashAttention 如何减少显存访问"
+ *         (lincklin.cn, lesson 22)
+ *   [FG]  "少搬一趟：FlashAttention 四代进化史" (chengshu-blog booklet)
+ *   [OF]  "从 FlashAttention 看懂算子融合：为什么融合、少读写了什么、又会错在哪里"
+ *         (jokeuncle.github.io notes)
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller (for
+ *     example memory allocated through PyTorch).  The library never frees or
+ *     keeps them; it allocates no device memory per call.
+ *   - Work is enqueued on the library stream of the calling thread (see
+ *     fa_set_stream) and the call returns without synchronising, except where
+ *     a function says otherwise.  A return value of FA_OK means the work was
+ *     launched; faults inside a kernel surface at the caller's next
+ *     synchronisation, and timeouts of the kernels' internal waits are
+ *     reported by fa_get_device_error.
+ *   - A negative return value means nothing was launched.
+ *   - The library is thread-compatible: the stream setting is per host thread.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+/* Entry points keep default visibility; everything else in the library is hidden. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes --------------------------------------------------------- */
+#define FA_OK 0
+#define FA_ERR_NULL_POINTER (-1)    /* a required pointer is NULL               */
+#define FA_ERR_BAD_SIZE (-2)        /* a size is negative or inconsistent         */
+#define FA_ERR_UNSUPPORTED (-3)     /* head dimension or option not supported     */
+#define FA_ERR_MISALIGNED (-4)      /* a pointer breaks the alignment rule        */
+#define FA_ERR_CUDA (-5)            /* a CUDA runtime/driver call failed          */
+#define FA_ERR_TOO_LARGE (-6)       /* a size exceeds what the kernels index      */
+#define FA_ERR_NO_DEVICE (-7)       /* no usable sm_103 device is current         */
+
+/* ---- device error word bits (fa_get_device_error) ------------------------- */
+#define FA_DEVERR_WAIT_TIMEOUT 0x1  /* a pipeline wait gave up (bounded wait)     */
+#define FA_DEVERR_BAD_SEQLENS 0x2   /* cu_seqlens disagreed with N or the tensors */
+
+/*
+ * Row softmax, numerically stable ([L22] §二 "数值稳定 Softmax": shift by the
+ * row maximum; §三 the max / exp-sum / normalise steps; §六–§十 warp-per-row
+ * and block-per-row reductions):
+ *     y[r, j] = exp(x[r, j] - m_r) / sum_k exp(x[r, k] - m_r),  m_r = max_k x[r, k]
+ *
+ *   x     fp32 [rows, N], row-major, contiguous (row stride N elements).
+ *   y     fp32 [rows, N], same layout.  y == x (in place) is allowed; any other
+ *         overlap is not.
+ *   rows  number of rows, >= 0 (0 launches nothing and returns FA_OK).
+ *   N     row length, >= 0 (0 launches nothing).  rows * N < 2^62.
+ * Pointers need 4-byte alignment; 16-byte aligned pointers with N % 4 == 0 take
+ * the vectorised path.  A row with a NaN yields NaN; a row of only -inf yields
+ * NaN (0/0 in the definition).
+ * Errors: FA_ERR_NULL_POINTER (x or y NULL with rows*N > 0), FA_ERR_BAD_SIZE
+ * (negative size), FA_ERR_MISALIGNED, FA_ERR_CUDA.
+ */
+FA_API int fa_softmax_rows(const float *x, float *y, int64_t rows, int64_t N);
+
+/*
+ * Exact attention forward, bf16 in / bf16 out, fp32 accumulation, on the
+ * tensor cores (tcgen05 + TMEM, TMA-fed):
+ *     S = scale * Q K^T (+ mask),  P = softmax(S) row-wise,  O = P V,
+ *     lse[i] = log(sum_j exp(S[i, j]))  (natural log)
+ * computed tile by tile with the online-softmax recurrence ([L22] §三十二
+ * pseudo-code; [FG] §2.2 update of m, l and the unnormalised output, §3.2
+ * deferred normalisation, §2.4 logsumexp; [OF] "FlashAttention 的核心变化")
+ * without materialising S or P in device memory.
+ *
+ * Layouts (all contiguous, row-major):
+ *   dense  (cu_seqlens == NULL): Q, K, V, O  [B, N, H, d];  lse [B, H, N].
+ *   packed (cu_seqlens != NULL): Q, K, V, O  [total, H, d]; lse [H, total];
+ *          sequence b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 ([L22] §三十五
+ *          "Packed Sequence / Variable-Length"); B = number of sequences,
+ *          N = longest sequence length (an upper bound is fine).
+ *   Q, K, V, O: bf16 (raw 16-bit storage); lse: fp32.
+ *   cu_seqlens: DEVICE int32 [B + 1], non-decreasing, cu_seqlens[0] = 0.
+ *   d: 64 or 128.  scale: multiplies Q K^T (1/sqrt(d) for standard attention).
+ *   causal != 0: query i sees keys j <= i of its own sequence ([L22] §三十四).
+ * Alignment: Q, K, V, O 16-byte aligned; lse 4-byte aligned.
+ * The packed form reads total = cu_seqlens[B] back to the host and therefore
+ * synchronises the library stream once per call (fa_attention_fwd_varlen takes
+ * total from the caller and does not).  A sequence longer than N is not
+ * computed and sets FA_DEVERR_BAD_SEQLENS in the device error word.
+ * Errors: FA_ERR_NULL_POINTER, FA_ERR_BAD_SIZE, FA_ERR_UNSUPPORTED (d),
+ * FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE, FA_ERR_NO_DEVICE, FA_ERR_CUDA.
+ */
+FA_API int fa_attention_fwd(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                     int H, int N, int d, float scale, int causal, const int32_t *cu_seqlens);
+
+/*
+ * Same as fa_attention_fwd with packed sequences, with the packed token count
+ * `total` (= cu_seqlens[B]) given by the caller: nothing is read back and the
+ * call does not synchronise.  cu_seqlens must not be NULL.
+ */
+FA_API int fa_attention_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *lse,
+                            int B, int H, int N, int64_t total, int d, float scale, int causal,
+                            const int32_t *cu_seqlens);
+
+/*
+ * Exact attention forward in fp32 throughout (fp32 Q, K, V, O, lse), on the
+ * CUDA cores, for inputs that need fp32 accuracy.  Same definition, layouts,
+ * masks and cu_seqlens convention as fa_attention_fwd (the packed form reads
+ * cu_seqlens[B] back and synchronises the stream once).  d: 1 .. 128.
+ * Pointers 4-byte aligned.
+ */
+FA_API int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t *cu_seqlens);
+
+/*
+ * Sets the CUDA stream (a cudaStream_t passed as void*) that later calls from
+ * this host thread launch on; NULL selects the legacy default stream.  The
+ * library does not take ownership.  Returns FA_OK.
+ */
+FA_API int fa_set_stream(void *stream);
+
+/* The stream currently selected for this host thread. */
+FA_API void *fa_get_stream(void);
+
+/*
+ * Returns the device error word of the current device (an OR of FA_DEVERR_*
+ * bits raised by kernels since the last call) and clears it.  Synchronises the
+ * device.  Returns a negative FA_ERR_* code if the word cannot be read.
+ */
+FA_API int fa_get_device_error(void);
+
+/* Static, human-readable text for an FA_* return code. */
+FA_API const char *fa_strerror(int code);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

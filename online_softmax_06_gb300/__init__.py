@@ -1,0 +1,209 @@
+"""Python binding of libfa.so: row softmax and fused attention forward on GB300.
+
+This module only marshals arguments: it passes device pointers of torch
+tensors, sizes and the current CUDA stream to the C-ABI entry points declared
+in ``include/fa.h`` and raises on a non-zero return code.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+compiled library is missing, importing the C functions fails loudly.
+
+Raw C-ABI names (same names, same argument order, ints and pointers only):
+``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
+``fa_attention_fwd_f32``, ``fa_set_stream``, ``fa_get_stream``,
+``fa_get_device_error``, ``fa_strerror``, ``fa_version``.
+Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfa.so")
+
+FA_OK = 0
+FA_DEVERR_WAIT_TIMEOUT = 0x1
+FA_DEVERR_BAD_SEQLENS = 0x2
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed: {code} ({strerror(code)})")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA sources into _build/libfa.so (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded libfa.so (ctypes.CDLL).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libfa.so not built ({LIB_PATH} missing); run "
+                              "online_softmax_06_gb300.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        L.fa_softmax_rows.argtypes = [vp, vp, i64, i64]
+        L.fa_attention_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+        L.fa_attention_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32,
+                                              i32, vp]
+        L.fa_attention_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+        L.fa_set_stream.argtypes = [vp]
+        L.fa_get_stream.argtypes = []
+        L.fa_get_stream.restype = vp
+        L.fa_get_device_error.argtypes = []
+        L.fa_strerror.argtypes = [i32]
+        L.fa_strerror.restype = ctypes.c_char_p
+        L.fa_version.argtypes = []
+        for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
+                     "fa_attention_fwd_f32", "fa_set_stream", "fa_get_device_error",
+                     "fa_version"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().fa_strerror(int(code)).decode()
+    except ImportError:
+        return "libfa.so not loaded"
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != FA_OK:
+        raise FaError(rc, where)
+
+
+# ---- raw C-ABI wrappers (same names as include/fa.h) -------------------------
+
+def fa_softmax_rows(x_ptr: int, y_ptr: int, rows: int, N: int) -> int:
+    return lib().fa_softmax_rows(x_ptr, y_ptr, rows, N)
+
+
+def fa_attention_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens) -> int:
+    return lib().fa_attention_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens)
+
+
+def fa_attention_fwd_varlen(q, k, v, o, lse, B, H, N, total, d, scale, causal,
+                            cu_seqlens) -> int:
+    return lib().fa_attention_fwd_varlen(q, k, v, o, lse, B, H, N, total, d, scale, causal,
+                                         cu_seqlens)
+
+
+def fa_attention_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens) -> int:
+    return lib().fa_attention_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens)
+
+
+def fa_set_stream(stream_ptr) -> int:
+    return lib().fa_set_stream(stream_ptr)
+
+
+def fa_get_stream():
+    return lib().fa_get_stream()
+
+
+def fa_get_device_error() -> int:
+    return lib().fa_get_device_error()
+
+
+def fa_version() -> int:
+    return lib().fa_version()
+
+
+# ---- tensor-level helpers -------------------------------------------------------
+
+def _use_current_stream(device):
+    import torch
+    fa_set_stream(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return t.data_ptr() if t is not None else None
+
+
+def softmax_rows(x, out=None):
+    """Row softmax of a contiguous fp32 CUDA tensor viewed as [rows, N] (last dim N).
+
+    ``out`` may be ``x`` itself (in place).  Returns ``out``.
+    """
+    import torch
+    if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or not out.is_contiguous() or out.dtype != torch.float32:
+        raise ValueError("out must match x")
+    N = x.shape[-1] if x.dim() > 0 else 1
+    rows = x.numel() // N if N > 0 else 0
+    _use_current_stream(x.device)
+    _check(fa_softmax_rows(_ptr(x), _ptr(out), rows, N), "fa_softmax_rows")
+    return out
+
+
+def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None,
+                  cu_seqlens=None, max_seqlen: int | None = None, total: int | None = None,
+                  out=None, lse=None):
+    """Exact attention forward through the C ABI.
+
+    Dense: q, k, v [B, N, H, d] -> (O [B, N, H, d], lse [B, H, N] fp32).
+    Packed: q, k, v [total, H, d] with ``cu_seqlens`` (int32 CUDA [B+1]) and
+    ``max_seqlen`` -> (O [total, H, d], lse [H, total]).  ``total`` defaults to
+    q.shape[0], which avoids the library's read-back of cu_seqlens[B].
+    bf16 inputs run on the tensor cores (d = 64 or 128); fp32 inputs on the
+    fp32 path (d <= 128).
+    """
+    import torch
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must all be bfloat16 or all float32")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must have the same shape")
+    d = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if cu_seqlens is None:
+        B, N, H, _ = q.shape
+        lse_shape = (B, H, N)
+    else:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        tot, H, _ = q.shape
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen) if max_seqlen is not None else tot
+        total = tot if total is None else int(total)
+        lse_shape = (H, tot)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    _use_current_stream(q.device)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse))
+    cu = _ptr(cu_seqlens)
+    if q.dtype == torch.float32:
+        rc = fa_attention_fwd_f32(*args, B, H, N, d, float(scale), int(bool(causal)), cu)
+        _check(rc, "fa_attention_fwd_f32")
+    elif cu_seqlens is not None:
+        rc = fa_attention_fwd_varlen(*args, B, H, N, total, d, float(scale), int(bool(causal)),
+                                     cu)
+        _check(rc, "fa_attention_fwd_varlen")
+    else:
+        rc = fa_attention_fwd(*args, B, H, N, d, float(scale), int(bool(causal)), None)
+        _check(rc, "fa_attention_fwd")
+    return out, lse
+
+
+__all__ = [
+    "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
+    "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
+    "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
+    "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",
+]

@@ -1,0 +1,578 @@
+// attn_bf16.cu -- exact attention forward on the sm_103a tensor cores.
+//
+// What it computes: O = softmax(scale * Q K^T + mask) V and the row logsumexp,
+// tile by tile with the online-softmax recurrence of "第二十二课：Softmax 为什么难以
+// 高效…" (lincklin.cn) §三十二 and "少搬一趟：FlashAttention 四代进化史" §2.2: for each
+// K/V tile the running row max m, running sum l and the unnormalised output o~
+// are updated (o~ and l rescaled by exp(m_old - m_new)), and O = o~ / l and
+// lse = m + ln l are written once at the end (§3.2 deferred normalisation,
+// §2.4 logsumexp).  S and P never leave the chip.
+//
+// How it maps to a GB300 SM (the booklet's §5.5 pipeline for Blackwell is the
+// starting point; everything here is written for tcgen05 from the PTX ISA):
+//   * one CTA per SM, 320 threads, owns two 128-row Q tiles of one
+//     (sequence, head) -- "Q0" and "Q1", adjacent in the sequence -- so every
+//     K/V tile loaded into shared memory feeds 2 x 128 rows;
+//   * warp 8 (one lane) issues TMA loads: both Q tiles once, then K_0, V_0, K_1,
+//     V_1, ... into a ring of shared-memory stages guarded by full/empty
+//     mbarriers;
+//   * warp 9 (one lane) owns the tensor memory and issues every tcgen05.mma:
+//     S_t = Q_t K_j^T (bf16 x bf16 -> fp32, M=N=128, K=d) into TMEM, and
+//     O_t += P_t V_j with P_t read from TMEM (written there by the softmax
+//     threads over the upper half of S_t) and V_j from shared memory as an
+//     MN-major operand; the issue order QK0, QK1, PV0, QK0', PV1, QK1', ...
+//     lets one tile's softmax run while the other tile's MMAs execute;
+//   * warps 0-3 and 4-7 are the softmax warpgroups of Q0 and Q1: thread r owns
+//     query row r (TMEM lane r), loads its 128 scores with tcgen05.ld, applies
+//     the causal / sequence-end mask on the tiles that need it, updates m and
+//     l, converts P to bf16 into TMEM, and rescales its row of O in TMEM only
+//     when its maximum grew (warp-uniform skip otherwise); after the last tile
+//     it normalises O and writes O (bf16) and lse (fp32).
+// Tensor memory per CTA (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d),
+// O1 [256+d, 256+2d); P_t aliases columns 64..127 of S_t.
+// Every wait is bounded (ptx::mbar_wait); a timed-out wait raises an error bit,
+// all roles leave their loops, in-flight copies and MMAs are drained, and the
+// CTA frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_error.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int BM = 128;              // query rows per Q tile
+constexpr int BN = 128;              // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColPinS = 64;    // P_t starts 64 columns into S_t
+constexpr float kLn2 = 0.69314718055994531f;
+
+// TMEM column of S_t and of O_t (t = 0, 1) for head dimension D.
+__device__ __forceinline__ uint32_t col_s(int t) { return uint32_t(t) * 128u; }
+template <int D>
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
+constexpr uint32_t kChunkBytes = BM * 128;  // 128 rows x 128 bytes (64 bf16)
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;                  // 128-byte column chunks
+    static constexpr uint32_t kTileBytes = BM * D * 2;      // one Q, K or V tile
+    static constexpr int kStages = (D == 128) ? 4 : 8;      // K/V ring depth
+    // shared memory: [Q0][Q1][ring x kStages][barriers, flags]
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffRing = 2 * kTileBytes;
+    static constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
+    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 2 + 2 + 2 + 1);
+    static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;  // +1024 align slack
+};
+
+struct Bf16Params {
+    CUtensorMap tm_q, tm_k, tm_v;    // 3-D maps over [total, H, d] bf16, box {64, 1, 128}
+    __nv_bfloat16 *O;
+    float *lse;
+    int B, H, N;
+    int n_pairs;                     // Q-tile pairs per (sequence, head) at length N
+    int64_t total;
+    float scale_log2;                // scale * log2(e)
+    int causal;
+    const int32_t *cu_seqlens;
+    int *err_word;
+};
+
+struct Barriers {
+    uint64_t *q_full, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *drain;
+};
+
+// Bounded wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return;
+        if ((it & 255u) == 255u && ptx::globaltimer() - t0 > kWaitTimeoutNs)
+            return;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_bf16_kernel(const __grid_constant__ Bf16Params p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    Barriers bar;
+    bar.q_full = bars;
+    bar.kv_full = bars + 1;
+    bar.kv_empty = bars + 1 + C::kStages;
+    bar.s_full = bars + 1 + 2 * C::kStages;
+    bar.p_full = bar.s_full + 2;
+    bar.o_full = bar.p_full + 2;
+    bar.drain = bar.o_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + (C::kBarBytes / 8));
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    // ---- work item: (sequence b, head h, Q-tile pair), heaviest pairs first ----
+    const int bh_count = p.B * p.H;
+    const int pair = p.n_pairs - 1 - int(blockIdx.x / bh_count);
+    const int bh = int(blockIdx.x % bh_count);
+    const int b = bh / p.H, h = bh % p.H;
+    int64_t start;
+    int L;
+    if (p.cu_seqlens != nullptr) {
+        const int64_t s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.total || s1 - s0 > p.N) {
+            if (threadIdx.x == 0 && pair == 0 && h == 0)
+                record_device_error(p.err_word, FA_DEVERR_BAD_SEQLENS);
+            return;
+        }
+        start = s0;
+        L = int(s1 - s0);
+    } else {
+        start = int64_t(b) * p.N;
+        L = p.N;
+    }
+    const int qt0 = 2 * pair;                  // Q0 = tile qt0, Q1 = tile qt0 + 1
+    if (qt0 * BM >= L)
+        return;                                // whole CTA: nothing to do
+    const bool has_q1 = (qt0 + 1) * BM < L;
+    const int n_kv = (L + BN - 1) / BN;
+    const int n0 = p.causal ? qt0 + 1 : n_kv;
+    const int n1 = has_q1 ? (p.causal ? qt0 + 2 : n_kv) : 0;
+    const int n_max = n0 > n1 ? n0 : n1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- set-up: barriers, tensor memory ----------------------------------
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar.q_full, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(&bar.kv_full[s], 1);
+            ptx::mbar_init(&bar.kv_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(&bar.s_full[t], 1);
+            ptx::mbar_init(&bar.p_full[t], 128);
+            ptx::mbar_init(&bar.o_full[t], 1);
+        }
+        ptx::mbar_init(bar.drain, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kWarpLoad && lane == 0) {
+        ptx::prefetch_tmap(&p.tm_q);
+        ptx::prefetch_tmap(&p.tm_k);
+        ptx::prefetch_tmap(&p.tm_v);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool aborted = false;
+
+    uint8_t *q_smem[2] = {smem + C::kOffQ, smem + C::kOffQ + C::kTileBytes};
+    uint8_t *ring = smem + C::kOffRing;
+
+    if (warp == kWarpLoad) {
+        // ======================= TMA producer ==============================
+        if (lane == 0) {
+            int last_phase[C::kStages];
+            for (int s = 0; s < C::kStages; ++s)
+                last_phase[s] = -1;
+            const int nq = has_q1 ? 2 : 1;
+            ptx::mbar_arrive_expect_tx(bar.q_full, nq * C::kTileBytes);
+            for (int t = 0; t < nq; ++t)
+                for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_3d(q_smem[t] + c * kChunkBytes, &p.tm_q, bar.q_full, c * 64, h,
+                                     int(start + int64_t(qt0 + t) * BM));
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int j = 0; j < n_max && !aborted; ++j) {
+                for (int kv = 0; kv < 2; ++kv) {
+                    if (!ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag,
+                                        p.err_word)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kTileBytes);
+                    const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes, tm,
+                                         &bar.kv_full[stage], c * 64, h,
+                                         int(start + int64_t(j) * BN));
+                    last_phase[stage] = int(phase);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (aborted || *abort_flag) {
+                // let every copy already issued land before the CTA goes away
+                drain_wait(bar.q_full, 0);
+                for (int s = 0; s < C::kStages; ++s)
+                    if (last_phase[s] >= 0)
+                        drain_wait(&bar.kv_full[s], uint32_t(last_phase[s]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ======================= MMA issuer ================================
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, true);
+            constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
+            constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kChunkBytes, 1024);
+            const uint32_t q_addr[2] = {ptx::smem_u32(q_smem[0]), ptx::smem_u32(q_smem[1])};
+            const uint32_t ring_addr = ptx::smem_u32(ring);
+
+            auto issue_qk = [&](int t, uint32_t k_addr) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    ptx::mma_ss(tmem + col_s(t), ptx::smem_desc(desc_kmajor, q_addr[t] + off),
+                                ptx::smem_desc(desc_kmajor, k_addr + off), idesc_qk,
+                                kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bar.s_full[t]);
+            };
+            auto issue_pv = [&](int t, uint32_t v_addr, bool accumulate) {
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    ptx::mma_ts(tmem + col_o<D>(t), tmem + col_s(t) + kColPinS + kk * 8,
+                                ptx::smem_desc(desc_mnmajor, v_addr + kk * 16 * 128), idesc_pv,
+                                (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            int stage = 0;
+            uint32_t phase = 0;
+            auto next_stage = [&](uint32_t &addr) -> bool {
+                if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word))
+                    return false;
+                addr = ring_addr + stage * C::kTileBytes;
+                return true;
+            };
+            auto advance = [&]() {
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+
+            do {
+                if (!ptx::mbar_wait(bar.q_full, 0, abort_flag, p.err_word)) {
+                    aborted = true;
+                    break;
+                }
+                uint32_t k_addr;
+                if (!next_stage(k_addr)) {
+                    aborted = true;
+                    break;
+                }
+                int k_stage = stage;
+                advance();
+                ptx::tc_fence_after_sync();
+                issue_qk(0, k_addr);
+                if (n1 > 0)
+                    issue_qk(1, k_addr);
+                ptx::mma_commit(&bar.kv_empty[k_stage]);
+
+                for (int j = 0; j < n_max; ++j) {
+                    uint32_t v_addr;
+                    if (!next_stage(v_addr)) {
+                        aborted = true;
+                        break;
+                    }
+                    const int v_stage = stage;
+                    advance();
+                    if (j < n0) {
+                        if (!ptx::mbar_wait(&bar.p_full[0], uint32_t(j) & 1u, abort_flag,
+                                            p.err_word)) {
+                            aborted = true;
+                            break;
+                        }
+                        ptx::tc_fence_after_sync();
+                        issue_pv(0, v_addr, j > 0);
+                        if (j == n0 - 1)
+                            ptx::mma_commit(&bar.o_full[0]);
+                    }
+                    const bool more = j + 1 < n_max;
+                    if (more) {
+                        if (!next_stage(k_addr)) {
+                            aborted = true;
+                            break;
+                        }
+                        k_stage = stage;
+                        advance();
+                        ptx::tc_fence_after_sync();
+                        if (j + 1 < n0)
+                            issue_qk(0, k_addr);
+                    }
+                    if (j < n1) {
+                        if (!ptx::mbar_wait(&bar.p_full[1], uint32_t(j) & 1u, abort_flag,
+                                            p.err_word)) {
+                            aborted = true;
+                            break;
+                        }
+                        ptx::tc_fence_after_sync();
+                        issue_pv(1, v_addr, j > 0);
+                        if (j == n1 - 1)
+                            ptx::mma_commit(&bar.o_full[1]);
+                    }
+                    ptx::mma_commit(&bar.kv_empty[v_stage]);
+                    if (more) {
+                        if (j + 1 < n1)
+                            issue_qk(1, k_addr);
+                        ptx::mma_commit(&bar.kv_empty[k_stage]);
+                    }
+                }
+            } while (false);
+            // Every MMA issued above has completed (and every commit has arrived)
+            // once this last commit arrives.
+            ptx::mma_commit(bar.drain);
+            drain_wait(bar.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ======================= softmax warpgroups ========================
+        const int t = warp >> 2;                       // 0: Q0, 1: Q1
+        const int r = threadIdx.x & 127;               // row in the Q tile = TMEM lane
+        const int n_t = t == 0 ? n0 : n1;
+        const int qt = qt0 + t;
+        const int i = qt * BM + r;                     // query position in the sequence
+        const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_bits + col_s(t);
+        const uint32_t tO = tmem + lane_bits + col_o<D>(t);
+        const float sl = p.scale_log2;
+        float m = -INFINITY;                           // running max, log2 units
+        float l = 0.f;                                 // running sum
+
+        for (int j = 0; j < n_t; ++j) {
+            if (!ptx::mbar_wait(&bar.s_full[t], uint32_t(j) & 1u, abort_flag, p.err_word)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld32(tS + c * 32, sr[c]);
+            ptx::tmem_wait_ld();
+
+            // mask: causal diagonal tile and the tile holding the sequence end
+            const bool diag = p.causal && j == qt;
+            const bool tail = (j + 1) * BN > L;
+            if (diag || tail) {
+                const int lim_causal = diag ? i - j * BN : BN - 1;  // last visible column
+                const int lim_len = L - 1 - j * BN;
+                const int lim = lim_causal < lim_len ? lim_causal : lim_len;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c * 32 + e > lim)
+                            sr[c][e] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+            const float m_new = fmaxf(m, mx * sl);
+            const bool grew = m_new > m;
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float corr = grew ? ptx::ex2(m - m_use) : 1.f;
+
+            // P = exp2(s * sl - m) in bf16 over columns 64..127 of S_t
+            float rowsum = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int col = half * 64 + 2 * e;
+                    const float p0 =
+                        ptx::ex2(fmaf(__uint_as_float(sr[col >> 5][col & 31]), sl, -m_use));
+                    const float p1 = ptx::ex2(
+                        fmaf(__uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]), sl, -m_use));
+                    rowsum += p0 + p1;
+                    pk[e] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st32(tS + kColPinS + half * 32, pk);
+            }
+            l = l * corr + rowsum;
+            m = m_new;
+
+            // rescale this row of O~ when the maximum grew (never on the first
+            // tile: the first P V overwrites O)
+            if (j > 0 && __any_sync(0xffffffffu, grew)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                    ptx::tmem_st32(tO + c * 32, o);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(&bar.p_full[t]);
+        }
+
+        // ---- epilogue: O = O~ / l (bf16), lse = (m + log2 l) * ln 2 -----------
+        if (!aborted && n_t > 0) {
+            if (ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word)) {
+                ptx::tc_fence_after_sync();
+                const float inv = 1.f / l;
+                const bool row_ok = i < L;
+                __nv_bfloat16 *orow = p.O + ((start + i) * p.H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tO + c * 32, o);
+                    ptx::tmem_wait_ld();
+                    if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
+                                                   __uint_as_float(o[8 * q + 1]) * inv);
+                            w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
+                                                   __uint_as_float(o[8 * q + 3]) * inv);
+                            w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
+                                                   __uint_as_float(o[8 * q + 5]) * inv);
+                            w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
+                                                   __uint_as_float(o[8 * q + 7]) * inv);
+                            dst[q] = w;
+                        }
+                    }
+                }
+                if (row_ok) {
+                    const float lse = (m + log2f(l)) * kLn2;
+                    if (p.cu_seqlens != nullptr)
+                        p.lse[int64_t(h) * p.total + start + i] = lse;
+                    else
+                        p.lse[(int64_t(b) * p.H + h) * p.N + i] = lse;
+                }
+            }
+        }
+    }
+
+    // ---- teardown ------------------------------------------------------------
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    if (warp == kWarpMma)
+        ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 3-D map over a [total, H, d] bf16 tensor; box = 64 head-dim elements (128
+// bytes, the 128-byte swizzle span) x 1 head x 128 tokens.  Rows past `total`
+// read as zero.
+bool make_tmap(CUtensorMap *tm, const void *base, int64_t total, int H, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(total)};
+    const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(H) * d * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
+{
+    auto kern = attn_fwd_bf16_kernel<D>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(Cfg<D>::kSmemBytes));
+    });
+    if (attr_err != cudaSuccess)
+        return FA_ERR_CUDA;
+    kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
+{
+    Bf16Params p;
+    if (!make_tmap(&p.tm_q, a.Q, a.total, a.H, a.d) || !make_tmap(&p.tm_k, a.K, a.total, a.H, a.d) ||
+        !make_tmap(&p.tm_v, a.V, a.total, a.H, a.d))
+        return FA_ERR_CUDA;
+    p.O = static_cast<__nv_bfloat16 *>(a.O);
+    p.lse = a.lse;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    const int n_qt = (a.N + BM - 1) / BM;
+    p.n_pairs = (n_qt + 1) / 2;
+    p.total = a.total;
+    p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
+    p.causal = a.causal;
+    p.cu_seqlens = a.cu_seqlens;
+    p.err_word = a.err_word;
+    const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H;
+    if (blocks == 0)
+        return FA_OK;
+    if (blocks > 0x7fffffffLL)
+        return FA_ERR_TOO_LARGE;
+    return a.d == 64 ? launch_d<64>(p, blocks, stream) : launch_d<128>(p, blocks, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,219 @@
+// fa_api.cu -- the extern "C" boundary of libfa.so (declared in include/fa.h):
+// argument validation, stream selection, the device error word, and dispatch
+// to the kernels' launchers.  No computation happens here.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "launch.h"
+
+namespace fa {
+
+// One copy per device that loads the library; kernels receive its address.
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local cudaStream_t t_stream = nullptr;
+
+struct DeviceInfo {
+    std::once_flag once;
+    int ok = 0;            // 1: compute capability 10.3 (sm_103)
+    int *err_word = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device set-up, done once with that device current.
+DeviceInfo *current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    DeviceInfo *info = &g_dev[dev];
+    std::call_once(info->once, [info, dev] {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess)
+            return;
+        info->err_word = static_cast<int *>(addr);
+        info->ok = (major == 10 && minor == 3) ? 1 : 0;
+    });
+    return info->ok ? info : nullptr;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared validation of the attention arguments; fills `a` on success.
+int check_attention(const void *Q, const void *K, const void *V, void *O, float *lse, int B, int H,
+                    int N, int d, int causal, const int32_t *cu_seqlens, int64_t total,
+                    bool bf16, AttnArgs *a)
+{
+    if (B < 0 || H < 0 || N < 0 || total < 0)
+        return FA_ERR_BAD_SIZE;
+    if (bf16 ? (d != 64 && d != 128) : (d < 1 || d > 128))
+        return FA_ERR_UNSUPPORTED;
+    if (!Q || !K || !V || !O || !lse)
+        return FA_ERR_NULL_POINTER;
+    const uintptr_t al = bf16 ? 16 : 4;
+    if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) ||
+        !aligned(lse, 4))
+        return FA_ERR_MISALIGNED;
+    if (cu_seqlens && !aligned(cu_seqlens, 4))
+        return FA_ERR_MISALIGNED;
+    // TMA coordinates and the kernels' row indices are 32-bit.
+    if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512)
+        return FA_ERR_TOO_LARGE;
+    if (total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+        return FA_ERR_TOO_LARGE;
+    a->Q = Q;
+    a->K = K;
+    a->V = V;
+    a->O = O;
+    a->lse = lse;
+    a->B = B;
+    a->H = H;
+    a->N = N;
+    a->d = d;
+    a->total = total;
+    a->causal = causal ? 1 : 0;
+    a->cu_seqlens = cu_seqlens;
+    return FA_OK;
+}
+
+// total = cu_seqlens[B], read back on the library stream (synchronises it).
+int read_total(const int32_t *cu_seqlens, int B, int64_t *total)
+{
+    int32_t t = 0;
+    if (cudaMemcpyAsync(&t, cu_seqlens + B, sizeof(t), cudaMemcpyDeviceToHost, t_stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(t_stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (t < 0)
+        return FA_ERR_BAD_SIZE;
+    *total = t;
+    return FA_OK;
+}
+
+int attention_common(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                     int H, int N, int64_t total, bool total_known, int d, float scale,
+                     int causal, const int32_t *cu_seqlens, bool bf16)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (B == 0 || H == 0 || N == 0)
+        return FA_OK;
+    DeviceInfo *dev = current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    if (cu_seqlens == nullptr) {
+        total = int64_t(B) * N;
+    } else if (!total_known) {
+        if (!aligned(cu_seqlens, 4))
+            return FA_ERR_MISALIGNED;
+        const int rc = read_total(cu_seqlens, B, &total);
+        if (rc != FA_OK)
+            return rc;
+    }
+    AttnArgs a;
+    const int rc = check_attention(Q, K, V, O, lse, B, H, N, d, causal, cu_seqlens, total, bf16, &a);
+    if (rc != FA_OK)
+        return rc;
+    if (total == 0)
+        return FA_OK;
+    a.scale = scale;
+    a.err_word = dev->err_word;
+    return bf16 ? launch_attention_bf16(a, t_stream) : launch_attention_f32(a, t_stream);
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_softmax_rows(const float *x, float *y, int64_t rows, int64_t N)
+{
+    if (rows < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (rows == 0 || N == 0)
+        return FA_OK;
+    if (rows > (int64_t(1) << 62) / N)
+        return FA_ERR_TOO_LARGE;
+    if (!x || !y)
+        return FA_ERR_NULL_POINTER;
+    if (!fa::aligned(x, 4) || !fa::aligned(y, 4))
+        return FA_ERR_MISALIGNED;
+    if (fa::current_device() == nullptr)
+        return FA_ERR_NO_DEVICE;
+    return fa::launch_softmax_rows(x, y, rows, N, fa::t_stream);
+}
+
+int fa_attention_fwd(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                     int H, int N, int d, float scale, int causal, const int32_t *cu_seqlens)
+{
+    return fa::attention_common(Q, K, V, O, lse, B, H, N, 0, false, d, scale, causal, cu_seqlens,
+                                true);
+}
+
+int fa_attention_fwd_varlen(const void *Q, const void *K, const void *V, void *O, float *lse,
+                            int B, int H, int N, int64_t total, int d, float scale, int causal,
+                            const int32_t *cu_seqlens)
+{
+    if (cu_seqlens == nullptr)
+        return FA_ERR_NULL_POINTER;
+    return fa::attention_common(Q, K, V, O, lse, B, H, N, total, true, d, scale, causal,
+                                cu_seqlens, true);
+}
+
+int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         const int32_t *cu_seqlens)
+{
+    return fa::attention_common(Q, K, V, O, lse, B, H, N, 0, false, d, scale, causal, cu_seqlens,
+                                false);
+}
+
+int fa_set_stream(void *stream)
+{
+    fa::t_stream = static_cast<cudaStream_t>(stream);
+    return FA_OK;
+}
+
+void *fa_get_stream(void) { return fa::t_stream; }
+
+int fa_get_device_error(void)
+{
+    if (fa::current_device() == nullptr)
+        return FA_ERR_NO_DEVICE;
+    int v = 0;
+    const int zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&v, fa::g_device_error, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(fa::g_device_error, &zero, sizeof(zero)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return v;
+}
+
+const char *fa_strerror(int code)
+{
+    switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case FA_ERR_BAD_SIZE: return "a size is negative or inconsistent";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or option";
+    case FA_ERR_MISALIGNED: return "a pointer breaks the alignment rule";
+    case FA_ERR_CUDA: return "a CUDA call failed";
+    case FA_ERR_TOO_LARGE: return "a size exceeds what the kernels can index";
+    case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown error code";
+    }
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

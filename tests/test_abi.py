@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads and exports what include/fa.h declares (no GPU).
+
+Also checks the host-side argument validation that returns before any CUDA
+call (negative sizes, empty work).  No kernel is launched here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import online_softmax_06_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.lib()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_f32",
+                     "fa_attention_fwd_varlen", "fa_set_stream", "fa_get_device_error",
+                     "fa_strerror"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_only_the_boundary_is_exported():
+    # -fvisibility=hidden: the kernels' host launchers stay internal
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {s for s in exported if s.startswith("fa_")}
+    assert ours == set(declared_functions())
+
+
+def test_version_and_strerror(lib):
+    assert fa.fa_version() >= 100
+    assert fa.strerror(0) == "success"
+    assert "NULL" in fa.strerror(-1)
+    assert fa.strerror(12345) == "unknown error code"
+
+
+def test_host_validation_without_gpu(lib):
+    # these return before any CUDA call
+    assert fa.fa_softmax_rows(None, None, -1, 4) == -2
+    assert fa.fa_softmax_rows(None, None, 0, 4) == 0
+    assert fa.fa_softmax_rows(None, None, 4, 0) == 0
+    assert fa.fa_attention_fwd(None, None, None, None, None, -1, 1, 1, 64, 1.0, 0, None) == -2
+    assert fa.fa_attention_fwd(None, None, None, None, None, 0, 1, 1, 64, 1.0, 0, None) == 0
+    assert fa.fa_attention_fwd_varlen(None, None, None, None, None, 1, 1, 1, 1, 64, 1.0, 0,
+                                      None) == -1
+    assert fa.fa_attention_fwd_f32(None, None, None, None, None, 1, -1, 1, 64, 1.0, 0, None) == -2
+
+
+def test_stream_setting_is_per_thread(lib):
+    import threading
+    fa.fa_set_stream(ctypes.c_void_p(0x1234))
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(fa.fa_get_stream()))
+    t.start()
+    t.join()
+    assert fa.fa_get_stream() == 0x1234
+    assert seen == [None]
+    fa.fa_set_stream(None)
+    assert fa.fa_get_stream() is None
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="CPU-only check")
+def test_no_device_is_reported(lib):
+    # valid-looking sizes with no GPU present: the library refuses before launching
+    assert fa.fa_softmax_rows(ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 4) == -7

@@ -163,3 +163,36 @@ WORKLOADS = {
 def softmax_workload(N: int, rows: int = SOFTMAX_ROWS, seed: int = SOFTMAX_SEED) -> np.ndarray:
     """The row-softmax input for one row length (a distinct stream per N)."""
     return softmax_rows_input(rows, N, seed * 100003 + N)
+
+
+def rising_scores_inputs(B: int, N: int, H: int, d: int, seed: int, growth: float = 0.05):
+    """Q, K, V (bf16, [B, N, H, d]) whose scores rise along the key index.
+
+    Every query is a fixed direction u (plus small noise) and key j is
+    (growth * j) * u plus noise, so each query's largest score sits at the last
+    key it can see and its running maximum grows on every key tile: the
+    rescale path runs on every tile.  The last key of each sequence is
+    additionally scaled up by 4 so the final tile carries a large jump.
+    """
+    rng = rng_for(seed)
+    u = normal_f32(rng, (1, 1, H, d))
+    u /= np.linalg.norm(u, axis=-1, keepdims=True)
+    q = (u * np.float32(4.0) + normal_f32(rng, (B, N, H, d), 0.05)).astype(np.float32)
+    steps = (np.arange(N, dtype=np.float32) * np.float32(growth)).reshape(1, N, 1, 1)
+    k = (u * steps + normal_f32(rng, (B, N, H, d), 0.05)).astype(np.float32)
+    k[:, -1] *= np.float32(4.0)
+    v = normal_f32(rng, (B, N, H, d))
+    return to_bf16(q), to_bf16(k), to_bf16(v)
+
+
+def sample_rows(total: int, H: int, n: int, seed: int, must_tokens=()):
+    """(token, head) pairs to check one by one: n random pairs plus every head of
+    the listed tokens."""
+    rng = rng_for(seed)
+    tok = rng.integers(0, total, size=n)
+    head = rng.integers(0, H, size=n)
+    extra = np.asarray(list(must_tokens), dtype=np.int64)
+    if extra.size:
+        tok = np.concatenate([tok, np.repeat(extra, H)])
+        head = np.concatenate([head, np.tile(np.arange(H), extra.size)])
+    return tok.astype(np.int64), head.astype(np.int64)
