@@ -57,6 +57,7 @@ constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColPinS = 64;    // P_t starts 64 columns into S_t
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kRescaleLog2 = 8.f;  // move the reference max only past 2^8
 
 // TMEM column of S_t and of O_t (t = 0, 1) for head dimension D.
 __device__ __forceinline__ uint32_t col_s(int t) { return uint32_t(t) * 128u; }
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_bits + col_s(t);
         const uint32_t tO = tmem + lane_bits + col_o<D>(t);
         const float sl = p.scale_log2;
-        float m = -INFINITY;                           // running max, log2 units
+        float m = -INFINITY;                           // reference max, log2 units
         float l = 0.f;                                 // running sum
 
         for (int j = 0; j < n_t; ++j) {
@@ -398,12 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     mx = fmaxf(mx, __uint_as_float(sr[c][e]));
-            const float m_new = fmaxf(m, mx * sl);
-            const bool grew = m_new > m;
+            // Conditional rescale (booklet §5.4): the row keeps a reference
+            // maximum m and moves it only when the tile maximum exceeds it by
+            // more than kRescaleLog2, so every p stays <= 2^kRescaleLog2 (far
+            // from overflow) while o~ is rescaled only on rare tiles.  o~ and l
+            // share the reference, so it cancels in o~ / l and in
+            // lse = m + log2 l: the result is exact for any reference.
+            const float mt = mx * sl;
+            const bool grew = mt > m + kRescaleLog2;
+            const float m_new = grew ? mt : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float corr = grew ? ptx::ex2(m - m_use) : 1.f;
+            const float corr = grew ? ptx::ex2(m - m_use) : 1.f;   // 0 on the first tile
 
-            // P = exp2(s * sl - m) in bf16 over columns 64..127 of S_t
+            // P = exp2(s * sl - m) in bf16 over columns 64..127 of S_t; the
+            // exponent arguments are formed two at a time (packed fp32x2 FMA)
+            const float2 sl2 = make_float2(sl, sl);
+            const float2 nm2 = make_float2(-m_use, -m_use);
             float rowsum = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -411,10 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int col = half * 64 + 2 * e;
-                    const float p0 =
-                        ptx::ex2(fmaf(__uint_as_float(sr[col >> 5][col & 31]), sl, -m_use));
-                    const float p1 = ptx::ex2(
-                        fmaf(__uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]), sl, -m_use));
+                    const float2 sv = make_float2(__uint_as_float(sr[col >> 5][col & 31]),
+                                                  __uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]));
+                    const float2 arg = __ffma2_rn(sv, sl2, nm2);
+                    const float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
                     rowsum += p0 + p1;
                     pk[e] = ptx::pack_bf16x2(p0, p1);
                 }
@@ -423,8 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             l = l * corr + rowsum;
             m = m_new;
 
-            // rescale this row of O~ when the maximum grew (never on the first
-            // tile: the first P V overwrites O)
+            // rescale this row of O~ when its reference moved (never on the
+            // first tile: the first P V overwrites O); the warp goes together,
+            // lanes whose reference did not move multiply by exactly 1
             if (j > 0 && __any_sync(0xffffffffu, grew)) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {

@@ -309,9 +309,9 @@ cudaError_t dispatch(const float *x, float *y, int64_t rows, int64_t N, cudaStre
     if (N <= 4096)   return launch_resident<256, 4, 256, 1, VEC>(x, y, rows, N, stream);
     if (N <= 8192)   return launch_resident<512, 4, 512, 1, VEC>(x, y, rows, N, stream);
     if (N <= 16384)  return launch_resident<512, 8, 512, 1, VEC>(x, y, rows, N, stream);
-    if (N <= 32768)  return launch_resident<256, 8, 256, 4, VEC>(x, y, rows, N, stream);
-    if (N <= 65536)  return launch_resident<512, 8, 512, 4, VEC>(x, y, rows, N, stream);
-    if (N <= 131072) return launch_resident<512, 8, 512, 8, VEC>(x, y, rows, N, stream);
+    if (N <= 32768)  return launch_resident<1024, 8, 1024, 1, VEC>(x, y, rows, N, stream);
+    if (N <= 65536)  return launch_resident<1024, 8, 1024, 2, VEC>(x, y, rows, N, stream);
+    if (N <= 131072) return launch_resident<1024, 8, 1024, 4, VEC>(x, y, rows, N, stream);
     if (rows > 0x7fffffffLL)
         return cudaErrorInvalidConfiguration;
     softmax_rows_twopass_kernel<1024><<<dim3(unsigned(rows)), dim3(1024), 0, stream>>>(x, y, rows,
