@@ -242,34 +242,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, true);
             constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
             constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kChunkBytes, 1024);
-            const uint32_t q_addr[2] = {ptx::smem_u32(q_smem[0]), ptx::smem_u32(q_smem[1])};
+            // A descriptor built for a tile's base address is advanced to a
+            // sub-block by adding (byte offset >> 4) to it: the start-address
+            // field sits in the low 14 bits and every shared-memory address
+            // here is below 256 KB, so the add never carries out of the field.
+            const uint64_t dq0 = ptx::smem_desc(desc_kmajor, ptx::smem_u32(q_smem[0]));
+            const uint64_t dq1 = ptx::smem_desc(desc_kmajor, ptx::smem_u32(q_smem[1]));
             const uint32_t ring_addr = ptx::smem_u32(ring);
 
-            auto issue_qk = [&](int t, uint32_t k_addr) {
+            auto issue_qk = [&](int t, uint64_t dk) {
+                const uint64_t dq = t == 0 ? dq0 : dq1;
+                const uint32_t ts = tmem + col_s(t);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + col_s(t), ptx::smem_desc(desc_kmajor, q_addr[t] + off),
-                                ptx::smem_desc(desc_kmajor, k_addr + off), idesc_qk,
-                                kk > 0 ? 1u : 0u);
+                    const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_ss(ts, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(&bar.s_full[t]);
             };
-            auto issue_pv = [&](int t, uint32_t v_addr, bool accumulate) {
+            auto issue_pv = [&](int t, uint64_t dv, bool accumulate) {
+                const uint32_t to = tmem + col_o<D>(t);
+                const uint32_t tp = tmem + col_s(t) + kColPinS;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    ptx::mma_ts(tmem + col_o<D>(t), tmem + col_s(t) + kColPinS + kk * 8,
-                                ptx::smem_desc(desc_mnmajor, v_addr + kk * 16 * 128), idesc_pv,
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts(to, tp + kk * 8, dv + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
                                 (accumulate || kk > 0) ? 1u : 0u);
-                }
             };
 
             int stage = 0;
             uint32_t phase = 0;
-            auto next_stage = [&](uint32_t &addr) -> bool {
+            // waits for the next ring stage; returns its K-major and MN-major
+            // descriptors (the stage holds a K tile or a V tile)
+            auto next_stage = [&](uint64_t &dk, uint64_t &dv) -> bool {
                 if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word))
                     return false;
-                addr = ring_addr + stage * C::kTileBytes;
+                const uint32_t addr = ring_addr + stage * C::kTileBytes;
+                dk = ptx::smem_desc(desc_kmajor, addr);
+                dv = ptx::smem_desc(desc_mnmajor, addr);
                 return true;
             };
             auto advance = [&]() {
@@ -284,22 +293,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aborted = true;
                     break;
                 }
-                uint32_t k_addr;
-                if (!next_stage(k_addr)) {
+                uint64_t k_desc, unused;
+                if (!next_stage(k_desc, unused)) {
                     aborted = true;
                     break;
                 }
                 int k_stage = stage;
                 advance();
                 ptx::tc_fence_after_sync();
-                issue_qk(0, k_addr);
+                issue_qk(0, k_desc);
                 if (n1 > 0)
-                    issue_qk(1, k_addr);
+                    issue_qk(1, k_desc);
                 ptx::mma_commit(&bar.kv_empty[k_stage]);
 
                 for (int j = 0; j < n_max; ++j) {
-                    uint32_t v_addr;
-                    if (!next_stage(v_addr)) {
+                    uint64_t v_desc;
+                    if (!next_stage(unused, v_desc)) {
                         aborted = true;
                         break;
                     }
@@ -312,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ptx::tc_fence_after_sync();
-                        issue_pv(0, v_addr, j > 0);
+                        issue_pv(0, v_desc, j > 0);
                         if (j == n0 - 1)
                             ptx::mma_commit(&bar.o_full[0]);
                     }
                     const bool more = j + 1 < n_max;
                     if (more) {
-                        if (!next_stage(k_addr)) {
+                        if (!next_stage(k_desc, unused)) {
                             aborted = true;
                             break;
                         }
@@ -326,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         advance();
                         ptx::tc_fence_after_sync();
                         if (j + 1 < n0)
-                            issue_qk(0, k_addr);
+                            issue_qk(0, k_desc);
                     }
                     if (j < n1) {
                         if (!ptx::mbar_wait(&bar.p_full[1], uint32_t(j) & 1u, abort_flag,
@@ -335,14 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         ptx::tc_fence_after_sync();
-                        issue_pv(1, v_addr, j > 0);
+                        issue_pv(1, v_desc, j > 0);
                         if (j == n1 - 1)
                             ptx::mma_commit(&bar.o_full[1]);
                     }
                     ptx::mma_commit(&bar.kv_empty[v_stage]);
                     if (more) {
                         if (j + 1 < n1)
-                            issue_qk(1, k_addr);
+                            issue_qk(1, k_desc);
                         ptx::mma_commit(&bar.kv_empty[k_stage]);
                     }
                 }
