@@ -70,6 +70,9 @@ def _bind(lib):
     lib.oracle_attention_fwd_online.argtypes = [vp, vp, vp, vp, vp, c_i64, c_i64, c_i64,
                                                 c_dbl, c_int, vp, c_i64]
     lib.oracle_attention_fwd_online.restype = None
+    lib.oracle_attention_qk.argtypes = [vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_dbl,
+                                        c_int, vp, vp, vp, c_i64, vp, vp]
+    lib.oracle_attention_qk.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
     return lib
@@ -192,6 +195,42 @@ def attention_rows(Q, K, V, cu_seqlens, scale, causal, tok, head, lib=None):
     (lib or load()).oracle_attention_rows(_ptr(Q), _ptr(K), _ptr(V), B, H, d, float(scale),
                                           int(bool(causal)), _ptr(cu), _ptr(tok), _ptr(head),
                                           n, _ptr(O), _ptr(lse))
+    return O, lse
+
+
+def attention_qk(Q, K, V, scale, causal, samples=None, lib=None):
+    """Attention with separate query / key lengths on dense batches.
+
+    Q: [B, Nq, H, d]; K, V: [B, Nk, H, d]; causal is bottom-right aligned
+    (query i sees keys j <= i + Nk - Nq).  Without ``samples`` returns
+    (O [B, Nq, H, d] f64, lse [B, H, Nq] f64); with ``samples`` = (b, i, h)
+    index arrays returns (O_rows [n, d], lse_rows [n]).
+    """
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    B, Nq, H, d = Q.shape
+    Nk = K.shape[1]
+    if K.shape != (B, Nk, H, d) or V.shape != K.shape:
+        raise ValueError("K and V must be [B, Nk, H, d] with Q's B, H, d")
+    lib = lib or load()
+    if samples is None:
+        n = B * Nq * H
+        O = np.zeros((n, d), dtype=np.float64)
+        lse = np.zeros(n, dtype=np.float64)
+        lib.oracle_attention_qk(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d, float(scale),
+                                int(bool(causal)), None, None, None, n, _ptr(O), _ptr(lse))
+        return O.reshape(B, Nq, H, d), lse.reshape(B, Nq, H).transpose(0, 2, 1).copy()
+    sb, si, sh = (np.ascontiguousarray(np.asarray(a, dtype=np.int64)) for a in samples)
+    if not (sb.shape == si.shape == sh.shape):
+        raise ValueError("sample arrays must have one shape")
+    if sb.size and (sb.min() < 0 or sb.max() >= B or si.min() < 0 or si.max() >= Nq
+                    or sh.min() < 0 or sh.max() >= H):
+        raise ValueError("sample index out of range")
+    n = sb.size
+    O = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    lib.oracle_attention_qk(_ptr(Q), _ptr(K), _ptr(V), B, H, Nq, Nk, d, float(scale),
+                            int(bool(causal)), _ptr(sb), _ptr(si), _ptr(sh), n, _ptr(O),
+                            _ptr(lse))
     return O, lse
 
 

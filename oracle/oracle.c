@@ -312,6 +312,70 @@ void oracle_attention_fwd_online(const float *Q, const float *K, const float *V,
     }
 }
 
+/*
+ * Attention with separate query and key lengths (dense batches), the form used
+ * when the keys of a query block are processed in several splits:
+ *   Q, O: [B, Nq, H, d];  K, V: [B, Nk, H, d];  lse: [B, H, Nq].
+ * Same definition as attention_row; when causal, query i sees the keys
+ * j <= i + (Nk - Nq): the queries are the last Nq positions of a sequence of
+ * Nk keys (bottom-right alignment; with Nq == Nk this is [L22] §三十四's j <= i).
+ * Rows are evaluated only for the n sampled (b, i, h) triples given (all rows
+ * when samp_b == NULL, in which case n must be B * Nq * H).
+ */
+void oracle_attention_qk(const float *Q, const float *K, const float *V, int64_t B, int64_t H,
+                         int64_t Nq, int64_t Nk, int64_t d, double scale, int causal,
+                         const int64_t *samp_b, const int64_t *samp_i, const int64_t *samp_h,
+                         int64_t n, double *O_rows, double *lse_rows)
+{
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(Nk > 0 ? Nk : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n; ++r) {
+            int64_t b, i, h;
+            if (samp_b != NULL) {
+                b = samp_b[r];
+                i = samp_i[r];
+                h = samp_h[r];
+            } else {
+                b = r / (Nq * H);
+                i = (r / H) % Nq;
+                h = r % H;
+            }
+            const float *q = Q + ((b * Nq + i) * H + h) * d;
+            int64_t nvis = causal ? i + (Nk - Nq) + 1 : Nk;
+            if (nvis > Nk)
+                nvis = Nk;
+            if (nvis < 0)
+                nvis = 0;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nvis; ++j) {
+                const float *k = K + ((b * Nk + j) * H + h) * d;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += (double)q[c] * (double)k[c];
+                s[j] = scale * dot;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nvis; ++j)
+                l += exp(s[j] - m);
+            double *o = O_rows + r * d;
+            for (int64_t c = 0; c < d; ++c)
+                o[c] = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double p = exp(s[j] - m) / l;
+                const float *v = V + ((b * Nk + j) * H + h) * d;
+                for (int64_t c = 0; c < d; ++c)
+                    o[c] += p * (double)v[c];
+            }
+            lse_rows[r] = nvis > 0 ? m + log(l) : -INFINITY;
+        }
+        free(s);
+    }
+}
+
 /* Threads the OpenMP runtime will use for the parallel loops above. */
 int oracle_num_threads(void)
 {

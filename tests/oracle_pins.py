@@ -312,4 +312,97 @@ def pin_attention_brute_force_tiny(lib):
                 _close(lse[b, h], np.log(np.exp(S).sum(axis=1)), 1e-13, "brute-force lse")
 
 
+# --------------------------------------------------------------------------
+# Attention with separate query / key lengths (bottom-right causal)
+# --------------------------------------------------------------------------
+
+def _bottom_right_mask(Nq, Nk):
+    """True where query i may see key j: j <= i + Nk - Nq."""
+    i = np.arange(Nq)[:, None]
+    j = np.arange(Nk)[None, :]
+    return j <= i + (Nk - Nq)
+
+
+def pin_attention_qk_vs_torch_sdpa(lib):
+    import torch
+    import torch.nn.functional as F
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(20)
+    for (B, Nq, Nk, H, d, causal) in [(2, 3, 11, 2, 8, True), (1, 7, 7, 3, 4, True),
+                                      (2, 4, 9, 1, 16, False), (1, 1, 13, 2, 8, True)]:
+        Q = rng.standard_normal((B, Nq, H, d)).astype(np.float32)
+        K = rng.standard_normal((B, Nk, H, d)).astype(np.float32)
+        V = rng.standard_normal((B, Nk, H, d)).astype(np.float32)
+        scale = 1 / math.sqrt(d)
+        O, lse = oracle.attention_qk(Q, K, V, scale, causal, lib=lib)
+        q, k, v = (torch.from_numpy(X.astype(np.float64)).permute(0, 2, 1, 3) for X in (Q, K, V))
+        mask = torch.from_numpy(_bottom_right_mask(Nq, Nk)) if causal else None
+        ref = F.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale)
+        _close(O, ref.permute(0, 2, 1, 3).numpy(), 1e-12, f"qk sdpa Nq{Nq} Nk{Nk} causal={causal}")
+        S = np.einsum("bihc,bjhc->bhij", Q.astype(np.float64), K.astype(np.float64)) * scale
+        if causal:
+            S = np.where(_bottom_right_mask(Nq, Nk), S, -np.inf)
+        _close(lse, logsumexp(S, axis=-1), 1e-12, "qk lse vs scipy logsumexp")
+
+
+def pin_attention_qk_uniform_scores(lib):
+    rng = np.random.default_rng(21)
+    B, Nq, Nk, H, d = 2, 4, 10, 2, 6
+    Q = np.zeros((B, Nq, H, d), np.float32)
+    K = rng.standard_normal((B, Nk, H, d)).astype(np.float32)
+    V = rng.standard_normal((B, Nk, H, d)).astype(np.float32)
+    O, lse = oracle.attention_qk(Q, K, V, 0.3, True, lib=lib)
+    for i in range(Nq):
+        n = i + (Nk - Nq) + 1
+        _close(O[:, i], V[:, :n].astype(np.float64).mean(axis=1), 1e-14, "qk uniform O")
+        _close(lse[:, :, i], np.full((B, H), math.log(n)), 1e-14, "qk uniform lse")
+
+
+def pin_attention_qk_causal_ignores_future(lib):
+    rng = np.random.default_rng(22)
+    B, Nq, Nk, H, d = 1, 5, 12, 2, 4
+    Q, K, V = (rng.standard_normal(s).astype(np.float32)
+               for s in ((B, Nq, H, d), (B, Nk, H, d), (B, Nk, H, d)))
+    O, lse = oracle.attention_qk(Q, K, V, 0.5, True, lib=lib)
+    for i in range(Nq):
+        last = i + (Nk - Nq)                       # last visible key
+        K2, V2 = K.copy(), V.copy()
+        K2[:, last + 1:] = 9.0
+        V2[:, last + 1:] = -9.0
+        O2, lse2 = oracle.attention_qk(Q, K2, V2, 0.5, True, lib=lib)
+        _close(O2[:, :i + 1], O[:, :i + 1], 0.0, "qk causal rows changed")
+        _close(lse2[:, :, :i + 1], lse[:, :, :i + 1], 0.0, "qk causal lse changed")
+        if last + 1 < Nk:
+            K3 = K.copy()
+            K3[:, last] = 9.0                      # the last visible key does matter
+            O3, _ = oracle.attention_qk(Q, K3, V, 0.5, True, lib=lib)
+            if np.allclose(O3[:, i], O[:, i]):
+                raise AssertionError("last visible key ignored")
+
+
+def pin_attention_qk_square_matches_packed(lib):
+    """With Nq == Nk the bottom-right and top-left alignments coincide."""
+    rng = np.random.default_rng(23)
+    B, N, H, d = 2, 9, 2, 5
+    Q, K, V = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(3))
+    for causal in (False, True):
+        O, lse = oracle.attention_qk(Q, K, V, 0.4, causal, lib=lib)
+        ref = _sdpa(Q, K, V, 0.4, causal)
+        _close(O, ref, 1e-12, f"qk square causal={causal}")
+
+
+def pin_attention_qk_samples(lib):
+    rng = np.random.default_rng(24)
+    B, Nq, Nk, H, d = 2, 6, 15, 3, 4
+    Q, K, V = (rng.standard_normal(s).astype(np.float32)
+               for s in ((B, Nq, H, d), (B, Nk, H, d), (B, Nk, H, d)))
+    O, lse = oracle.attention_qk(Q, K, V, 0.5, True, lib=lib)
+    sb = rng.integers(0, B, 30)
+    si = rng.integers(0, Nq, 30)
+    sh = rng.integers(0, H, 30)
+    Or, lr = oracle.attention_qk(Q, K, V, 0.5, True, samples=(sb, si, sh), lib=lib)
+    _close(Or, O[sb, si, sh], 0.0, "qk sampled O")
+    _close(lr, lse[sb, sh, si], 0.0, "qk sampled lse")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -41,6 +41,10 @@ MUTANTS = [
     ("online_no_correction", "                l *= corr;\n", "", 0),
     ("online_acc_no_correction", "                    acc[c] *= corr;\n", "", 0),
     ("rows_wrong_lse_slot", "O_rows + r * d, lse_rows + r);", "O_rows + r * d, lse_rows + (r > 0 ? r - 1 : 0));", 0),
+    ("qk_top_left_causal", "int64_t nvis = causal ? i + (Nk - Nq) + 1 : Nk;", "int64_t nvis = causal ? i + 1 : Nk;", 0),
+    ("qk_offset_sign", "int64_t nvis = causal ? i + (Nk - Nq) + 1 : Nk;", "int64_t nvis = causal ? i + (Nq - Nk) + 1 : Nk;", 0),
+    ("qk_key_stride_uses_nq", "const float *k = K + ((b * Nk + j) * H + h) * d;", "const float *k = K + ((b * Nq + j) * H + h) * d;", 0),
+    ("qk_sample_head_ignored", "                h = samp_h[r];", "                h = 0;", 0),
 ]
 
 
