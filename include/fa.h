@@ -113,6 +113,40 @@ FA_API int fa_attention_fwd_varlen(const void *Q, const void *K, const void *V, 
                             const int32_t *cu_seqlens);
 
 /*
+ * Split-KV attention forward ("从 FlashAttention 看懂算子融合…": split the keys of a
+ * query block, keep per-split outputs and logsumexps, merge them in a combine
+ * kernel; the merge is the online-softmax rule of [L22] §十九 / §二十二).  For
+ * problems whose (sequence, head, 256-query block) count is too small to fill
+ * the GPU, e.g. a short block of new queries against a long context.
+ *
+ *   Q, O: bf16 [B, Nq, H, d];  K, V: bf16 [B, Nk, H, d];  lse: fp32 [B, H, Nq].
+ *   causal != 0: the queries are the last Nq positions of each sequence of Nk
+ *   keys (bottom-right alignment): query i sees keys j <= i + Nk - Nq; needs
+ *   Nk >= Nq.  With Nq == Nk this is fa_attention_fwd's masking.
+ *   num_splits: key ranges per query block; 0 lets the library choose
+ *   (fa_splitkv_num_splits); values above ceil(Nk / 128) are clamped.
+ *   O_accum: fp32 [num_splits, B, Nq, H, d] and lse_accum: fp32
+ *   [num_splits, B, H, Nq] -- DEVICE scratch owned by the caller, 16-byte and
+ *   4-byte aligned; contents on entry are ignored.  Unused (may be NULL) when
+ *   the split count in effect is 1.  Sizes use the split count in effect.
+ *   d: 64 or 128; Q, K, V, O 16-byte aligned.
+ * Runs the tensor-core kernel on every (block, split) and, when splits > 1,
+ * the combine kernel; no synchronisation.
+ * Errors: as fa_attention_fwd, and FA_ERR_BAD_SIZE for causal with Nk < Nq or
+ * num_splits < 0, FA_ERR_NULL_POINTER for missing scratch.
+ */
+FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V, void *O,
+                                    float *lse, int B, int H, int Nq, int Nk, int d, float scale,
+                                    int causal, int num_splits, float *O_accum, float *lse_accum);
+
+/*
+ * The split count fa_attention_fwd_splitkv uses for num_splits = 0 on the
+ * current device: enough (block, split) work items for every SM, at least two
+ * 128-key tiles per split.  Returns >= 1, or a negative FA_ERR_* code.
+ */
+FA_API int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
+
+/*
  * Exact attention forward in fp32 throughout (fp32 Q, K, V, O, lse), on the
  * CUDA cores, for inputs that need fp32 accuracy.  Same definition, layouts,
  * masks and cu_seqlens convention as fa_attention_fwd (the packed form reads

@@ -8,9 +8,11 @@ compiled library is missing, importing the C functions fails loudly.
 
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
-``fa_attention_fwd_f32``, ``fa_set_stream``, ``fa_get_stream``,
-``fa_get_device_error``, ``fa_strerror``, ``fa_version``.
-Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`.
+``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_f32``,
+``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
+``fa_version``.
+Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
+:func:`attention_fwd_splitkv`.
 """
 from __future__ import annotations
 
@@ -54,6 +56,9 @@ def lib():
         L.fa_attention_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32,
                                               i32, vp]
         L.fa_attention_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp]
+        L.fa_attention_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                               i32, i32, vp, vp]
+        L.fa_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
         L.fa_set_stream.argtypes = [vp]
         L.fa_get_stream.argtypes = []
         L.fa_get_stream.restype = vp
@@ -62,8 +67,8 @@ def lib():
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_version.argtypes = []
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
-                     "fa_attention_fwd_f32", "fa_set_stream", "fa_get_device_error",
-                     "fa_version"):
+                     "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
+                     "fa_set_stream", "fa_get_device_error", "fa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -99,6 +104,16 @@ def fa_attention_fwd_varlen(q, k, v, o, lse, B, H, N, total, d, scale, causal,
 
 def fa_attention_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens) -> int:
     return lib().fa_attention_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, cu_seqlens)
+
+
+def fa_attention_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits,
+                             o_accum, lse_accum) -> int:
+    return lib().fa_attention_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal,
+                                          num_splits, o_accum, lse_accum)
+
+
+def fa_splitkv_num_splits(B, H, Nq, Nk, d) -> int:
+    return lib().fa_splitkv_num_splits(B, H, Nq, Nk, d)
 
 
 def fa_set_stream(stream_ptr) -> int:
@@ -201,8 +216,47 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None,
     return out, lse
 
 
+def attention_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                          num_splits: int = 0, out=None, lse=None):
+    """Split-KV attention forward through the C ABI (bf16, dense).
+
+    q: [B, Nq, H, d]; k, v: [B, Nk, H, d]; causal is bottom-right aligned
+    (query i sees keys j <= i + Nk - Nq).  The fp32 split scratch is allocated
+    here (torch) and passed in.  Returns (O [B, Nq, H, d], lse [B, H, Nq]).
+    """
+    import torch
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, Nq, H, d = q.shape
+    Nk = k.shape[1]
+    if k.shape != (B, Nk, H, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Nk, H, d]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _use_current_stream(q.device)
+    splits = num_splits if num_splits > 0 else fa_splitkv_num_splits(B, H, Nq, Nk, d)
+    if splits < 0:
+        raise FaError(splits, "fa_splitkv_num_splits")
+    splits = min(splits, (Nk + 127) // 128)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    o_acc = l_acc = None
+    if splits > 1:
+        o_acc = torch.empty((splits, B, Nq, H, d), dtype=torch.float32, device=q.device)
+        l_acc = torch.empty((splits, B, H, Nq), dtype=torch.float32, device=q.device)
+    rc = fa_attention_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk,
+                                  d, float(scale), int(bool(causal)), splits, _ptr(o_acc),
+                                  _ptr(l_acc))
+    _check(rc, "fa_attention_fwd_splitkv")
+    return out, lse
+
+
 __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
+    "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
     "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",

@@ -79,14 +79,19 @@ struct Cfg {
 };
 
 struct Bf16Params {
-    CUtensorMap tm_q, tm_k, tm_v;    // 3-D maps over [total, H, d] bf16, box {64, 1, 128}
+    CUtensorMap tm_q, tm_k, tm_v;    // 3-D maps over [rows, H, d] bf16, box {64, 1, 128}
     __nv_bfloat16 *O;
     float *lse;
-    int B, H, N;
+    int B, H, N;                     // N: queries per sequence (dense) / longest sequence
+    int Nk;                          // keys per sequence (dense); packed batches use L
     int n_pairs;                     // Q-tile pairs per (sequence, head) at length N
-    int64_t total;
+    int64_t total;                   // query rows of Q / O
     float scale_log2;                // scale * log2(e)
     int causal;
+    int kv_off;                      // causal: query i sees keys j <= i + kv_off
+    int splits;                      // key ranges per Q-tile pair (1: write O, lse)
+    float *O_accum;                  // splits > 1: [splits, B, N, H, d] fp32 partial O
+    float *lse_accum;                // splits > 1: [splits, B, H, N] fp32 partial lse
     const int32_t *cu_seqlens;
     int *err_word;
 };
@@ -107,7 +112,10 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
-template <int D>
+// SPLIT: compiled for split-KV calls (key ranges, query/key lengths that
+// differ, partial outputs); the plain instantiation has one range per pair and
+// kv_off = 0, so that logic folds away.
+template <int D, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ Bf16Params p)
 {
@@ -127,34 +135,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + (C::kBarBytes / 8));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    // ---- work item: (sequence b, head h, Q-tile pair), heaviest pairs first ----
+    // ---- work item: (sequence b, head h, Q-tile pair, key split), heaviest
+    //      pairs first ------------------------------------------------------------
     const int bh_count = p.B * p.H;
-    const int pair = p.n_pairs - 1 - int(blockIdx.x / bh_count);
-    const int bh = int(blockIdx.x % bh_count);
+    const int n_splits = SPLIT ? p.splits : 1;
+    const int kv_off = SPLIT ? p.kv_off : 0;
+    const int split = SPLIT ? int(blockIdx.x % unsigned(n_splits)) : 0;
+    const int rest = SPLIT ? int(blockIdx.x / unsigned(n_splits)) : int(blockIdx.x);
+    const int pair = p.n_pairs - 1 - rest / bh_count;
+    const int bh = rest % bh_count;
     const int b = bh / p.H, h = bh % p.H;
-    int64_t start;
-    int L;
+    int64_t start, start_k;    // first query row / first key row of the sequence
+    int L, Lk;                 // query and key counts of the sequence
     if (p.cu_seqlens != nullptr) {
         const int64_t s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
         if (s0 < 0 || s1 < s0 || s1 > p.total || s1 - s0 > p.N) {
-            if (threadIdx.x == 0 && pair == 0 && h == 0)
+            if (threadIdx.x == 0 && pair == 0 && h == 0 && split == 0)
                 record_device_error(p.err_word, FA_DEVERR_BAD_SEQLENS);
             return;
         }
-        start = s0;
-        L = int(s1 - s0);
+        start = start_k = s0;
+        L = Lk = int(s1 - s0);
     } else {
         start = int64_t(b) * p.N;
         L = p.N;
+        start_k = SPLIT ? int64_t(b) * p.Nk : start;
+        Lk = SPLIT ? p.Nk : L;
     }
     const int qt0 = 2 * pair;                  // Q0 = tile qt0, Q1 = tile qt0 + 1
     if (qt0 * BM >= L)
         return;                                // whole CTA: nothing to do
     const bool has_q1 = (qt0 + 1) * BM < L;
-    const int n_kv = (L + BN - 1) / BN;
-    const int n0 = p.causal ? qt0 + 1 : n_kv;
-    const int n1 = has_q1 ? (p.causal ? qt0 + 2 : n_kv) : 0;
-    const int n_max = n0 > n1 ? n0 : n1;
+    const int n_kv = (Lk + BN - 1) / BN;
+    int n0, n1, n_max, j0 = 0;
+    if constexpr (SPLIT) {
+        // K/V tiles a Q tile sees: when causal, up to the one holding key
+        // (last row of the tile) + kv_off
+        auto tiles_seen = [&](int qt) {
+            if (!p.causal)
+                return n_kv;
+            const int last = (qt * BM + BM - 1 + kv_off) / BN + 1;
+            return last < n_kv ? last : n_kv;
+        };
+        const int n0_all = tiles_seen(qt0);
+        const int n1_all = has_q1 ? tiles_seen(qt0 + 1) : 0;
+        const int n_all = n0_all > n1_all ? n0_all : n1_all;
+        // this split's key tiles [j0, j0 + chunk) of the pair's range; a tile
+        // takes the steps of that range its keys reach (possibly none)
+        const int chunk = (n_all + n_splits - 1) / n_splits;
+        j0 = split * chunk;
+        auto steps = [&](int n_t) {
+            const int e = n_t < j0 + chunk ? n_t : j0 + chunk;
+            return e > j0 ? e - j0 : 0;
+        };
+        n0 = steps(n0_all);
+        n1 = steps(n1_all);
+    } else {
+        n0 = p.causal ? qt0 + 1 : n_kv;
+        n1 = has_q1 ? (p.causal ? qt0 + 2 : n_kv) : 0;
+    }
+    n_max = n0 > n1 ? n0 : n1;
+    if (SPLIT && n_max == 0) {
+        // an empty split: its partial result for the pair's rows is empty
+        // (lse = -inf, weight 0 in the combine)
+        if (n_splits > 1 && threadIdx.x < 2 * BM) {
+            const int i = qt0 * BM + int(threadIdx.x);
+            if (i < L)
+                p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = -INFINITY;
+        }
+        return;
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -198,12 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_phase[C::kStages];
             for (int s = 0; s < C::kStages; ++s)
                 last_phase[s] = -1;
-            const int nq = has_q1 ? 2 : 1;
+            // the Q tiles that have key tiles in this split
+            const int nq = (n0 > 0 ? 1 : 0) + (n1 > 0 ? 1 : 0);
             ptx::mbar_arrive_expect_tx(bar.q_full, nq * C::kTileBytes);
-            for (int t = 0; t < nq; ++t)
+            for (int t = 0; t < 2; ++t) {
+                if ((t == 0 ? n0 : n1) == 0)
+                    continue;
                 for (int c = 0; c < C::kChunks; ++c)
                     ptx::tma_load_3d(q_smem[t] + c * kChunkBytes, &p.tm_q, bar.q_full, c * 64, h,
                                      int(start + int64_t(qt0 + t) * BM));
+            }
             int stage = 0;
             uint32_t phase = 0;
             for (int j = 0; j < n_max && !aborted; ++j) {
@@ -218,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < C::kChunks; ++c)
                         ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes, tm,
                                          &bar.kv_full[stage], c * 64, h,
-                                         int(start + int64_t(j) * BN));
+                                         int(start_k + int64_t(j0 + j) * BN));
                     last_phase[stage] = int(phase);
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -301,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int k_stage = stage;
                 advance();
                 ptx::tc_fence_after_sync();
-                issue_qk(0, k_desc);
+                if (n0 > 0)
+                    issue_qk(0, k_desc);
                 if (n1 > 0)
                     issue_qk(1, k_desc);
                 ptx::mma_commit(&bar.kv_empty[k_stage]);
@@ -388,12 +443,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld32(tS + c * 32, sr[c]);
             ptx::tmem_wait_ld();
 
-            // mask: causal diagonal tile and the tile holding the sequence end
-            const bool diag = p.causal && j == qt;
-            const bool tail = (j + 1) * BN > L;
+            // mask: keys past the causal bound (query i sees keys <= i + kv_off)
+            // and past the end of the sequence's keys; jg is the key tile
+            const int jg = j0 + j;
+            bool diag, tail;
+            int lim_causal, lim_len;
+            if constexpr (SPLIT) {
+                diag = p.causal && jg * BN + BN - 1 > qt * BM + kv_off;
+                tail = (jg + 1) * BN > Lk;
+                lim_causal = diag ? i + kv_off - jg * BN : BN - 1;  // last visible column
+                lim_len = Lk - 1 - jg * BN;
+            } else {
+                diag = p.causal && j == qt;   // the diagonal tile (one range, kv_off = 0)
+                tail = (j + 1) * BN > L;
+                lim_causal = diag ? i - j * BN : BN - 1;
+                lim_len = L - 1 - j * BN;
+            }
             if (diag || tail) {
-                const int lim_causal = diag ? i - j * BN : BN - 1;  // last visible column
-                const int lim_len = L - 1 - j * BN;
                 const int lim = lim_causal < lim_len ? lim_causal : lim_len;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -464,7 +530,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- epilogue: O = O~ / l (bf16), lse = (m + log2 l) * ln 2 -----------
-        if (!aborted && n_t > 0) {
+        // With several key splits the partial O (fp32) and lse of this split are
+        // written instead; a row that saw no key in this split (possible only
+        // there) gets lse = -inf, which gives it weight 0 in the combine.
+        if constexpr (SPLIT) {
+            if (!aborted && n_t > 0) {
+                if (ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word)) {
+                    ptx::tc_fence_after_sync();
+                    const bool row_ok = i < L;
+                    const bool empty = !(l > 0.f);
+                    const float inv = empty ? 0.f : 1.f / l;
+                    __nv_bfloat16 *orow = p.O + ((start + i) * p.H + h) * D;
+                    float *arow = p.O_accum +
+                                  (((int64_t(split) * p.B + b) * p.N + i) * p.H + h) * D;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tO + c * 32, o);
+                        ptx::tmem_wait_ld();
+                        if (!row_ok)
+                            continue;
+                        if (n_splits > 1) {
+                            float4 *dst = reinterpret_cast<float4 *>(arow + c * 32);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(__uint_as_float(o[4 * q + 0]) * inv,
+                                                     __uint_as_float(o[4 * q + 1]) * inv,
+                                                     __uint_as_float(o[4 * q + 2]) * inv,
+                                                     __uint_as_float(o[4 * q + 3]) * inv);
+                            continue;
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
+                                                   __uint_as_float(o[8 * q + 1]) * inv);
+                            w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
+                                                   __uint_as_float(o[8 * q + 3]) * inv);
+                            w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
+                                                   __uint_as_float(o[8 * q + 5]) * inv);
+                            w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
+                                                   __uint_as_float(o[8 * q + 7]) * inv);
+                            dst[q] = w;
+                        }
+                    }
+                    if (row_ok) {
+                        const float lse = empty ? -INFINITY : (m + log2f(l)) * kLn2;
+                        if (n_splits > 1)
+                            p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = lse;
+                        else
+                            p.lse[(int64_t(b) * p.H + h) * p.N + i] = lse;
+                    }
+                }
+            } else if (!aborted && n_splits > 1 && i < L) {
+                // this tile has no keys in this split
+                p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = -INFINITY;
+            }
+        } else if (!aborted && n_t > 0) {
             if (ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word)) {
                 ptx::tc_fence_after_sync();
                 const float inv = 1.f / l;
@@ -552,10 +675,10 @@ bool make_tmap(CUtensorMap *tm, const void *base, int64_t total, int H, int d)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool SPLIT>
 int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 {
-    auto kern = attn_fwd_bf16_kernel<D>;
+    auto kern = attn_fwd_bf16_kernel<D, SPLIT>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -573,9 +696,16 @@ int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
 {
     Bf16Params p;
-    if (!make_tmap(&p.tm_q, a.Q, a.total, a.H, a.d) || !make_tmap(&p.tm_k, a.K, a.total, a.H, a.d) ||
-        !make_tmap(&p.tm_v, a.V, a.total, a.H, a.d))
+    const int Nk = a.Nk > 0 ? a.Nk : a.N;
+    const int64_t total_k = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
+    if (!make_tmap(&p.tm_q, a.Q, a.total, a.H, a.d) || !make_tmap(&p.tm_k, a.K, total_k, a.H, a.d) ||
+        !make_tmap(&p.tm_v, a.V, total_k, a.H, a.d))
         return FA_ERR_CUDA;
+    p.Nk = Nk;
+    p.kv_off = a.kv_off;
+    p.splits = a.splits > 0 ? a.splits : 1;
+    p.O_accum = a.O_accum;
+    p.lse_accum = a.lse_accum;
     p.O = static_cast<__nv_bfloat16 *>(a.O);
     p.lse = a.lse;
     p.B = a.B;
@@ -588,12 +718,39 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     p.causal = a.causal;
     p.cu_seqlens = a.cu_seqlens;
     p.err_word = a.err_word;
-    const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H;
+    const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H * p.splits;
     if (blocks == 0)
         return FA_OK;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
-    return a.d == 64 ? launch_d<64>(p, blocks, stream) : launch_d<128>(p, blocks, stream);
+    const bool split = p.splits > 1 || p.kv_off != 0 || Nk != a.N;
+    int rc;
+    if (a.d == 64)
+        rc = split ? launch_d<64, true>(p, blocks, stream) : launch_d<64, false>(p, blocks, stream);
+    else
+        rc = split ? launch_d<128, true>(p, blocks, stream) : launch_d<128, false>(p, blocks, stream);
+    if (rc != FA_OK || p.splits == 1)
+        return rc;
+    return launch_attention_combine(a, stream);
+}
+
+int choose_num_splits(int B, int H, int N, int Nk)
+{
+    // enough (sequence, head, Q-tile pair, split) items to give every SM one,
+    // with at least two 128-key tiles per split
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        sms = 148;
+    const int64_t pairs = int64_t((N + 2 * BM - 1) / (2 * BM)) * B * H;
+    if (pairs <= 0 || pairs >= sms)
+        return 1;
+    const int64_t want = (sms + pairs - 1) / pairs;
+    const int64_t cap = (Nk + BN - 1) / BN / 2;
+    int64_t s = want < cap ? want : cap;
+    if (s > 256)
+        s = 256;
+    return s < 1 ? 1 : int(s);
 }
 
 }  // namespace fa

@@ -1,0 +1,118 @@
+// attn_combine.cu -- merge of split-KV partial results.
+//
+// When the keys of a Q-tile pair are processed in several splits, split s
+// leaves, for every query row, its own normalised output O_s and logsumexp
+// lse_s over its keys.  The full result follows from the online-softmax merge
+// rule ("第二十二课：Softmax 为什么难以高效…" §十九 and §二十二: m = max(m_A, m_B),
+// l = e^{m_A - m} l_A + e^{m_B - m} l_B, and the same weights on the outputs),
+// written in logsumexp form:
+//     lse = m + ln sum_s exp(lse_s - m),   m = max_s lse_s
+//     O   = sum_s exp(lse_s - lse) * O_s
+// ("从 FlashAttention 看懂算子融合…": split-KV with per-split outputs and lse,
+// then a combine kernel).  One warp per (sequence, query row, head); lanes
+// split the splits for the reductions and the head dimension for O.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/fa.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr int kWarpsPerBlock = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    attn_combine_kernel(const float *O_accum, const float *lse_accum, __nv_bfloat16 *O,
+                        float *lse, int B, int H, int N, int splits)
+{
+    constexpr int kPerLane = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int64_t rows = int64_t(B) * N * H;
+    if (row >= rows)
+        return;
+    const int h = int(row % H);
+    const int i = int((row / H) % N);
+    const int b = int(row / (int64_t(N) * H));
+    const int64_t split_stride_lse = int64_t(B) * H * N;
+    const int64_t lse_off = (int64_t(b) * H + h) * N + i;
+
+    // m = max_s lse_s; lse = m + ln sum_s exp(lse_s - m)   (log2 units inside)
+    float mx = -INFINITY;
+    for (int s = lane; s < splits; s += 32)
+        mx = fmaxf(mx, lse_accum[s * split_stride_lse + lse_off] * kLog2e);
+    for (int o = 16; o > 0; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.f;
+    if (mx != -INFINITY)
+        for (int s = lane; s < splits; s += 32)
+            sum += ptx::ex2(lse_accum[s * split_stride_lse + lse_off] * kLog2e - mx);
+    for (int o = 16; o > 0; o >>= 1)
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float total = (mx == -INFINITY) ? -INFINITY : mx + log2f(sum);   // log2 units
+
+    float acc[kPerLane];
+#pragma unroll
+    for (int e = 0; e < kPerLane; ++e)
+        acc[e] = 0.f;
+    const int64_t split_stride_o = int64_t(B) * N * H * D;
+    const int64_t o_off = row * D + lane * kPerLane;   // row = (b * N + i) * H + h
+    if (total != -INFINITY) {
+        for (int s = 0; s < splits; ++s) {
+            const float ls = lse_accum[s * split_stride_lse + lse_off] * kLog2e;
+            if (ls == -INFINITY)
+                continue;                          // this split saw no key of the row
+            const float w = ptx::ex2(ls - total);
+            const float *src = O_accum + s * split_stride_o + o_off;
+            if (kPerLane == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(w, v.x, acc[0]);
+                acc[1] = fmaf(w, v.y, acc[1]);
+                acc[2] = fmaf(w, v.z, acc[2]);
+                acc[3] = fmaf(w, v.w, acc[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kPerLane; ++e)
+                    acc[e] = fmaf(w, src[e], acc[e]);
+            }
+        }
+    }
+    __nv_bfloat16 *dst = O + o_off;
+#pragma unroll
+    for (int e = 0; e < kPerLane; e += 2) {
+        const uint32_t w = ptx::pack_bf16x2(acc[e], acc[e + 1]);
+        *reinterpret_cast<uint32_t *>(dst + e) = w;
+    }
+    if (lane == 0)
+        lse[lse_off] = total * kLn2;
+}
+
+}  // namespace
+
+int launch_attention_combine(const AttnArgs &a, cudaStream_t stream)
+{
+    const int64_t rows = int64_t(a.B) * a.N * a.H;
+    if (rows == 0)
+        return FA_OK;
+    const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    if (blocks > 0x7fffffffLL)
+        return FA_ERR_TOO_LARGE;
+    auto *O = static_cast<__nv_bfloat16 *>(a.O);
+    if (a.d == 64)
+        attn_combine_kernel<64><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
+            a.O_accum, a.lse_accum, O, a.lse, a.B, a.H, a.N, a.splits);
+    else
+        attn_combine_kernel<128><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
+            a.O_accum, a.lse_accum, O, a.lse, a.B, a.H, a.N, a.splits);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace fa

@@ -170,6 +170,63 @@ int fa_attention_fwd_varlen(const void *Q, const void *K, const void *V, void *O
                                 cu_seqlens, true);
 }
 
+int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (fa::current_device() == nullptr)
+        return FA_ERR_NO_DEVICE;
+    return fa::choose_num_splits(B, H, Nq, Nk);
+}
+
+int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V, void *O, float *lse,
+                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                             int num_splits, float *O_accum, float *lse_accum)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || num_splits < 0)
+        return FA_ERR_BAD_SIZE;
+    if (causal && Nk < Nq)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || Nq == 0)
+        return FA_OK;
+    if (Nk == 0)
+        return FA_ERR_BAD_SIZE;            // no key for any query
+    fa::DeviceInfo *dev = fa::current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    const int64_t total_q = int64_t(B) * Nq, total_k = int64_t(B) * Nk;
+    if (total_k > (int64_t(1) << 31) - 512 || int64_t(Nk) > (int64_t(1) << 31) - 512)
+        return FA_ERR_TOO_LARGE;
+    fa::AttnArgs a;
+    int rc = fa::check_attention(Q, K, V, O, lse, B, H, Nq, d, causal, nullptr, total_q, true, &a);
+    if (rc != FA_OK)
+        return rc;
+    int splits = num_splits == 0 ? fa::choose_num_splits(B, H, Nq, Nk) : num_splits;
+    const int n_kv = (Nk + 127) / 128;
+    if (splits > n_kv)
+        splits = n_kv;
+    if (splits > 1) {
+        if (O_accum == nullptr || lse_accum == nullptr)
+            return FA_ERR_NULL_POINTER;
+        if (!fa::aligned(O_accum, 16) || !fa::aligned(lse_accum, 4))
+            return FA_ERR_MISALIGNED;
+        if (int64_t(splits) * total_q * H * d > (int64_t(1) << 56))
+            return FA_ERR_TOO_LARGE;
+    }
+    a.scale = scale;
+    a.err_word = dev->err_word;
+    a.Nk = Nk;
+    a.kv_off = Nk - Nq;
+    a.splits = splits;
+    a.O_accum = splits > 1 ? O_accum : nullptr;
+    a.lse_accum = splits > 1 ? lse_accum : nullptr;
+    return fa::launch_attention_bf16(a, fa::t_stream);
+}
+
 int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,
                          int B, int H, int N, int d, float scale, int causal,
                          const int32_t *cu_seqlens)

@@ -21,9 +21,23 @@ struct AttnArgs {
     int causal;
     const int32_t *cu_seqlens;  // device pointer or nullptr (dense)
     int *err_word;            // device error word
+    // split-KV (dense bf16 only): keys per sequence, causal offset (query i
+    // sees keys j <= i + kv_off), key ranges per Q-tile pair, fp32 scratch
+    int Nk = 0;               // 0: same as N
+    int kv_off = 0;
+    int splits = 1;
+    float *O_accum = nullptr; // [splits, B, N, H, d]
+    float *lse_accum = nullptr;  // [splits, B, H, N]
 };
 
 int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream);
 int launch_attention_f32(const AttnArgs &a, cudaStream_t stream);
+
+// Merges `splits` partial results (O_accum, lse_accum as above) into O (bf16,
+// [B, N, H, d]) and lse ([B, H, N]).
+int launch_attention_combine(const AttnArgs &a, cudaStream_t stream);
+
+// Number of key splits the library picks for a dense problem (>= 1).
+int choose_num_splits(int B, int H, int N, int Nk);
 
 }  // namespace fa

@@ -140,6 +140,53 @@ def _varlen_workload(name, n_seqs, lo, hi, H, d, seed, causal=True, q_std=2.0, k
                              lengths=lens)
 
 
+@dataclass(frozen=True)
+class SplitKVWorkload:
+    """Nq queries against Nk keys per (sequence, head); causal is bottom-right
+    aligned (query i sees keys j <= i + Nk - Nq)."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    dtype: str = "bf16"
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def visible_keys(self):
+        """Visible keys of each query position (array of Nq)."""
+        i = np.arange(self.Nq, dtype=np.int64)
+        if not self.causal:
+            return np.full(self.Nq, self.Nk, dtype=np.int64)
+        return np.minimum(i + (self.Nk - self.Nq) + 1, self.Nk)
+
+    def flops(self) -> float:
+        """Algorithmic flops: 4 * d per (query, visible key), summed."""
+        return float(4.0 * self.d * self.B * self.H * self.visible_keys().sum())
+
+    def inputs(self):
+        """Q [B, Nq, H, d]; K, V [B, Nk, H, d]; N(0, 1) drawn in that order."""
+        rng = rng_for(self.seed)
+        q = normal_f32(rng, (self.B, self.Nq, self.H, self.d))
+        k = normal_f32(rng, (self.B, self.Nk, self.H, self.d))
+        v = normal_f32(rng, (self.B, self.Nk, self.H, self.d))
+        return to_bf16(q), to_bf16(k), to_bf16(v)
+
+
+SPLITKV_WORKLOADS = {
+    # a block of 256 new queries against a 32K-token context, 16 heads: only 16
+    # (sequence, head, query block) items without key splits
+    "attn_bf16_splitkv_b1h16nq256nk32768d128_causal": SplitKVWorkload(
+        "attn_bf16_splitkv_b1h16nq256nk32768d128_causal", B=1, H=16, Nq=256, Nk=32768, d=128,
+        causal=True, seed=SEED_BASE + 6),
+}
+
+
 SOFTMAX_ROWS = 4096
 SOFTMAX_NS = (32, 128, 1024, 4096, 32768)
 SOFTMAX_SEED = SEED_BASE + 2
