@@ -48,6 +48,7 @@ extern "C" {
 #define FA_ERR_CUDA (-5)            /* a CUDA runtime/driver call failed          */
 #define FA_ERR_TOO_LARGE (-6)       /* a size exceeds what the kernels index      */
 #define FA_ERR_NO_DEVICE (-7)       /* no usable sm_103 device is current         */
+#define FA_ERR_SCRATCH_LIMIT (-8)   /* needs more than the library's static scratch */
 
 /* ---- device error word bits (fa_get_device_error) ------------------------- */
 #define FA_DEVERR_WAIT_TIMEOUT 0x1  /* a pipeline wait gave up (bounded wait)     */
@@ -145,6 +146,53 @@ FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V,
  * 128-key tiles per split.  Returns >= 1, or a negative FA_ERR_* code.
  */
 FA_API int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * Size in bytes of the device scratch array that
+ * fa_attention_fwd_splitkv_noalloc uses (64 MiB).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fa_attention_fwd_splitkv without caller scratch.  The pages have no
+ * counterpart to this function: it is a library convenience, not a step of
+ * the method.  Same definition, arguments (minus O_accum and lse_accum),
+ * masks, split choice and results as fa_attention_fwd_splitkv.
+ *
+ * For callers that cannot allocate device memory or pass a workspace at the
+ * call site: a plug-in whose host framework hands it only its input and output
+ * buffers, code that must not call cudaMalloc (which can synchronise the device
+ * and can fail under memory pressure) in a latency-bound decode loop, or a
+ * process whose device memory budget is fixed after start-up.  This function
+ * makes no device allocation and calls no allocating routine.
+ *
+ * Scratch: the per-split partials live in one library-owned device array of
+ * FA_NOALLOC_SCRATCH_BYTES per device, taken when the CUDA runtime loads that
+ * part of the library on the device (with lazy module loading, the CUDA
+ * default, at the first call of this function there) and held until the
+ * context ends.  With S splits in effect a call needs
+ * S * B * Nq * H * (d + 1) * 4 bytes of it; a call that needs more returns
+ * FA_ERR_SCRATCH_LIMIT and launches nothing (pass a smaller num_splits, or use
+ * fa_attention_fwd_splitkv with scratch of your own).  With one split in
+ * effect no scratch is used.  Nothing in the array has to start at zero:
+ * every element the combine reads is written earlier in the same call.
+ *
+ * The array's device address is looked up once per device, with that device
+ * current, on the first call that needs scratch there; make that first call
+ * before any stream capture begins.
+ *
+ * Calls share the one array per device: two calls whose work can run at the
+ * same time on one device (different streams, or different host threads with
+ * different streams) race on it and may return wrong results.  Calls on one
+ * stream run in order and are safe.
+ *
+ * Errors: as fa_attention_fwd_splitkv (except FA_ERR_NULL_POINTER for
+ * scratch), FA_ERR_SCRATCH_LIMIT as above, FA_ERR_CUDA if the array's address
+ * cannot be looked up.
+ */
+FA_API int fa_attention_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O,
+                                            float *lse, int B, int H, int Nq, int Nk, int d,
+                                            float scale, int causal, int num_splits);
 
 /*
  * Exact attention forward in fp32 throughout (fp32 Q, K, V, O, lse), on the

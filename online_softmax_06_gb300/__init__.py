@@ -8,7 +8,8 @@ compiled library is missing, importing the C functions fails loudly.
 
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
-``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_f32``,
+``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
+``fa_attention_fwd_f32``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
 ``fa_version``.
 Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
@@ -26,6 +27,8 @@ LIB_PATH = os.path.join(HERE, "_build", "libfa.so")
 FA_OK = 0
 FA_DEVERR_WAIT_TIMEOUT = 0x1
 FA_DEVERR_BAD_SEQLENS = 0x2
+FA_ERR_SCRATCH_LIMIT = -8
+FA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # static scratch of the _noalloc entry point
 
 _lib = None
 
@@ -59,6 +62,8 @@ def lib():
         L.fa_attention_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp, vp]
         L.fa_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                       i32, f32, i32, i32]
         L.fa_set_stream.argtypes = [vp]
         L.fa_get_stream.argtypes = []
         L.fa_get_stream.restype = vp
@@ -68,6 +73,7 @@ def lib():
         L.fa_version.argtypes = []
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
+                     "fa_attention_fwd_splitkv_noalloc",
                      "fa_set_stream", "fa_get_device_error", "fa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -114,6 +120,12 @@ def fa_attention_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nu
 
 def fa_splitkv_num_splits(B, H, Nq, Nk, d) -> int:
     return lib().fa_splitkv_num_splits(B, H, Nq, Nk, d)
+
+
+def fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal,
+                                     num_splits) -> int:
+    return lib().fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale,
+                                                  causal, num_splits)
 
 
 def fa_set_stream(stream_ptr) -> int:
@@ -257,6 +269,7 @@ def attention_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = N
 __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
     "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
+    "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
     "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",

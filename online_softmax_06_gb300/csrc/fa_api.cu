@@ -267,6 +267,8 @@ const char *fa_strerror(int code)
     case FA_ERR_CUDA: return "a CUDA call failed";
     case FA_ERR_TOO_LARGE: return "a size exceeds what the kernels can index";
     case FA_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case FA_ERR_SCRATCH_LIMIT:
+        return "the problem needs more scratch than the library's static array holds";
     default: return "unknown error code";
     }
 }

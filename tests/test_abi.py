@@ -67,6 +67,20 @@ def test_host_validation_without_gpu(lib):
     assert fa.fa_attention_fwd_varlen(None, None, None, None, None, 1, 1, 1, 1, 64, 1.0, 0,
                                       None) == -1
     assert fa.fa_attention_fwd_f32(None, None, None, None, None, 1, -1, 1, 64, 1.0, 0, None) == -2
+    nl = fa.fa_attention_fwd_splitkv_noalloc
+    assert nl(None, None, None, None, None, 1, 1, -1, 8, 64, 1.0, 0, 0) == -2
+    assert nl(None, None, None, None, None, 1, 1, 9, 8, 64, 1.0, 1, 0) == -2   # causal Nk < Nq
+    assert nl(None, None, None, None, None, 1, 1, 8, 8, 96, 1.0, 0, 0) == -3
+    assert nl(None, None, None, None, None, 0, 1, 8, 8, 64, 1.0, 0, 0) == 0
+
+
+def test_noalloc_scratch_size_matches_header():
+    text = open(HEADER, encoding="utf-8").read()
+    m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", text)
+    assert m, "FA_NOALLOC_SCRATCH_BYTES not found"
+    assert int(m[1]) * int(m[2]) * int(m[3]) == fa.FA_NOALLOC_SCRATCH_BYTES
+    assert re.search(r"#define FA_ERR_SCRATCH_LIMIT \((-\d+)\)", text)[1] == \
+        str(fa.FA_ERR_SCRATCH_LIMIT)
 
 
 def test_stream_setting_is_per_thread(lib):
