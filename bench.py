@@ -6,7 +6,8 @@ on the causal bf16 workload B=2, H=32, N=4096, d=128 (Q, K, V ~ N(0,1) rounded
 to bf16; 192 MiB of Q/K/V, larger than the 129 MB L2), through the C ABI.
 The row softmax (fp32, 4096 x N, the HBM-resident lengths) is timed in the
 same run with L2 flushed before every repetition and reported under
-"softmax".  Prints one JSON line (rank 0).
+"softmax"; split-KV attention on a decode-like shape (256 queries, 32768 keys)
+under "splitkv".  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -54,6 +55,7 @@ def parse_args():
                     help="comma-separated row lengths for the softmax leg ('' to skip)")
     ap.add_argument("--softmax-reps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-splitkv", action="store_true", help="skip the split-KV leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -380,6 +382,69 @@ def time_softmax(fa, dev, Ns, reps, peaks, clocks):
     return out
 
 
+def time_splitkv(fa, dev, reps, peaks, clocks):
+    """Split-KV attention (tensor-core kernel per key split + combine kernel) on
+    the decode-like workload: 256 new queries, 32768 keys, 16 heads, causal.
+
+    K and V (256 MiB) exceed the L2, so back-to-back calls re-read them from
+    HBM.  At this shape the HBM floor (every Q, K, V, O byte once: 270 MB) is
+    above the tensor floor (68.5 GFLOP), so both fractions are reported and the
+    bound is HBM.  The one-split figure (same kernel, 16 CTAs) is beside it."""
+    import torch
+    w = workloads.SPLITKV_WORKLOADS["attn_bf16_splitkv_b1h16nq256nk32768d128_causal"]
+    Q, K, V = w.inputs()
+    q, k, v = (t.to(dev) for t in (Q, K, V))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    splits = fa.fa_splitkv_num_splits(w.B, w.H, w.Nq, w.Nk, w.d)
+    if splits < 1:
+        raise RuntimeError(fa.strerror(splits))
+    o_acc = torch.empty((splits, w.B, w.Nq, w.H, w.d), dtype=torch.float32, device=dev)
+    l_acc = torch.empty((splits, w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+
+    def timed(n_splits):
+        def launch():
+            rc = fa.fa_attention_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Nq,
+                                             w.Nk, w.d, w.scale, int(w.causal), n_splits,
+                                             o_acc.data_ptr(), l_acc.data_ptr())
+            if rc != 0:
+                raise RuntimeError(fa.strerror(rc))
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    t0 = time.time()
+    ms = timed(splits)
+    ms1 = timed(1)
+    clocks.mark(t0, time.time())
+    dev_err = fa.fa_get_device_error()
+    if dev_err != 0:
+        raise RuntimeError(f"device error word {dev_err:#x}")
+    flops = w.flops()
+    nbytes = 2.0 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4.0 * lse.numel()
+    partial_bytes = 2.0 * 4.0 * (o_acc.numel() + l_acc.numel())
+    tf = flops / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+            "causal": w.causal, "splits": splits, "launches_per_call": 2 if splits > 1 else 1,
+            "ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "algorithmic_bytes": nbytes, "GB_per_s": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "bound": "hbm", "partial_bytes_written_and_read": partial_bytes,
+            "flops_per_call": flops, "one_split_ms": ms1,
+            "one_split_TFLOP_per_s": flops / (ms1 / 1e3) / 1e12,
+            "l2": "K/V 256 MiB, larger than L2; %d back-to-back calls" % reps}
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -412,6 +477,9 @@ def main():
         if args.softmax_n and rank == 0:
             Ns = [int(s) for s in args.softmax_n.split(",") if s]
             softmax = time_softmax(fa, dev, Ns, args.softmax_reps, peaks, clocks)
+        splitkv = None
+        if not args.no_splitkv and rank == 0:
+            splitkv = time_splitkv(fa, dev, 50, peaks, clocks)
     finally:
         clk = clocks.stop()
     e2e = None
@@ -435,6 +503,7 @@ def main():
         "gpu_launches": steps,
         "clocks": clk,
         "softmax": softmax,
+        "splitkv": splitkv,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -142,8 +142,10 @@ FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V,
 
 /*
  * The split count fa_attention_fwd_splitkv uses for num_splits = 0 on the
- * current device: enough (block, split) work items for every SM, at least two
- * 128-key tiles per split.  Returns >= 1, or a negative FA_ERR_* code.
+ * current device: as many splits as fill the SMs in one wave (floor of SMs /
+ * 256-query blocks, 1 when the blocks alone fill more than half of the SMs),
+ * at least two 128-key tiles per split.  Returns >= 1, or a negative FA_ERR_*
+ * code.
  */
 FA_API int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
 

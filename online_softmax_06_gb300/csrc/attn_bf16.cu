@@ -736,16 +736,18 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
 
 int choose_num_splits(int B, int H, int N, int Nk)
 {
-    // enough (sequence, head, Q-tile pair, split) items to give every SM one,
-    // with at least two 128-key tiles per split
+    // one CTA runs per SM, so the (sequence, head, Q-tile pair, split) items
+    // should fill the SMs in one wave: floor(SMs / pairs) splits (a partial
+    // second wave would double the time), with at least two 128-key tiles per
+    // split
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         sms = 148;
     const int64_t pairs = int64_t((N + 2 * BM - 1) / (2 * BM)) * B * H;
-    if (pairs <= 0 || pairs >= sms)
+    if (pairs <= 0 || 2 * pairs > sms)
         return 1;
-    const int64_t want = (sms + pairs - 1) / pairs;
+    const int64_t want = sms / pairs;
     const int64_t cap = (Nk + BN - 1) / BN / 2;
     int64_t s = want < cap ? want : cap;
     if (s > 256)

@@ -16,6 +16,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/fa.h"
 #include "launch.h"
@@ -59,6 +60,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float total = (mx == -INFINITY) ? -INFINITY : mx + log2f(sum);   // log2 units
 
+    // O = sum_s w_s O_s with w_s = exp(lse_s - lse).  Lane l holds w of split
+    // c0 + l of the current chunk of 32; the splits are taken eight at a time
+    // with their loads issued before the FMAs, so a warp keeps eight 128-bit
+    // loads per lane in flight.  A split with w = 0 (lse_s = -inf: it saw no
+    // key of the row, its O_s was never written) is not read.
+    using Vec = typename std::conditional<kPerLane == 4, float4, float2>::type;
     float acc[kPerLane];
 #pragma unroll
     for (int e = 0; e < kPerLane; ++e)
@@ -66,22 +73,35 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int64_t split_stride_o = int64_t(B) * N * H * D;
     const int64_t o_off = row * D + lane * kPerLane;   // row = (b * N + i) * H + h
     if (total != -INFINITY) {
-        for (int s = 0; s < splits; ++s) {
-            const float ls = lse_accum[s * split_stride_lse + lse_off] * kLog2e;
-            if (ls == -INFINITY)
-                continue;                          // this split saw no key of the row
-            const float w = ptx::ex2(ls - total);
-            const float *src = O_accum + s * split_stride_o + o_off;
-            if (kPerLane == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
-                acc[2] = fmaf(w, v.z, acc[2]);
-                acc[3] = fmaf(w, v.w, acc[3]);
-            } else {
+        for (int c0 = 0; c0 < splits; c0 += 32) {
+            const int s_l = c0 + lane;
+            const float w_l = s_l < splits
+                                  ? ptx::ex2(lse_accum[s_l * split_stride_lse + lse_off] * kLog2e -
+                                             total)
+                                  : 0.f;
+            const int n = splits - c0 < 32 ? splits - c0 : 32;
+            for (int u0 = 0; u0 < n; u0 += 8) {
+                float w[8];
+                Vec v[8];
 #pragma unroll
-                for (int e = 0; e < kPerLane; ++e)
-                    acc[e] = fmaf(w, src[e], acc[e]);
+                for (int u = 0; u < 8; ++u)
+                    w[u] = __shfl_sync(0xffffffffu, w_l, u0 + u);   // 0 past the last split
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const Vec *src = reinterpret_cast<const Vec *>(
+                        O_accum + (c0 + u0 + u) * split_stride_o + o_off);
+                    if (w[u] != 0.f)
+                        v[u] = *src;
+                    else
+                        v[u] = Vec{};
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float *f = reinterpret_cast<const float *>(&v[u]);
+#pragma unroll
+                    for (int e = 0; e < kPerLane; ++e)
+                        acc[e] = fmaf(w[u], f[e], acc[e]);
+                }
             }
         }
     }

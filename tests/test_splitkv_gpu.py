@@ -41,6 +41,8 @@ def run(Q, K, V, causal, splits, dev):
     (1, 2, 256, 4096, 128, True, 0),    # split count chosen by the library
     (2, 1, 257, 777, 128, False, 7),
     (1, 2, 130, 1300, 64, False, 64),   # clamped to the 11 key tiles
+    (1, 2, 200, 5120, 128, False, 40),  # 40 one-tile splits: two chunks of the combine
+    (1, 2, 256, 8192, 128, True, 37),   # splits 32..36 empty (lse -inf) in the second chunk
 ])
 def test_splitkv_matches_oracle(dev, B, H, Nq, Nk, d, causal, splits):
     Q, K, V = inputs(B, H, Nq, Nk, d, seed=Nq * 31 + Nk + d + splits)
