@@ -13,9 +13,9 @@
 //   * one CTA per SM, 320 threads, owns two 128-row Q tiles of one
 //     (sequence, head) -- "Q0" and "Q1", adjacent in the sequence -- so every
 //     K/V tile loaded into shared memory feeds 2 x 128 rows;
-//   * warp 8 (one lane) issues TMA loads: both Q tiles once, then K_0, V_0, K_1,
-//     V_1, ... into a ring of shared-memory stages guarded by full/empty
-//     mbarriers;
+//   * warp 8 (one lane) issues TMA loads: Q0, K_0, Q1 (one barrier per Q tile,
+//     so the first Q0 K_0^T does not wait for Q1), then V_0, K_1, V_1, ...
+//     into a ring of shared-memory stages guarded by full/empty mbarriers;
 //   * warp 9 (one lane) owns the tensor memory and issues every tcgen05.mma:
 //     S_t = Q_t K_j^T (bf16 x bf16 -> fp32, M=N=128, K=d) into TMEM, and
 //     O_t += P_t V_j with P_t read from TMEM (written there by the softmax
@@ -27,7 +27,10 @@
 //     the causal / sequence-end mask on the tiles that need it, updates m and
 //     l, converts P to bf16 into TMEM, and rescales its row of O in TMEM only
 //     when its maximum grew (warp-uniform skip otherwise); after the last tile
-//     it normalises O and writes O (bf16) and lse (fp32).
+//     it normalises O and writes lse (fp32) and O (bf16): a whole tile is
+//     written into the Q tile's shared-memory buffer (free by then, and laid
+//     out as the TMA box) and leaves in one TMA store; a tile that runs past
+//     the end of its sequence is stored row by row.
 // Tensor memory per CTA (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d),
 // O1 [256+d, 256+2d); P_t aliases columns 64..127 of S_t.
 // Every wait is bounded (ptx::mbar_wait); a timed-out wait raises an error bit,
@@ -74,12 +77,13 @@ struct Cfg {
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffRing = 2 * kTileBytes;
     static constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
-    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 2 + 2 + 2 + 1);
+    static constexpr uint32_t kBarBytes = 8 * (2 + 2 * kStages + 2 + 2 + 2 + 1);
     static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;  // +1024 align slack
 };
 
 struct Bf16Params {
     CUtensorMap tm_q, tm_k, tm_v;    // 3-D maps over [rows, H, d] bf16, box {64, 1, 128}
+    CUtensorMap tm_o;                // the same over O (stores of whole tiles)
     __nv_bfloat16 *O;
     float *lse;
     int B, H, N;                     // N: queries per sequence (dense) / longest sequence
@@ -125,10 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
     Barriers bar;
-    bar.q_full = bars;
-    bar.kv_full = bars + 1;
-    bar.kv_empty = bars + 1 + C::kStages;
-    bar.s_full = bars + 1 + 2 * C::kStages;
+    bar.q_full = bars;                         // one per Q tile
+    bar.kv_full = bars + 2;
+    bar.kv_empty = bars + 2 + C::kStages;
+    bar.s_full = bars + 2 + 2 * C::kStages;
     bar.p_full = bar.s_full + 2;
     bar.o_full = bar.p_full + 2;
     bar.drain = bar.o_full + 2;
@@ -210,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- set-up: barriers, tensor memory ----------------------------------
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar.q_full, 1);
+        ptx::mbar_init(&bar.q_full[0], 1);
+        ptx::mbar_init(&bar.q_full[1], 1);
         for (int s = 0; s < C::kStages; ++s) {
             ptx::mbar_init(&bar.kv_full[s], 1);
             ptx::mbar_init(&bar.kv_empty[s], 1);
@@ -248,16 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             int last_phase[C::kStages];
             for (int s = 0; s < C::kStages; ++s)
                 last_phase[s] = -1;
-            // the Q tiles that have key tiles in this split
-            const int nq = (n0 > 0 ? 1 : 0) + (n1 > 0 ? 1 : 0);
-            ptx::mbar_arrive_expect_tx(bar.q_full, nq * C::kTileBytes);
-            for (int t = 0; t < 2; ++t) {
-                if ((t == 0 ? n0 : n1) == 0)
-                    continue;
+            // Q0 (if it has key tiles here), then K_0, then Q1: the first
+            // Q0 K_0^T can start before Q1 has landed
+            bool q_issued[2] = {false, false};
+            auto load_q = [&](int t) {
+                q_issued[t] = true;
+                ptx::mbar_arrive_expect_tx(&bar.q_full[t], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_3d(q_smem[t] + c * kChunkBytes, &p.tm_q, bar.q_full, c * 64, h,
+                    ptx::tma_load_3d(q_smem[t] + c * kChunkBytes, &p.tm_q, &bar.q_full[t], c * 64, h,
                                      int(start + int64_t(qt0 + t) * BM));
-            }
+            };
+            if (n0 > 0)
+                load_q(0);
             int stage = 0;
             uint32_t phase = 0;
             for (int j = 0; j < n_max && !aborted; ++j) {
@@ -278,11 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (j == 0 && kv == 0 && n1 > 0)
+                        load_q(1);
                 }
             }
             if (aborted || *abort_flag) {
                 // let every copy already issued land before the CTA goes away
-                drain_wait(bar.q_full, 0);
+                for (int t = 0; t < 2; ++t)
+                    if (q_issued[t])
+                        drain_wait(&bar.q_full[t], 0);
                 for (int s = 0; s < C::kStages; ++s)
                     if (last_phase[s] >= 0)
                         drain_wait(&bar.kv_full[s], uint32_t(last_phase[s]));
@@ -343,10 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
 
             do {
-                if (!ptx::mbar_wait(bar.q_full, 0, abort_flag, p.err_word)) {
-                    aborted = true;
-                    break;
-                }
                 uint64_t k_desc, unused;
                 if (!next_stage(k_desc, unused)) {
                     aborted = true;
@@ -354,11 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 int k_stage = stage;
                 advance();
-                ptx::tc_fence_after_sync();
-                if (n0 > 0)
-                    issue_qk(0, k_desc);
-                if (n1 > 0)
-                    issue_qk(1, k_desc);
+                bool q_ok = true;
+                for (int t = 0; t < 2 && q_ok; ++t) {
+                    if ((t == 0 ? n0 : n1) == 0)
+                        continue;
+                    q_ok = ptx::mbar_wait(&bar.q_full[t], 0, abort_flag, p.err_word);
+                    if (q_ok) {
+                        ptx::tc_fence_after_sync();
+                        issue_qk(t, k_desc);
+                    }
+                }
+                if (!q_ok) {
+                    aborted = true;
+                    break;
+                }
                 ptx::mma_commit(&bar.kv_empty[k_stage]);
 
                 for (int j = 0; j < n_max; ++j) {
@@ -587,8 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this tile has no keys in this split
                 p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = -INFINITY;
             }
-        } else if (!aborted && n_t > 0) {
-            if (ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word)) {
+        } else if (n_t > 0) {
+            // A whole tile goes out through shared memory and one TMA store:
+            // Q_t's buffer is free (every Q_t K^T completed before the last S_t
+            // was published) and has the store's swizzled layout.  A tile that
+            // runs past the end of its sequence is stored row by row, so that
+            // no row of the next sequence is touched.
+            const bool full_tile = (qt + 1) * BM <= L;
+            uint8_t *o_stage = q_smem[t];
+            const bool ok = !aborted && ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word);
+            if (ok) {
                 ptx::tc_fence_after_sync();
                 const float inv = 1.f / l;
                 const bool row_ok = i < L;
@@ -598,21 +622,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     ptx::tmem_ld32(tO + c * 32, o);
                     ptx::tmem_wait_ld();
-                    if (row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                    uint4 w[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        w[q].x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
+                                                  __uint_as_float(o[8 * q + 1]) * inv);
+                        w[q].y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
+                                                  __uint_as_float(o[8 * q + 3]) * inv);
+                        w[q].z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
+                                                  __uint_as_float(o[8 * q + 5]) * inv);
+                        w[q].w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
+                                                  __uint_as_float(o[8 * q + 7]) * inv);
+                    }
+                    if (full_tile) {
+                        // 128-byte swizzle: 16-byte unit u of row r sits at
+                        // unit position u ^ (r % 8) of the row's 128 bytes
+                        uint8_t *rowp = o_stage + (c >> 1) * kChunkBytes + r * 128;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            w.x = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv,
-                                                   __uint_as_float(o[8 * q + 1]) * inv);
-                            w.y = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv,
-                                                   __uint_as_float(o[8 * q + 3]) * inv);
-                            w.z = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv,
-                                                   __uint_as_float(o[8 * q + 5]) * inv);
-                            w.w = ptx::pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv,
-                                                   __uint_as_float(o[8 * q + 7]) * inv);
-                            dst[q] = w;
+                            const int u = (c & 1) * 4 + q;
+                            *reinterpret_cast<uint4 *>(rowp + ((u ^ (r & 7)) << 4)) = w[q];
                         }
+                    } else if (row_ok) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = w[q];
                     }
                 }
                 if (row_ok) {
@@ -621,6 +656,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p.lse[int64_t(h) * p.total + start + i] = lse;
                     else
                         p.lse[(int64_t(b) * p.H + h) * p.N + i] = lse;
+                }
+            }
+            if (full_tile) {
+                ptx::fence_proxy_async_smem();
+                // every thread of the tile arrives here once, also after a
+                // failed wait; the store goes out only if all 128 rows are in
+                if (!ptx::bar_red_or(1 + t, 128, !ok) && r == 0) {
+                    for (int ch = 0; ch < C::kChunks; ++ch)
+                        ptx::tma_store_3d(&p.tm_o, o_stage + ch * kChunkBytes, ch * 64, h,
+                                     int(start + int64_t(qt) * BM));
+                    ptx::bulk_commit_and_wait_read();
                 }
             }
         }
@@ -699,7 +745,8 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     const int Nk = a.Nk > 0 ? a.Nk : a.N;
     const int64_t total_k = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
     if (!make_tmap(&p.tm_q, a.Q, a.total, a.H, a.d) || !make_tmap(&p.tm_k, a.K, total_k, a.H, a.d) ||
-        !make_tmap(&p.tm_v, a.V, total_k, a.H, a.d))
+        !make_tmap(&p.tm_v, a.V, total_k, a.H, a.d) ||
+        !make_tmap(&p.tm_o, a.O, a.total, a.H, a.d))
         return FA_ERR_CUDA;
     p.Nk = Nk;
     p.kv_off = a.kv_off;

@@ -113,6 +113,43 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tmap)
 }
 
 // ---------------------------------------------------------------------------
+// TMA store, proxy fence, named-barrier reduction
+// ---------------------------------------------------------------------------
+// Named-barrier reduction over `count` threads: returns the OR of `pred`.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// TMA tiled store shared -> global (bulk group), and the wait for its source read.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tmap, const void *smem_src, int x,
+                                             int y, int z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait_read()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ---------------------------------------------------------------------------
 // Whole-warp TMEM allocation; the base address is written to *dst (shared).
