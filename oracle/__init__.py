@@ -73,6 +73,13 @@ def _bind(lib):
     lib.oracle_attention_qk.argtypes = [vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_i64, c_dbl,
                                         c_int, vp, vp, vp, c_i64, vp, vp]
     lib.oracle_attention_qk.restype = None
+    lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i64, c_dbl,
+                                         c_int, vp, vp, vp, vp, vp, vp]
+    lib.oracle_attention_bwd.restype = None
+    lib.oracle_attention_bwd_head.argtypes = [vp, vp, vp, vp, c_i64, c_i64, c_i64, c_i64,
+                                              c_dbl, c_int, c_i64, c_i64, vp, c_i64, vp, c_i64,
+                                              vp, vp, vp]
+    lib.oracle_attention_bwd_head.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
     return lib
@@ -232,6 +239,51 @@ def attention_qk(Q, K, V, scale, causal, samples=None, lib=None):
                             int(bool(causal)), _ptr(sb), _ptr(si), _ptr(sh), n, _ptr(O),
                             _ptr(lse))
     return O, lse
+
+
+def attention_bwd(Q, K, V, dO, scale, causal, lib=None):
+    """Gradients of sum(dO * O) for dense Q, K, V, dO [B, N, H, d].
+
+    Returns a dict of float64 arrays: dQ, dK, dV, O [B, N, H, d] and lse, D
+    [B, H, N] (the row logsumexp and D_i = sum_j P_ij dP_ij).  Materialises
+    N x N per (b, h): small N only.
+    """
+    Q, K, V, dO = _f32(Q), _f32(K), _f32(V), _f32(dO)
+    B, N, H, d = Q.shape
+    for t in (K, V, dO):
+        if t.shape != Q.shape:
+            raise ValueError("Q, K, V, dO must have one shape")
+    out = {k: np.zeros((B, N, H, d)) for k in ("dQ", "dK", "dV", "O")}
+    out["lse"] = np.zeros((B, H, N))
+    out["D"] = np.zeros((B, H, N))
+    (lib or load()).oracle_attention_bwd(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, N, d, float(scale), int(bool(causal)),
+        _ptr(out["dQ"]), _ptr(out["dK"]), _ptr(out["dV"]), _ptr(out["O"]), _ptr(out["lse"]),
+        _ptr(out["D"]))
+    return out
+
+
+def attention_bwd_head(Q, K, V, dO, scale, causal, b, h, q_idx, k_idx, lib=None):
+    """dQ of the query rows q_idx and dK, dV of the keys k_idx for one (b, h).
+
+    Returns (dQ_rows [len(q_idx), d], dK_rows, dV_rows [len(k_idx), d]) in float64.
+    """
+    Q, K, V, dO = _f32(Q), _f32(K), _f32(V), _f32(dO)
+    B, N, H, d = Q.shape
+    qi = np.ascontiguousarray(np.asarray(q_idx, dtype=np.int64))
+    ki = np.ascontiguousarray(np.asarray(k_idx, dtype=np.int64))
+    for a in (qi, ki):
+        if a.size and (a.min() < 0 or a.max() >= N):
+            raise ValueError("row index out of range")
+    if not (0 <= b < B and 0 <= h < H):
+        raise ValueError("(b, h) out of range")
+    dq = np.zeros((qi.size, d))
+    dk = np.zeros((ki.size, d))
+    dv = np.zeros((ki.size, d))
+    (lib or load()).oracle_attention_bwd_head(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, N, d, float(scale), int(bool(causal)), b, h,
+        _ptr(qi), qi.size, _ptr(ki), ki.size, _ptr(dq), _ptr(dk), _ptr(dv))
+    return dq, dk, dv
 
 
 if __name__ == "__main__":  # pragma: no cover - manual rebuild

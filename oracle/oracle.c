@@ -1,6 +1,6 @@
 /*
- * oracle.c -- plain, slow, fp64 CPU oracle for the row softmax and the
- * attention forward.
+ * oracle.c -- plain, slow, fp64 CPU oracle for the row softmax, the
+ * attention forward and the attention backward (gradients).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the tests, the smoke check and the benchmark's
@@ -374,6 +374,192 @@ void oracle_attention_qk(const float *Q, const float *K, const float *V, int64_t
         }
         free(s);
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention backward                                                        */
+/* ------------------------------------------------------------------------ */
+/*
+ * Gradients of the loss sum(dO * O) with respect to Q, K and V, for the forward
+ * definition above on dense batches [B, N, H, d] (causal: j <= i).  The pages
+ * recompute the probabilities from the saved row statistic instead of storing
+ * them ([FG] §2.4: P_ij = exp(S_ij - L_i) with L = m + log l; [L22] §三十) and
+ * leave the derivation of the gradients out ([FG], list of omitted topics at
+ * the end).  Reading: the plain chain rule through S = scale Q K^T,
+ * P = softmax(S) (row-wise over the visible keys), O = P V:
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)      (softmax Jacobian)
+ *   dQ_i  = scale sum_j dS_ij K_j
+ *   dK_j  = scale sum_i dS_ij Q_i
+ * Everything is recomputed here from Q, K, V, dO in double; the row statistic
+ * L_i = m_i + log l_i and D_i = sum_k P_ik dP_ik are returned for checks.
+ * One (b, h) at a time; S and P are materialised (N x N doubles): small N.
+ * Outputs: dQ, dK, dV, O [B, N, H, d]; lse, D [B, H, N] (O, lse, D may be NULL).
+ */
+void oracle_attention_bwd(const float *Q, const float *K, const float *V, const float *dO,
+                          int64_t B, int64_t H, int64_t N, int64_t d, double scale, int causal,
+                          double *dQ, double *dK, double *dV, double *O, double *lse, double *D)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const int64_t b = bh / H, h = bh % H;
+        double *P = (double *)calloc((size_t)(N * N > 0 ? N * N : 1), sizeof(double));
+        double *dP = (double *)calloc((size_t)(N * N > 0 ? N * N : 1), sizeof(double));
+#define ROW(X, t) ((X) + ((b * N + (t)) * H + h) * d)
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t nvis = causal ? i + 1 : N;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += (double)ROW(Q, i)[c] * (double)ROW(K, j)[c];
+                P[i * N + j] = scale * dot;             /* S for now */
+                if (P[i * N + j] > m)
+                    m = P[i * N + j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nvis; ++j)
+                l += exp(P[i * N + j] - m);
+            const double L = m + log(l);
+            for (int64_t j = 0; j < nvis; ++j)
+                P[i * N + j] = exp(P[i * N + j] - L);   /* [FG] §2.4 */
+            double Di = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += (double)ROW(dO, i)[c] * (double)ROW(V, j)[c];
+                dP[i * N + j] = dot;
+                Di += P[i * N + j] * dot;
+            }
+            if (lse)
+                lse[(b * H + h) * N + i] = L;
+            if (D)
+                D[(b * H + h) * N + i] = Di;
+            if (O)
+                for (int64_t c = 0; c < d; ++c) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < nvis; ++j)
+                        acc += P[i * N + j] * (double)ROW(V, j)[c];
+                    ROW(O, i)[c] = acc;
+                }
+            /* dS overwrites dP */
+            for (int64_t j = 0; j < nvis; ++j)
+                dP[i * N + j] = P[i * N + j] * (dP[i * N + j] - Di);
+        }
+        for (int64_t i = 0; i < N; ++i)
+            for (int64_t c = 0; c < d; ++c) {
+                const int64_t nvis = causal ? i + 1 : N;
+                double acc = 0.0;
+                for (int64_t j = 0; j < nvis; ++j)
+                    acc += dP[i * N + j] * (double)ROW(K, j)[c];
+                ROW(dQ, i)[c] = scale * acc;
+            }
+        for (int64_t j = 0; j < N; ++j)
+            for (int64_t c = 0; c < d; ++c) {
+                double acc_k = 0.0, acc_v = 0.0;
+                for (int64_t i = causal ? j : 0; i < N; ++i) {
+                    acc_k += dP[i * N + j] * (double)ROW(Q, i)[c];
+                    acc_v += P[i * N + j] * (double)ROW(dO, i)[c];
+                }
+                ROW(dK, j)[c] = scale * acc_k;
+                ROW(dV, j)[c] = acc_v;
+            }
+#undef ROW
+        free(P);
+        free(dP);
+    }
+}
+
+/*
+ * The same gradients for one (b, h) of a large batch, for the listed query
+ * rows (dQ) and keys (dK, dV) only.  First L_i and D_i of every query row of
+ * the head are computed (one pass over its keys per row), then each listed
+ * row or key costs one pass over the other side.  Outputs: dQ_rows [nq, d],
+ * dK_rows, dV_rows [nk, d].
+ */
+void oracle_attention_bwd_head(const float *Q, const float *K, const float *V, const float *dO,
+                               int64_t B, int64_t H, int64_t N, int64_t d, double scale,
+                               int causal, int64_t b, int64_t h, const int64_t *q_idx, int64_t nq,
+                               const int64_t *k_idx, int64_t nk, double *dQ_rows,
+                               double *dK_rows, double *dV_rows)
+{
+    (void)B;
+    double *L = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    double *Dv = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#define ROW(X, t) ((X) + ((b * N + (t)) * H + h) * d)
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t nvis = causal ? i + 1 : N;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += (double)ROW(Q, i)[c] * (double)ROW(K, j)[c];
+                s[j] = scale * dot;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nvis; ++j)
+                l += exp(s[j] - m);
+            L[i] = m + log(l);
+            double Di = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dot += (double)ROW(dO, i)[c] * (double)ROW(V, j)[c];
+                Di += exp(s[j] - L[i]) * dot;
+            }
+            Dv[i] = Di;
+        }
+        free(s);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nq; ++r) {
+            const int64_t i = q_idx[r];
+            const int64_t nvis = causal ? i + 1 : N;
+            double *out = dQ_rows + r * d;
+            for (int64_t c = 0; c < d; ++c)
+                out[c] = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) {
+                double sdot = 0.0, pdot = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    sdot += (double)ROW(Q, i)[c] * (double)ROW(K, j)[c];
+                    pdot += (double)ROW(dO, i)[c] * (double)ROW(V, j)[c];
+                }
+                const double P = exp(scale * sdot - L[i]);
+                const double dS = P * (pdot - Dv[i]);
+                for (int64_t c = 0; c < d; ++c)
+                    out[c] += scale * dS * (double)ROW(K, j)[c];
+            }
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nk; ++r) {
+            const int64_t j = k_idx[r];
+            double *ok = dK_rows + r * d, *ov = dV_rows + r * d;
+            for (int64_t c = 0; c < d; ++c)
+                ok[c] = ov[c] = 0.0;
+            for (int64_t i = causal ? j : 0; i < N; ++i) {
+                double sdot = 0.0, pdot = 0.0;
+                for (int64_t c = 0; c < d; ++c) {
+                    sdot += (double)ROW(Q, i)[c] * (double)ROW(K, j)[c];
+                    pdot += (double)ROW(dO, i)[c] * (double)ROW(V, j)[c];
+                }
+                const double P = exp(scale * sdot - L[i]);
+                const double dS = P * (pdot - Dv[i]);
+                for (int64_t c = 0; c < d; ++c) {
+                    ok[c] += scale * dS * (double)ROW(Q, i)[c];
+                    ov[c] += P * (double)ROW(dO, i)[c];
+                }
+            }
+        }
+    }
+#undef ROW
+    free(L);
+    free(Dv);
 }
 
 /* Threads the OpenMP runtime will use for the parallel loops above. */

@@ -405,4 +405,117 @@ def pin_attention_qk_samples(lib):
     _close(lr, lse[sb, sh, si], 0.0, "qk sampled lse")
 
 
+# ---- backward ---------------------------------------------------------------
+
+def _dyadic(rng, shape, denom=64, span=2):
+    """Values k / denom in [-span, span): exactly representable in float32
+    with room for the +-2^-12 steps of the finite differences below."""
+    return (rng.integers(-span * denom, span * denom, size=shape) / denom).astype(np.float32)
+
+
+def pin_bwd_finite_differences(lib):
+    """Central differences of the (pinned) forward oracle's loss sum(dO * O)
+    against the backward oracle, entry by entry on a tiny problem."""
+    rng = np.random.default_rng(30)
+    for causal in (False, True):
+        B, N, H, d = 1, 5, 2, 3
+        Q, K, V, dO = (_dyadic(rng, (B, N, H, d)) for _ in range(4))
+        scale = 0.5
+        g = oracle.attention_bwd(Q, K, V, dO, scale, causal, lib=lib)
+        step = 2.0 ** -12
+
+        def loss(Qx, Kx, Vx):
+            O, _ = oracle.attention_dense(Qx, Kx, Vx, scale, causal, lib=lib)
+            return float((O * dO.astype(np.float64)).sum())
+
+        for name, X, key in (("Q", Q, "dQ"), ("K", K, "dK"), ("V", V, "dV")):
+            for idx in np.ndindex(X.shape):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[idx] += step
+                Xm[idx] -= step
+                args_p = [Q, K, V]
+                args_m = [Q, K, V]
+                pos = "QKV".index(name)
+                args_p[pos], args_m[pos] = Xp, Xm
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * step)
+                assert abs(fd - g[key][idx]) <= 1e-6 * max(1.0, abs(fd)), (
+                    f"d{name}{idx} causal={causal}: fd {fd} vs oracle {g[key][idx]}")
+
+
+def pin_bwd_vs_torch_autograd(lib):
+    """torch float64 autograd through an explicit softmax attention."""
+    import torch
+    rng = np.random.default_rng(31)
+    for (B, N, H, d, causal) in [(2, 9, 2, 8, True), (1, 13, 3, 4, False), (2, 6, 1, 16, True)]:
+        Q, K, V, dO = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(4))
+        scale = 1 / math.sqrt(d)
+        g = oracle.attention_bwd(Q, K, V, dO, scale, causal, lib=lib)
+        q, k, v = (torch.from_numpy(X.astype(np.float64)).permute(0, 2, 1, 3).requires_grad_()
+                   for X in (Q, K, V))
+        S = scale * q @ k.transpose(-1, -2)
+        if causal:
+            S = S.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+        O = torch.softmax(S, dim=-1) @ v
+        do = torch.from_numpy(dO.astype(np.float64)).permute(0, 2, 1, 3)
+        (O * do).sum().backward()
+        for key, t in (("dQ", q), ("dK", k), ("dV", v)):
+            _close(g[key], t.grad.permute(0, 2, 1, 3).numpy(), 1e-12,
+                   f"bwd {key} vs autograd N{N} causal={causal}")
+        _close(g["O"], O.detach().permute(0, 2, 1, 3).numpy(), 1e-12, "bwd O vs torch")
+
+
+def pin_bwd_invariants(lib):
+    """Exact identities of the gradients: sum_j dK_j = 0 (adding one vector to
+    every key leaves each row's softmax unchanged), sum_j dV_j = sum_i dO_i
+    (rows of P sum to one), D_i = dO_i . O_i, and under causal masking the first
+    query sees only key 0, so dQ_0 = 0."""
+    rng = np.random.default_rng(32)
+    B, N, H, d = 2, 17, 3, 8
+    Q, K, V, dO = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(4))
+    for causal in (False, True):
+        g = oracle.attention_bwd(Q, K, V, dO, 0.3, causal, lib=lib)
+        _close(g["dK"].sum(axis=1), np.zeros((B, H, d)), 1e-12, "sum_j dK_j")
+        _close(g["dV"].sum(axis=1), dO.astype(np.float64).sum(axis=1), 1e-12, "sum_j dV_j")
+        _close(g["D"], np.einsum("bihc,bihc->bhi", dO.astype(np.float64), g["O"]), 1e-12,
+               "D = dO . O")
+        if causal:
+            _close(g["dQ"][:, 0], np.zeros((B, H, d)), 1e-14, "causal dQ_0")
+
+
+def pin_bwd_uniform_scores(lib):
+    """Q = 0 makes every visible score equal: P_ij = 1 / n_i, so
+    dV_j = sum over the rows i that see j of dO_i / n_i (n_i = i + 1 causal),
+    and dK = 0 (dK_j = scale sum_i dS_ij q_i with q_i = 0)."""
+    rng = np.random.default_rng(33)
+    B, N, H, d = 1, 10, 2, 5
+    K, V, dO = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(3))
+    Q = np.zeros_like(K)
+    for causal in (False, True):
+        g = oracle.attention_bwd(Q, K, V, dO, 0.7, causal, lib=lib)
+        n_i = np.arange(1, N + 1) if causal else np.full(N, N)
+        w = dO.astype(np.float64) / n_i[None, :, None, None]
+        if causal:
+            expect = np.flip(np.cumsum(np.flip(w, axis=1), axis=1), axis=1)
+        else:
+            expect = np.broadcast_to(w.sum(axis=1, keepdims=True), w.shape)
+        _close(g["dV"], expect, 1e-13, f"uniform dV causal={causal}")
+        _close(g["dK"], np.zeros_like(g["dK"]), 1e-14, "uniform dK")
+
+
+def pin_bwd_head_matches_full(lib):
+    """The per-head sampled gradients equal the full computation."""
+    rng = np.random.default_rng(34)
+    B, N, H, d = 2, 23, 3, 8
+    Q, K, V, dO = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(4))
+    for causal in (False, True):
+        g = oracle.attention_bwd(Q, K, V, dO, 0.35, causal, lib=lib)
+        for (b, h) in [(0, 0), (1, 2)]:
+            qi, ki = [0, 5, 22], [0, 11, 22]
+            dq, dk, dv = oracle.attention_bwd_head(Q, K, V, dO, 0.35, causal, b, h, qi, ki,
+                                                   lib=lib)
+            _close(dq, g["dQ"][b, qi, h], 1e-12, "head dQ")
+            _close(dk, g["dK"][b, ki, h], 1e-12, "head dK")
+            _close(dv, g["dV"][b, ki, h], 1e-12, "head dV")
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

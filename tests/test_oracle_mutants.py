@@ -45,6 +45,14 @@ MUTANTS = [
     ("qk_offset_sign", "int64_t nvis = causal ? i + (Nk - Nq) + 1 : Nk;", "int64_t nvis = causal ? i + (Nq - Nk) + 1 : Nk;", 0),
     ("qk_key_stride_uses_nq", "const float *k = K + ((b * Nk + j) * H + h) * d;", "const float *k = K + ((b * Nq + j) * H + h) * d;", 0),
     ("qk_sample_head_ignored", "                h = samp_h[r];", "                h = 0;", 0),
+    ("bwd_ds_wrong_sign", "dP[i * N + j] = P[i * N + j] * (dP[i * N + j] - Di);", "dP[i * N + j] = P[i * N + j] * (dP[i * N + j] + Di);", 0),
+    ("bwd_ds_no_jacobian_term", "dP[i * N + j] = P[i * N + j] * (dP[i * N + j] - Di);", "dP[i * N + j] = P[i * N + j] * dP[i * N + j];", 0),
+    ("bwd_dq_scale_dropped", "ROW(dQ, i)[c] = scale * acc;", "ROW(dQ, i)[c] = acc;", 0),
+    ("bwd_dk_uses_keys", "acc_k += dP[i * N + j] * (double)ROW(Q, i)[c];", "acc_k += dP[i * N + j] * (double)ROW(K, i)[c];", 0),
+    ("bwd_dv_transposed_p", "acc_v += P[i * N + j] * (double)ROW(dO, i)[c];", "acc_v += P[j * N + i] * (double)ROW(dO, i)[c];", 0),
+    ("bwd_causal_dk_misses_diagonal", "for (int64_t i = causal ? j : 0; i < N; ++i) {\n                    acc_k", "for (int64_t i = causal ? j + 1 : 0; i < N; ++i) {\n                    acc_k", 0),
+    ("bwd_p_uses_max_not_lse", "P[i * N + j] = exp(P[i * N + j] - L);   /* [FG] §2.4 */", "P[i * N + j] = exp(P[i * N + j] - m);   /* [FG] §2.4 */", 0),
+    ("bwd_head_ds_wrong_sign", "const double dS = P * (pdot - Dv[i]);\n                for (int64_t c = 0; c < d; ++c)\n                    out", "const double dS = P * (pdot + Dv[i]);\n                for (int64_t c = 0; c < d; ++c)\n                    out", 0),
 ]
 
 
