@@ -7,7 +7,8 @@ to bf16; 192 MiB of Q/K/V, larger than the 129 MB L2), through the C ABI.
 The row softmax (fp32, 4096 x N, the HBM-resident lengths) is timed in the
 same run with L2 flushed before every repetition and reported under
 "softmax"; split-KV attention on a decode-like shape (256 queries, 32768 keys)
-under "splitkv".  Prints one JSON line (rank 0).
+under "splitkv"; the attention backward on the headline workload under
+"bwd".  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -56,6 +57,7 @@ def parse_args():
     ap.add_argument("--softmax-reps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-splitkv", action="store_true", help="skip the split-KV leg")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -445,6 +447,55 @@ def time_splitkv(fa, dev, reps, peaks, clocks):
             "l2": "K/V 256 MiB, larger than L2; %d back-to-back calls" % reps}
 
 
+def time_bwd(fa, w, dev, reps, peaks, clocks):
+    """Attention backward (dQ/D kernel + dK/dV kernel) on the headline
+    workload.  O and lse come from one forward call outside the timed region;
+    dO ~ N(0, 1) in bf16.  Algorithmic work = 2.5 x the forward's (the five
+    products dS-recompute, dP, dV, dK, dQ of 2 N^2 d each against the
+    forward's two; the kernels run seven, recomputing S and dP for dQ)."""
+    import torch
+    if w.varlen:
+        return None
+    Q, K, V = w.inputs()
+    q, k, v = (t.to(dev) for t in (Q, K, V))
+    rng = np.random.default_rng(w.seed + 77)
+    do = torch.from_numpy(rng.standard_normal(q.shape, dtype=np.float32)).to(torch.bfloat16).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    o, lse = fa.attention_fwd(q, k, v, causal=w.causal)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dbuf = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    args = [t.data_ptr() for t in (q, k, v, o, do, lse, dq, dk, dv, dbuf)]
+
+    def launch():
+        rc = fa.fa_attention_bwd(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal))
+        if rc != 0:
+            raise RuntimeError(fa.strerror(rc))
+
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(reps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(t0, time.time())
+    dev_err = fa.fa_get_device_error()
+    if dev_err != 0:
+        raise RuntimeError(f"device error word {dev_err:#x}")
+    ms = e0.elapsed_time(e1) / reps
+    flops = 2.5 * w.flops()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": w.name, "ms": ms, "TFLOP_per_s": tf,
+            "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "bound": "tensor",
+            "algorithmic_flops_per_call": flops, "executed_flops_per_call": 3.5 * w.flops(),
+            "launches_per_call": 2,
+            "l2": "inputs larger than L2 (Q/K/V/O/dO 320 MiB); %d back-to-back calls" % reps}
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -480,6 +531,9 @@ def main():
         splitkv = None
         if not args.no_splitkv and rank == 0:
             splitkv = time_splitkv(fa, dev, 50, peaks, clocks)
+        bwd = None
+        if not args.no_bwd and rank == 0:
+            bwd = time_bwd(fa, w, dev, 20, peaks, clocks)
     finally:
         clk = clocks.stop()
     e2e = None
@@ -504,6 +558,7 @@ def main():
         "clocks": clk,
         "softmax": softmax,
         "splitkv": splitkv,
+        "bwd": bwd,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -141,6 +141,28 @@ FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V,
                                     int causal, int num_splits, float *O_accum, float *lse_accum);
 
 /*
+ * Attention backward for the bf16 forward (dense batches): the gradients of
+ * sum(dO * O) with respect to Q, K and V, with the probabilities recomputed
+ * from the forward's row logsumexp ("少搬一趟…" §2.4: P_ij = exp(S_ij - L_i);
+ * "第二十二课…" §三十-三十一) and the chain rule written out:
+ *     dV = P^T dO,  dS = P o (dO V^T - D),  D_i = dO_i . O_i,
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ *   Q, K, V, O, dO: bf16 [B, N, H, d] (O and lse as written by fa_attention_fwd
+ *   for the same Q, K, V, scale and causal); lse: fp32 [B, H, N].
+ *   dQ, dK, dV: bf16 [B, N, H, d], written.
+ *   D_buf: fp32 [B, H, N] DEVICE scratch owned by the caller (receives D_i;
+ *   contents on entry are ignored).
+ *   d: 64 or 128; bf16 pointers 16-byte aligned, lse and D_buf 4-byte aligned.
+ * Two kernels run on the library stream (dQ and D, then dK and dV); no
+ * synchronisation.  Packed (cu_seqlens) batches are not supported here.
+ * Errors: FA_ERR_NULL_POINTER, FA_ERR_BAD_SIZE, FA_ERR_UNSUPPORTED (d),
+ * FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE, FA_ERR_NO_DEVICE, FA_ERR_CUDA.
+ */
+FA_API int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O,
+                            const void *dO, const float *lse, void *dQ, void *dK, void *dV,
+                            float *D_buf, int B, int H, int N, int d, float scale, int causal);
+
+/*
  * The split count fa_attention_fwd_splitkv uses for num_splits = 0 on the
  * current device: as many splits as fill the SMs in one wave (floor of SMs /
  * 256-query blocks, 1 when the blocks alone fill more than half of the SMs),

@@ -9,11 +9,11 @@ compiled library is missing, importing the C functions fails loudly.
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
-``fa_attention_fwd_f32``,
+``fa_attention_fwd_f32``, ``fa_attention_bwd``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
 ``fa_version``.
 Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
-:func:`attention_fwd_splitkv`.
+:func:`attention_fwd_splitkv`, :func:`attention_bwd`.
 """
 from __future__ import annotations
 
@@ -62,6 +62,8 @@ def lib():
         L.fa_attention_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp, vp]
         L.fa_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        L.fa_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                       i32, f32, i32]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                        i32, f32, i32, i32]
         L.fa_set_stream.argtypes = [vp]
@@ -73,7 +75,7 @@ def lib():
         L.fa_version.argtypes = []
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
-                     "fa_attention_fwd_splitkv_noalloc",
+                     "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
                      "fa_set_stream", "fa_get_device_error", "fa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -126,6 +128,11 @@ def fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, ca
                                      num_splits) -> int:
     return lib().fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale,
                                                   causal, num_splits)
+
+
+def fa_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale, causal) -> int:
+    return lib().fa_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale,
+                                  causal)
 
 
 def fa_set_stream(stream_ptr) -> int:
@@ -266,10 +273,39 @@ def attention_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = N
     return out, lse
 
 
+def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None):
+    """Attention backward through the C ABI (bf16, dense [B, N, H, d]).
+
+    ``o`` and ``lse`` are the forward's outputs for the same inputs.  The fp32
+    D scratch [B, H, N] is allocated here (torch).  Returns (dq, dk, dv).
+    """
+    import torch
+    for t in (q, k, v, o, do):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
+        if t.shape != q.shape:
+            raise ValueError("q, k, v, o, do must have one shape")
+    B, N, H, d = q.shape
+    if not (lse.is_cuda and lse.dtype == torch.float32 and lse.shape == (B, H, N)
+            and lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _use_current_stream(q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    d_buf = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), _ptr(d_buf), B, H, N, d, float(scale),
+                          int(bool(causal)))
+    _check(rc, "fa_attention_bwd")
+    return dq, dk, dv
+
+
 __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
     "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
+    "attention_bwd", "fa_attention_bwd",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
     "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",

@@ -683,44 +683,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// 3-D map over a [total, H, d] bf16 tensor; box = 64 head-dim elements (128
-// bytes, the 128-byte swizzle span) x 1 head x 128 tokens.  Rows past `total`
-// read as zero.
-bool make_tmap(CUtensorMap *tm, const void *base, int64_t total, int H, int d)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr)
-        return false;
-    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(total)};
-    const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(H) * d * 2};
-    const cuuint32_t box[3] = {64, 1, 128};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, bool SPLIT>
 int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 {
@@ -744,9 +706,10 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     Bf16Params p;
     const int Nk = a.Nk > 0 ? a.Nk : a.N;
     const int64_t total_k = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
-    if (!make_tmap(&p.tm_q, a.Q, a.total, a.H, a.d) || !make_tmap(&p.tm_k, a.K, total_k, a.H, a.d) ||
-        !make_tmap(&p.tm_v, a.V, total_k, a.H, a.d) ||
-        !make_tmap(&p.tm_o, a.O, a.total, a.H, a.d))
+    if (!make_tmap_bf16(&p.tm_q, a.Q, a.total, a.H, a.d) ||
+        !make_tmap_bf16(&p.tm_k, a.K, total_k, a.H, a.d) ||
+        !make_tmap_bf16(&p.tm_v, a.V, total_k, a.H, a.d) ||
+        !make_tmap_bf16(&p.tm_o, a.O, a.total, a.H, a.d))
         return FA_ERR_CUDA;
     p.Nk = Nk;
     p.kv_off = a.kv_off;

@@ -227,6 +227,51 @@ int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V, void *
     return fa::launch_attention_bf16(a, fa::t_stream);
 }
 
+int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *lse, void *dQ, void *dK, void *dV, float *D_buf, int B, int H,
+                     int N, int d, float scale, int causal)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0)
+        return FA_OK;
+    if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !D_buf)
+        return FA_ERR_NULL_POINTER;
+    const void *bf[8] = {Q, K, V, O, dO, dQ, dK, dV};
+    for (const void *ptr : bf)
+        if (!fa::aligned(ptr, 16))
+            return FA_ERR_MISALIGNED;
+    if (!fa::aligned(lse, 4) || !fa::aligned(D_buf, 4))
+        return FA_ERR_MISALIGNED;
+    const int64_t total = int64_t(B) * N;
+    if (total > (int64_t(1) << 31) - 512 || total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+        return FA_ERR_TOO_LARGE;
+    fa::DeviceInfo *dev = fa::current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    fa::AttnBwdArgs a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.dO = dO;
+    a.lse = lse;
+    a.dQ = dQ;
+    a.dK = dK;
+    a.dV = dV;
+    a.D = D_buf;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.err_word = dev->err_word;
+    return fa::launch_attention_bwd(a, fa::t_stream);
+}
+
 int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,
                          int B, int H, int N, int d, float scale, int causal,
                          const int32_t *cu_seqlens)

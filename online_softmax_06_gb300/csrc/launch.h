@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fa {
@@ -39,5 +40,23 @@ int launch_attention_combine(const AttnArgs &a, cudaStream_t stream);
 
 // Number of key splits the library picks for a dense problem (>= 1).
 int choose_num_splits(int B, int H, int N, int Nk);
+
+// 3-D TMA map over a [total, H, d] bf16 tensor: box = 64 head-dim elements
+// (128 bytes, the 128-byte swizzle span) x 1 head x 128 rows; rows past
+// `total` read as zero.  False if the driver refuses the map.
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d);
+
+// Backward of the bf16 attention (dense [B, N, H, d]); layouts as in fa.h.
+struct AttnBwdArgs {
+    const void *Q, *K, *V, *O, *dO;
+    const float *lse;          // [B, H, N], natural log, from the forward
+    void *dQ, *dK, *dV;
+    float *D;                  // [B, H, N] scratch: D_i = dO_i . O_i
+    int B, H, N, d;
+    float scale;
+    int causal;
+    int *err_word;
+};
+int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
 
 }  // namespace fa

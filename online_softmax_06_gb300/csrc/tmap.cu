@@ -1,0 +1,54 @@
+// tmap.cu -- TMA tensor maps over the [rows, H, d] bf16 tensors of the
+// attention kernels (built on the host, passed to kernels as __grid_constant__
+// parameters).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+
+namespace fa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime (the
+// library links no driver stub).
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(total)};
+    const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(H) * d * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fa

@@ -67,6 +67,14 @@ def test_host_validation_without_gpu(lib):
     assert fa.fa_attention_fwd_varlen(None, None, None, None, None, 1, 1, 1, 1, 64, 1.0, 0,
                                       None) == -1
     assert fa.fa_attention_fwd_f32(None, None, None, None, None, 1, -1, 1, 64, 1.0, 0, None) == -2
+    assert fa.fa_attention_bwd(None, None, None, None, None, None, None, None, None, None,
+                               1, 1, -1, 64, 1.0, 0) == -2
+    assert fa.fa_attention_bwd(None, None, None, None, None, None, None, None, None, None,
+                               1, 1, 8, 80, 1.0, 0) == -3
+    assert fa.fa_attention_bwd(None, None, None, None, None, None, None, None, None, None,
+                               0, 1, 8, 64, 1.0, 0) == 0
+    assert fa.fa_attention_bwd(None, None, None, None, None, None, None, None, None, None,
+                               1, 1, 8, 64, 1.0, 0) == -1
     nl = fa.fa_attention_fwd_splitkv_noalloc
     assert nl(None, None, None, None, None, 1, 1, -1, 8, 64, 1.0, 0, 0) == -2
     assert nl(None, None, None, None, None, 1, 1, 9, 8, 64, 1.0, 1, 0) == -2   # causal Nk < Nq
