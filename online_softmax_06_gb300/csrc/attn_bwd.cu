@@ -14,20 +14,24 @@
 //
 // Two kernels, launched in this order on one stream:
 //   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile).  Each
-//     thread of warps 0-3 owns one query row: it forms D_i = dO_i . O_i (and
-//     stores it for the second kernel), then for every visible key tile j
+//     query row is served by two threads (64 columns each): they form
+//     D_i = dO_i . O_i (stored for the second kernel), then for every visible key tile j
 //     turns S = Q K_j^T and dP = dO V_j^T (tcgen05, fp32 in TMEM) into
 //     dS = P o (dP - D_i) in bf16 in TMEM, and the MMA warp accumulates
 //     dQ += dS K_j in TMEM.
 //   * attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key tile), K and
 //     V resident in shared memory.  For every query tile i that sees the keys,
 //     S^T = K Q_i^T and dP^T = V dO_i^T land in TMEM with one key per TMEM
-//     lane; each thread of warps 0-3 owns one key row and forms P^T and dS^T
+//     lane; the two threads of each key row form P^T and dS^T
 //     (bf16, in TMEM) from the query tile's logsumexp and D (staged in shared
 //     memory by the load warp), and the MMA warp accumulates dV += P^T dO_i and
 //     dK += dS^T Q_i.
-// In both, warp 4 issues TMA loads into a ring of shared-memory stages and
-// warp 5 owns the tensor memory and issues every tcgen05.mma.  Every wait is
+// The elementwise work (P, dS) needs no reduction along a row, so a row's 128
+// columns are split between two threads: warps 0-7 serve the rows (warp w:
+// TMEM lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63), which hides
+// more of the exp and TMEM latencies than one thread per row.  Warp 8 issues
+// TMA loads into a ring of shared-memory stages and warp 9 owns the tensor
+// memory and issues every tcgen05.mma.  Every wait is
 // bounded; a wait that gives up raises the error word and the abort flag, the
 // roles leave their loops, in-flight copies and MMAs drain, and the CTA frees
 // its tensor memory.
@@ -48,9 +52,12 @@ namespace fa {
 namespace {
 
 constexpr int BT = 128;                     // rows of a Q, K, V or dO tile
-constexpr int kThreads = 192;               // warps 0-3 rows, 4 TMA, 5 MMA
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
+constexpr int G = 2;                        // threads per row (column groups)
+constexpr int kColsPerThread = BT / G;
+constexpr int kRowWarps = 4 * G;
+constexpr int kThreads = 32 * (kRowWarps + 2);
+constexpr int kWarpLoad = kRowWarps;
+constexpr int kWarpMma = kRowWarps + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kChunkBytes = BT * 128;  // 128 rows x 128 bytes (64 bf16)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -74,9 +81,15 @@ struct Cfg {
 };
 
 // TMEM columns: S (or S^T) [0, 128), dP (or dP^T) [128, 256), accumulators from
-// 256 (dQ; or dV then dK).  bf16 P / dS are packed over the first 64 columns of
-// the region they are formed from.
+// 256 (dQ; or dV then dK).  bf16 P / dS are packed into the region they are
+// formed from: the 32 values of each 32-column block go to the block's first 16
+// columns (two per column), so a thread only overwrites columns it has read.
 constexpr uint32_t kColS = 0, kColP = 128, kColAcc = 256;
+// Column of the packed bf16 operand for the MMA's K step kk (16 values).
+__host__ __device__ constexpr uint32_t packed_col(int kk)
+{
+    return uint32_t(32 * (kk >> 1) + 8 * (kk & 1));
+}
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;    // [B*N, H, d] bf16, box {64, 1, 128}
@@ -138,7 +151,7 @@ __device__ __forceinline__ uint32_t setup(const BwdParams &p, uint8_t *smem, con
             ptx::mbar_init(&bar.kv_empty[s], 1);
         }
         ptx::mbar_init(bar.s_full, 1);
-        ptx::mbar_init(bar.p_full, BT);
+        ptx::mbar_init(bar.p_full, BT * G);
         ptx::mbar_init(bar.o_full, 1);
         ptx::mbar_init(bar.drain, 1);
         *abort_flag = 0;
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dkn = ptx::smem_desc(desc_mnmajor, k_addr);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + kk * 8,
+                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + packed_col(kk),
                                     dkn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(&bar.kv_empty[k_stage]);
@@ -349,14 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ======================= query rows ================================
-        const int r = threadIdx.x;                   // query row in the tile = TMEM lane
+        const int r = (warp & 3) * 32 + lane;        // query row in the tile = TMEM lane
+        const int g = warp >> 2;                     // column group
         const int i = qt * BT + r;
         const bool row_ok = i < p.N;
-        const uint32_t lane_bits = uint32_t(warp * 32) << 16;
+        const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_bits + kColS;
         const uint32_t tP = tmem + lane_bits + kColP;
         const int64_t stat = (int64_t(b) * p.H + h) * p.N + i;
-        // D_i = dO_i . O_i (fp32), kept here and stored for the dK/dV kernel
+        // D_i = dO_i . O_i (fp32); group 0 stores it for the dK/dV kernel
         float Di = 0.f, lse2 = 0.f;
         if (row_ok) {
             const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + ((row0 + i) * p.H + h) * D);
@@ -368,13 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[e]));
-                    const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[e]));
+                    const float2 of =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[e]));
+                    const float2 gf =
+                        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[e]));
                     Di = fmaf(of.x, gf.x, Di);
                     Di = fmaf(of.y, gf.y, Di);
                 }
             }
-            p.D[stat] = Di;
+            if (g == 0)
+                p.D[stat] = Di;
             lse2 = p.lse[stat] * kLog2e;
         }
         const float sl = p.scale_log2;
@@ -395,39 +412,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!row_ok)
                 lim = -1;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t s[2][32], dp[2][32];
-                ptx::tmem_ld32(tS + half * 64, s[0]);
-                ptx::tmem_ld32(tS + half * 64 + 32, s[1]);
-                ptx::tmem_ld32(tP + half * 64, dp[0]);
-                ptx::tmem_ld32(tP + half * 64 + 32, dp[1]);
+            for (int blk = 0; blk < kColsPerThread / 32; ++blk) {
+                const int col0 = g * kColsPerThread + blk * 32;
+                uint32_t sv[32], dv[32], pk[16];
+                ptx::tmem_ld32(tS + col0, sv);
+                ptx::tmem_ld32(tP + col0, dv);
                 ptx::tmem_wait_ld();
-                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c0 = half * 64 + 2 * e;
+                for (int e = 0; e < 16; ++e) {
                     float ds[2];
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        const int c = c0 + k;
-                        const float sv = __uint_as_float(s[(2 * e + k) >> 5][(2 * e + k) & 31]);
-                        const float dv = __uint_as_float(dp[(2 * e + k) >> 5][(2 * e + k) & 31]);
-                        const float pv = c <= lim ? ptx::ex2(fmaf(sv, sl, -lse2)) : 0.f;
-                        ds[k] = pv * (dv - Di);
+                        const int c = col0 + 2 * e + k;
+                        const float x = __uint_as_float(sv[2 * e + k]);
+                        const float y = __uint_as_float(dv[2 * e + k]);
+                        // masked entries get exponent -inf: exp2 gives 0, no branch
+                        const float pv = ptx::ex2(c <= lim ? fmaf(x, sl, -lse2) : -INFINITY);
+                        ds[k] = pv * (y - Di);
                     }
                     pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
                 }
-                // columns [32 half, 32 half + 32) were read in half 0 already
-                ptx::tmem_st32(tS + half * 32, pk);
+                ptx::tmem_st16(tS + col0, pk);        // dS of this block, packed
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(bar.p_full);
         }
+        // the epilogue reads each row's dQ once: group 0 stores it
         if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
-            store_row<D>(tmem + lane_bits + kColAcc, p.scale,
-                         p.dQ + ((row0 + i) * p.H + h) * D, row_ok);
+            if (g == 0)
+                store_row<D>(tmem + lane_bits + kColAcc, p.scale,
+                             p.dQ + ((row0 + i) * p.H + h) * D, row_ok);
         }
     }
     teardown<D>(tmem);
@@ -594,12 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dq_mn = ptx::smem_desc(desc_mnmajor, q_addr);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + kk * 8,
+                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + packed_col(kk),
                                     ddo_mn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc + D, tmem + kColP + kk * 8,
+                        ptx::mma_ts(tmem + kColAcc + D, tmem + kColP + packed_col(kk),
                                     dq_mn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (s > 0 || kk > 0) ? 1u : 0u);
                     ptx::mma_commit(&bar.kv_empty[q_stage]);
@@ -614,9 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ======================= key rows ==================================
-        const int r = threadIdx.x;                   // key row in the tile = TMEM lane
+        const int r = (warp & 3) * 32 + lane;        // key row in the tile = TMEM lane
+        const int g = warp >> 2;                     // column group
         const int k = kt * BT + r;
-        const uint32_t lane_bits = uint32_t(warp * 32) << 16;
+        const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_bits + kColS;
         const uint32_t tP = tmem + lane_bits + kColP;
         const float sl = p.scale_log2;
@@ -641,17 +658,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (hi > BT - 1)
                 hi = BT - 1;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t sv[2][32], dv[2][32];
-                ptx::tmem_ld32(tS + half * 64, sv[0]);
-                ptx::tmem_ld32(tS + half * 64 + 32, sv[1]);
-                ptx::tmem_ld32(tP + half * 64, dv[0]);
-                ptx::tmem_ld32(tP + half * 64 + 32, dv[1]);
+            for (int blk = 0; blk < kColsPerThread / 32; ++blk) {
+                const int col0 = g * kColsPerThread + blk * 32;
+                uint32_t sv[32], dv[32], pk[16], dk[16];
+                ptx::tmem_ld32(tS + col0, sv);
+                ptx::tmem_ld32(tP + col0, dv);
                 ptx::tmem_wait_ld();
-                uint32_t pk[32], dk[32];
 #pragma unroll
-                for (int e4 = 0; e4 < 16; ++e4) {
-                    const int c0 = half * 64 + 4 * e4;
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const int c0 = col0 + 4 * e4;
                     const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + c0);
                     const float4 d4 = *reinterpret_cast<const float4 *>(Ds + c0);
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
@@ -659,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float pv[4], ds[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int e = 4 * e4 + u;     // 0..63 within the half
                         const int c = c0 + u;
-                        const float x = __uint_as_float(sv[e >> 5][e & 31]);
-                        const float y = __uint_as_float(dv[e >> 5][e & 31]);
-                        pv[u] = (c >= lo && c <= hi) ? ptx::ex2(fmaf(x, sl, -lv[u])) : 0.f;
+                        const float x = __uint_as_float(sv[4 * e4 + u]);
+                        const float y = __uint_as_float(dv[4 * e4 + u]);
+                        // masked entries get exponent -inf: exp2 gives 0, no branch
+                        pv[u] = ptx::ex2((c >= lo && c <= hi) ? fmaf(x, sl, -lv[u]) : -INFINITY);
                         ds[u] = pv[u] * (y - dd[u]);
                     }
                     pk[2 * e4] = ptx::pack_bf16x2(pv[0], pv[1]);
@@ -671,8 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dk[2 * e4] = ptx::pack_bf16x2(ds[0], ds[1]);
                     dk[2 * e4 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
                 }
-                ptx::tmem_st32(tS + half * 32, pk);
-                ptx::tmem_st32(tP + half * 32, dk);
+                ptx::tmem_st16(tS + col0, pk);        // P^T of this block, packed
+                ptx::tmem_st16(tP + col0, dk);        // dS^T of this block, packed
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
@@ -681,10 +696,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
             const bool key_ok = k < p.N;
-            store_row<D>(tmem + lane_bits + kColAcc, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
-                         key_ok);
-            store_row<D>(tmem + lane_bits + kColAcc + D, p.scale,
-                         p.dK + ((row0 + k) * p.H + h) * D, key_ok);
+            // group 0 writes dV, group 1 writes dK
+            if (g == 0)
+                store_row<D>(tmem + lane_bits + kColAcc, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
+                             key_ok);
+            if (g == 1)
+                store_row<D>(tmem + lane_bits + kColAcc + D, p.scale,
+                             p.dK + ((row0 + k) * p.H + h) * D, key_ok);
         }
     }
     teardown<D>(tmem);

@@ -42,9 +42,10 @@ int launch_attention_combine(const AttnArgs &a, cudaStream_t stream);
 int choose_num_splits(int B, int H, int N, int Nk);
 
 // 3-D TMA map over a [total, H, d] bf16 tensor: box = 64 head-dim elements
-// (128 bytes, the 128-byte swizzle span) x 1 head x 128 rows; rows past
-// `total` read as zero.  False if the driver refuses the map.
-bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d);
+// (128 bytes, the 128-byte swizzle span) x 1 head x box_rows rows (128 unless
+// given); rows past `total` read as zero.  False if the driver refuses the map.
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d,
+                    int box_rows = 128);
 
 // Backward of the bf16 attention (dense [B, N, H, d]); layouts as in fa.h.
 struct AttnBwdArgs {
