@@ -518,4 +518,125 @@ def pin_bwd_head_matches_full(lib):
             _close(dv, g["dV"][b, ki, h], 1e-12, "head dV")
 
 
+# ---- FP8 (blockwise quantisation + incoherent processing) -------------------
+
+def _e4m3_table():
+    """All finite e4m3 values from the format definition: sign, 4 exponent
+    bits (bias 7), 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6);
+    exponent 15 with mantissa 7 is NaN (no infinities); the largest value is
+    1.75 * 2^8 = 448."""
+    vals, codes = [], []
+    for code in range(256):
+        sgn = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 0x7
+        if e == 15 and m == 7:
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(sgn * v)
+        codes.append(code)
+    return np.array(vals), np.array(codes)
+
+
+def pin_fp8_e4m3_brute_force(lib):
+    """torch's e4m3 rounding (the reference's quantiser) against a brute-force
+    nearest-value search over the format's code table, ties to the even code,
+    saturating at +-448."""
+    from oracle import fp8
+    vals, codes = _e4m3_table()
+    rng = np.random.default_rng(40)
+    x = np.concatenate([rng.uniform(-500, 500, 4000), rng.uniform(-0.05, 0.05, 4000),
+                        vals, (vals[:-1] + vals[1:]) / 2 if False else [],
+                        [3.14159, 460.0, -460.0, 2.0 ** -10, 2.0 ** -9, 0.0]])
+    # midpoints between neighbouring positive values exercise ties-to-even
+    pos = np.unique(np.abs(vals))
+    x = np.concatenate([x, (pos[:-1] + pos[1:]) / 2, -(pos[:-1] + pos[1:]) / 2])
+    got = fp8.e4m3_round(x)
+    xc = np.clip(x, -448.0, 448.0)
+    d = np.abs(xc[:, None] - vals[None, :])
+    best = d.min(axis=1, keepdims=True)
+    ties = d <= best + 0.0
+    # among the nearest values take the even code (mantissa LSB 0)
+    even = (codes[None, :] & 1) == 0
+    pick = np.where(ties & even, 1, 0).argmax(axis=1)
+    has_even = (ties & even).any(axis=1)
+    expect = np.where(has_even, vals[pick], vals[ties.argmax(axis=1)])
+    expect = np.where(expect == 0, 0.0, expect)
+    assert np.array_equal(np.abs(got), np.abs(expect)) and np.all(
+        (got == 0) | (np.sign(got) == np.sign(xc))), "e4m3 rounding differs from the table"
+
+
+def pin_fp8_hadamard_vs_scipy(lib):
+    """The Sylvester construction equals scipy's Hadamard matrix."""
+    from scipy.linalg import hadamard
+    from oracle import fp8
+    for d in (1, 2, 4, 8, 16, 32, 64, 128):
+        assert np.array_equal(fp8.sylvester_hadamard(d), hadamard(d).astype(np.float64))
+
+
+def pin_fp8_rotation_orthogonal(lib):
+    """M M^T = I and (QM)(KM)^T = QK^T ([FG] §4.6), and attention is unchanged."""
+    from oracle import fp8
+    rng = np.random.default_rng(41)
+    for d in (64, 128):
+        signs = rng.choice([-1.0, 1.0], size=d)
+        M = fp8.rotation_matrix(signs)
+        _close(M @ M.T, np.eye(d), 1e-14, f"M M^T d={d}")
+        Q = rng.standard_normal((1, 7, 2, d)).astype(np.float32)
+        K = rng.standard_normal((1, 7, 2, d)).astype(np.float32)
+        V = rng.standard_normal((1, 7, 2, d)).astype(np.float32)
+        S = np.einsum("bihc,bjhc->bhij", Q.astype(np.float64), K.astype(np.float64))
+        Sr = np.einsum("bihc,bjhc->bhij", fp8.rotate(Q, signs), fp8.rotate(K, signs))
+        _close(Sr, S, 1e-12, "rotated scores")
+        O, lse = oracle.attention_dense(Q, K, V, 1 / math.sqrt(d), True, lib=lib)
+        Or, lr = oracle.attention_dense(fp8.rotate(Q, signs).astype(np.float32),
+                                        fp8.rotate(K, signs).astype(np.float32), V,
+                                        1 / math.sqrt(d), True, lib=lib)
+        _close(Or, O, 1e-5, "attention of rotated Q, K")
+        _close(lr, lse, 1e-5, "lse of rotated Q, K")
+
+
+def pin_fp8_blockwise_scales(lib):
+    """Each block's largest magnitude lands exactly on +-448 after scaling, and
+    every quantised value is within half an e4m3 step (relative 2^-4) of its
+    input, or below the subnormal range."""
+    from oracle import fp8
+    rng = np.random.default_rng(42)
+    X = rng.standard_normal((2, 300, 3, 64)) * rng.uniform(0.1, 10, size=(1, 1, 3, 1))
+    deq, scales = fp8.blockwise_qk(X)
+    assert scales.shape == (2, 3, 3)
+    for t in range(3):
+        blk = X[:, t * 128:(t + 1) * 128]
+        q = deq[:, t * 128:(t + 1) * 128] / scales[:, None, :, t, None]
+        _close(np.abs(q).max(axis=(1, 3)), np.full((2, 3), 448.0), 1e-12, "block amax -> 448")
+        rel = np.abs(deq[:, t * 128:(t + 1) * 128] - blk) / np.maximum(np.abs(blk), 1e-300)
+        tiny = np.abs(blk) / scales[:, None, :, t, None] < 2.0 ** -6
+        assert np.all((rel <= 2.0 ** -4 + 1e-12) | tiny)
+
+
+def pin_fp8_incoherent_processing_helps(lib):
+    """The pages' claim ([FG] §4.6, a test with outliers: per-tensor FP8 RMSE
+    2.4e-2 against 9.1e-3 with blockwise scales and the rotation).  Reading of
+    "outliers": 0.1 % of the entries of Q, K and V scaled by 10.  The method's
+    error against exact attention is of the pages' order and below the
+    per-tensor, unrotated baseline's (1.35-1.66x over six seeds here; e4m3's
+    error is relative, so only the values an outlier pushes towards the
+    subnormal range lose precision)."""
+    from oracle import fp8
+    rng = np.random.default_rng(104)
+    B, N, H, d = 1, 512, 2, 128
+    Q, K, V = (rng.standard_normal((B, N, H, d)) for _ in range(3))
+    for X in (Q, K, V):
+        X[rng.random(X.shape) < 0.001] *= 10.0
+    Q, K, V = (x.astype(np.float32) for x in (Q, K, V))
+    signs = rng.choice([-1.0, 1.0], size=d)
+    scale = 1 / math.sqrt(d)
+    O, _ = oracle.attention_dense(Q, K, V, scale, False, lib=lib)
+    Of, _ = fp8.fp8_attention(Q, K, V, signs, scale, False, lib=lib)
+    Ob, _ = fp8.fp8_attention(Q, K, V, signs, scale, False, per_tensor_scales=True,
+                              rotate_qk=False, lib=lib)
+    rmse = float(np.sqrt(np.mean((Of - O) ** 2)))
+    rmse_b = float(np.sqrt(np.mean((Ob - O) ** 2)))
+    assert rmse < 1.5e-2 and rmse < rmse_b / 1.2, (rmse, rmse_b)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
