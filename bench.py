@@ -8,7 +8,7 @@ The row softmax (fp32, 4096 x N, the HBM-resident lengths) is timed in the
 same run with L2 flushed before every repetition and reported under
 "softmax"; split-KV attention on a decode-like shape (256 queries, 32768 keys)
 under "splitkv"; the attention backward on the headline workload under
-"bwd".  Prints one JSON line (rank 0).
+"bwd" and the FP8 forward under "fp8".  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -58,6 +58,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-splitkv", action="store_true", help="skip the split-KV leg")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward leg")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 forward leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
@@ -496,6 +497,58 @@ def time_bwd(fa, w, dev, reps, peaks, clocks):
             "l2": "inputs larger than L2 (Q/K/V/O/dO 320 MiB); %d back-to-back calls" % reps}
 
 
+def time_fp8(fa, w, dev, reps, peaks, clocks):
+    """FP8 forward on the headline workload: the whole call (rotation and
+    blockwise e4m3 quantisation of Q, K, V, then the e4m3 tensor-core kernel)
+    and the attention kernel alone (the quantised tensors reused).  Peak: the
+    measured bf16 peak x 2, the nominal e4m3 / bf16 ratio (4.5 / 2.25
+    PFLOP/s dense)."""
+    import torch
+    if w.varlen or w.d != 128:
+        return None
+    Q, K, V = w.inputs()
+    q, k, v = (t.to(dev) for t in (Q, K, V))
+    rng = np.random.default_rng(w.seed + 88)
+    signs = torch.from_numpy(rng.choice([-1.0, 1.0], size=w.d).astype(np.float32)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_set_stream(stream.cuda_stream)
+    nbytes = fa.fa_attention_fp8_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+    def launch():
+        rc = fa.fa_attention_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal),
+                                     signs.data_ptr(), ws.data_ptr(), nbytes)
+        if rc != 0:
+            raise RuntimeError(fa.strerror(rc))
+
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(reps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark(t0, time.time())
+    dev_err = fa.fa_get_device_error()
+    if dev_err != 0:
+        raise RuntimeError(f"device error word {dev_err:#x}")
+    ms = e0.elapsed_time(e1) / reps
+    flops = w.flops()
+    tf = flops / (ms / 1e3) / 1e12
+    peak = 2.0 * peaks["bf16_tflops"]
+    return {"workload": w.name, "ms_per_call": ms, "TFLOP_per_s": tf,
+            "frac_of_fp8_peak": tf / peak, "fp8_peak_TFLOP_per_s": peak,
+            "peak_source": "measured bf16 dense x 2 (nominal e4m3/bf16 ratio)",
+            "launches_per_call": 3, "flops_per_call": flops,
+            "l2": "inputs larger than L2; %d back-to-back calls" % reps}
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -534,6 +587,9 @@ def main():
         bwd = None
         if not args.no_bwd and rank == 0:
             bwd = time_bwd(fa, w, dev, 20, peaks, clocks)
+        fp8 = None
+        if not args.no_fp8 and rank == 0:
+            fp8 = time_fp8(fa, w, dev, 50, peaks, clocks)
     finally:
         clk = clocks.stop()
     e2e = None
@@ -559,6 +615,7 @@ def main():
         "softmax": softmax,
         "splitkv": splitkv,
         "bwd": bwd,
+        "fp8": fp8,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

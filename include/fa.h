@@ -163,6 +163,39 @@ FA_API int fa_attention_bwd(const void *Q, const void *K, const void *V, const v
                             float *D_buf, int B, int H, int N, int d, float scale, int causal);
 
 /*
+ * FP8 attention forward ("少搬一趟…" §4.6: FP8 with blockwise quantisation and
+ * incoherent processing), for bf16 inputs on dense batches:
+ *   1. Q and K rows are multiplied by M = diag(signs) H_d / sqrt(d) (H_d the
+ *      Sylvester-Hadamard matrix): (QM)(KM)^T = Q K^T, large components spread
+ *      over the row;
+ *   2. each 128-row tile of a head of QM and KM, and each head of V, gets a
+ *      scale amax / 448 and is rounded to e4m3 (nearest even, saturating);
+ *   3. the attention runs on the tensor cores with e4m3 operands (P also in
+ *      e4m3), fp32 accumulation, the scales folded back in; O is bf16.
+ *   Q, K, V, O: bf16 [B, N, H, d]; lse: fp32 [B, H, N] (natural log);
+ *   causal: key j visible to query i iff j <= i.
+ *   signs: DEVICE fp32 [d] of +1 / -1 (the random signs of M, drawn by the
+ *   caller; any fixed draw gives the same result up to rounding).
+ *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
+ *   fa_attention_fp8_workspace_bytes(B, H, N, d) bytes; contents on entry are
+ *   ignored.  It receives, in this order, each part starting on a 256-byte
+ *   boundary (T = ceil(N / 128)): e4m3 Q M / sq [B*N, H, d], e4m3 K M / sk
+ *   [B*N, H, d], e4m3 V^T / sv [B, H, d, 128 T], fp32 sq and sk [B, H, T],
+ *   fp32 per-tile amax of V [B, H, T], fp32 sv [B, H].
+ *   d: 128 only.
+ * Three kernels run on the library stream; no synchronisation.
+ * Errors: FA_ERR_UNSUPPORTED (d != 128), FA_ERR_BAD_SIZE (also a workspace
+ * that is too small), FA_ERR_NULL_POINTER, FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE,
+ * FA_ERR_NO_DEVICE, FA_ERR_CUDA.
+ */
+FA_API int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, float *lse,
+                                int B, int H, int N, int d, float scale, int causal,
+                                const float *signs, void *workspace, int64_t workspace_bytes);
+
+/* Workspace bytes fa_attention_fwd_fp8 needs, or a negative FA_ERR_* code. */
+FA_API int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * The split count fa_attention_fwd_splitkv uses for num_splits = 0 on the
  * current device: as many splits as fill the SMs in one wave (floor of SMs /
  * 256-query blocks, 1 when the blocks alone fill more than half of the SMs),

@@ -9,11 +9,12 @@ compiled library is missing, importing the C functions fails loudly.
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
-``fa_attention_fwd_f32``, ``fa_attention_bwd``,
+``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_fwd_fp8``,
+``fa_attention_fp8_workspace_bytes``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
 ``fa_version``.
 Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
-:func:`attention_fwd_splitkv`, :func:`attention_bwd`.
+:func:`attention_fwd_splitkv`, :func:`attention_bwd`, :func:`attention_fwd_fp8`.
 """
 from __future__ import annotations
 
@@ -62,6 +63,10 @@ def lib():
         L.fa_attention_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                                                i32, i32, vp, vp]
         L.fa_splitkv_num_splits.argtypes = [i32, i32, i32, i32, i32]
+        L.fa_attention_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp,
+                                           vp, i64]
+        L.fa_attention_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.fa_attention_fp8_workspace_bytes.restype = i64
         L.fa_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                        i32, f32, i32]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -75,7 +80,7 @@ def lib():
         L.fa_version.argtypes = []
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
-                     "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
+                     "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd", "fa_attention_fwd_fp8",
                      "fa_set_stream", "fa_get_device_error", "fa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -128,6 +133,16 @@ def fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, ca
                                      num_splits) -> int:
     return lib().fa_attention_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale,
                                                   causal, num_splits)
+
+
+def fa_attention_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, causal, signs, workspace,
+                         workspace_bytes) -> int:
+    return lib().fa_attention_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, causal, signs,
+                                      workspace, workspace_bytes)
+
+
+def fa_attention_fp8_workspace_bytes(B, H, N, d) -> int:
+    return lib().fa_attention_fp8_workspace_bytes(B, H, N, d)
 
 
 def fa_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale, causal) -> int:
@@ -273,6 +288,38 @@ def attention_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = N
     return out, lse
 
 
+def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None = None,
+                      workspace=None):
+    """FP8 attention forward through the C ABI (bf16 dense [B, N, H, d], d = 128).
+
+    ``signs``: float32 CUDA tensor [d] of +-1.  The workspace (uint8, sized by
+    fa_attention_fp8_workspace_bytes) is allocated here unless given.
+    Returns (O [B, N, H, d] bf16, lse [B, H, N] fp32, workspace).
+    """
+    import torch
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+        if t.shape != q.shape:
+            raise ValueError("q, k, v must have one shape")
+    B, N, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = fa_attention_fp8_workspace_bytes(B, H, N, d)
+    if nbytes < 0:
+        raise FaError(int(nbytes), "fa_attention_fp8_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=q.device)
+    _use_current_stream(q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_attention_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                              float(scale), int(bool(causal)), _ptr(signs), _ptr(workspace),
+                              workspace.numel())
+    _check(rc, "fa_attention_fwd_fp8")
+    return o, lse, workspace
+
+
 def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None):
     """Attention backward through the C ABI (bf16, dense [B, N, H, d]).
 
@@ -305,7 +352,8 @@ __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
     "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
-    "attention_bwd", "fa_attention_bwd",
+    "attention_bwd", "fa_attention_bwd", "attention_fwd_fp8", "fa_attention_fwd_fp8",
+    "fa_attention_fp8_workspace_bytes",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
     "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",

@@ -68,14 +68,18 @@ template <int D>
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + uint32_t(t) * D; }
 constexpr uint32_t kChunkBytes = BM * 128;  // 128 rows x 128 bytes (64 bf16)
 
-template <int D>
+// FP8: Q, K and V arrive as e4m3 (one byte per element; V transposed per
+// head, keys contiguous), so a 128-row tile of d = 128 is one 128-byte chunk.
+template <int D, bool FP8 = false>
 struct Cfg {
-    static constexpr int kChunks = D / 64;                  // 128-byte column chunks
-    static constexpr uint32_t kTileBytes = BM * D * 2;      // one Q, K or V tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;      // K/V ring depth
+    static constexpr int kChunks = FP8 ? 1 : D / 64;        // 128-byte column chunks
+    static constexpr uint32_t kTileBytes = BM * D * (FP8 ? 1 : 2);   // one Q, K or V tile
+    static constexpr int kStages = (D == 128 && !FP8) ? 4 : 8;      // K/V ring depth
+    // a Q buffer also stages the tile's bf16 O for the epilogue's TMA store
+    static constexpr uint32_t kQBytes = BM * D * 2;
     // shared memory: [Q0][Q1][ring x kStages][barriers, flags]
     static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffRing = 2 * kTileBytes;
+    static constexpr uint32_t kOffRing = 2 * kQBytes;
     static constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
     static constexpr uint32_t kBarBytes = 8 * (2 + 2 * kStages + 2 + 2 + 2 + 1);
     static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;  // +1024 align slack
@@ -84,6 +88,10 @@ struct Cfg {
 struct Bf16Params {
     CUtensorMap tm_q, tm_k, tm_v;    // 3-D maps over [rows, H, d] bf16, box {64, 1, 128}
     CUtensorMap tm_o;                // the same over O (stores of whole tiles)
+    // FP8: tm_q, tm_k are e4m3 row maps, tm_v the transposed V' map; the
+    // scores are (Q'K'^T) sq[tile] sk[tile] and O = (P V') sv
+    const float *sq, *sk, *sv;       // [B, H, n_tiles], [B, H, n_tiles], [B, H]
+    int n_tiles;
     __nv_bfloat16 *O;
     float *lse;
     int B, H, N;                     // N: queries per sequence (dense) / longest sequence
@@ -119,11 +127,12 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
 // SPLIT: compiled for split-KV calls (key ranges, query/key lengths that
 // differ, partial outputs); the plain instantiation has one range per pair and
 // kv_off = 0, so that logic folds away.
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ Bf16Params p)
 {
-    using C = Cfg<D>;
+    static_assert(!FP8 || (D == 128 && !SPLIT), "FP8: d = 128, no key splits");
+    using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     bool aborted = false;
 
-    uint8_t *q_smem[2] = {smem + C::kOffQ, smem + C::kOffQ + C::kTileBytes};
+    uint8_t *q_smem[2] = {smem + C::kOffQ, smem + C::kOffQ + C::kQBytes};
     uint8_t *ring = smem + C::kOffRing;
 
     if (warp == kWarpLoad) {
@@ -276,10 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kTileBytes);
                     const CUtensorMap *tm = kv ? &p.tm_v : &p.tm_k;
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes, tm,
-                                         &bar.kv_full[stage], c * 64, h,
-                                         int(start_k + int64_t(j0 + j) * BN));
+                    if (FP8 && kv) {
+                        // V'^T rows (b, h, 0 .. d-1), keys of this tile
+                        ptx::tma_load_2d(ring + stage * C::kTileBytes, tm, &bar.kv_full[stage],
+                                         (j0 + j) * BN, (b * p.H + h) * D);
+                    } else {
+                        for (int c = 0; c < C::kChunks; ++c)
+                            ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes, tm,
+                                             &bar.kv_full[stage], c * 64, h,
+                                             int(start_k + int64_t(j0 + j) * BN));
+                    }
                     last_phase[stage] = int(phase);
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -318,20 +333,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_qk = [&](int t, uint64_t dk) {
                 const uint64_t dq = t == 0 ? dq0 : dq1;
                 const uint32_t ts = tmem + col_s(t);
+                if constexpr (FP8) {
+                    // e4m3: K = 32 per MMA, 32 bytes along the 128-byte row
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-                    ptx::mma_ss(ts, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 32; ++kk)
+                        ptx::mma_ss_f8(ts, dq + ((kk * 32) >> 4), dk + ((kk * 32) >> 4),
+                                       ptx::idesc_e4m3_f32(BM, BN), kk > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+                        ptx::mma_ss(ts, dq + off, dk + off, idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                 }
                 ptx::mma_commit(&bar.s_full[t]);
             };
             auto issue_pv = [&](int t, uint64_t dv, bool accumulate) {
                 const uint32_t to = tmem + col_o<D>(t);
                 const uint32_t tp = tmem + col_s(t) + kColPinS;
+                if constexpr (FP8) {
+                    // P' e4m3 in TMEM (4 per column), V'^T K-major (keys contiguous)
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts(to, tp + kk * 8, dv + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
-                                (accumulate || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / 32; ++kk)
+                        ptx::mma_ts_f8(to, tp + kk * 8, dv + uint64_t((kk * 32) >> 4),
+                                       ptx::idesc_e4m3_f32(BM, D), (accumulate || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        ptx::mma_ts(to, tp + kk * 8, dv + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
+                                    (accumulate || kk > 0) ? 1u : 0u);
+                }
             };
 
             int stage = 0;
@@ -343,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 const uint32_t addr = ring_addr + stage * C::kTileBytes;
                 dk = ptx::smem_desc(desc_kmajor, addr);
-                dv = ptx::smem_desc(desc_mnmajor, addr);
+                dv = ptx::smem_desc(FP8 ? desc_kmajor : desc_mnmajor, addr);
                 return true;
             };
             auto advance = [&]() {
@@ -443,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_bits + col_s(t);
         const uint32_t tO = tmem + lane_bits + col_o<D>(t);
-        const float sl = p.scale_log2;
+        float sl = p.scale_log2;
+        if constexpr (FP8)                             // dequantise Q' K'^T: x sq sk
+            sl *= p.sq[(int64_t(b) * p.H + h) * p.n_tiles + qt];
         float m = -INFINITY;                           // reference max, log2 units
         float l = 0.f;                                 // running sum
 
@@ -496,7 +529,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // from overflow) while o~ is rescaled only on rare tiles.  o~ and l
             // share the reference, so it cancels in o~ / l and in
             // lse = m + log2 l: the result is exact for any reference.
-            const float mt = mx * sl;
+            float slj = sl;
+            if constexpr (FP8)
+                slj *= p.sk[(int64_t(b) * p.H + h) * p.n_tiles + (j0 + j)];
+            const float mt = mx * slj;
             const bool grew = mt > m + kRescaleLog2;
             const float m_new = grew ? mt : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -504,9 +540,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // P = exp2(s * sl - m) in bf16 over columns 64..127 of S_t; the
             // exponent arguments are formed two at a time (packed fp32x2 FMA)
-            const float2 sl2 = make_float2(sl, sl);
+            const float2 sl2 = make_float2(slj, slj);
             const float2 nm2 = make_float2(-m_use, -m_use);
             float rowsum = 0.f;
+            if constexpr (FP8) {
+                // P' = e4m3(p) four per column over columns 64..95 of S_t (p <=
+                // 2^kRescaleLog2 < 448, so nothing saturates)
+                uint32_t pk[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 32; ++q4) {
+                    const int col = 4 * q4;
+                    const float2 a = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[col >> 5][col & 31]),
+                                    __uint_as_float(sr[col >> 5][(col + 1) & 31])),
+                        sl2, nm2);
+                    const float2 c = __ffma2_rn(
+                        make_float2(__uint_as_float(sr[col >> 5][(col + 2) & 31]),
+                                    __uint_as_float(sr[col >> 5][(col + 3) & 31])),
+                        sl2, nm2);
+                    const float p0 = ptx::ex2(a.x), p1 = ptx::ex2(a.y);
+                    const float p2 = ptx::ex2(c.x), p3 = ptx::ex2(c.y);
+                    rowsum += (p0 + p1) + (p2 + p3);
+                    pk[q4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+                }
+                ptx::tmem_st32(tS + kColPinS, pk);
+            } else
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
@@ -614,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = !aborted && ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word);
             if (ok) {
                 ptx::tc_fence_after_sync();
-                const float inv = 1.f / l;
+                const float inv = (FP8 ? p.sv[int64_t(b) * p.H + h] : 1.f) / l;
                 const bool row_ok = i < L;
                 __nv_bfloat16 *orow = p.O + ((start + i) * p.H + h) * D;
 #pragma unroll
@@ -663,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // every thread of the tile arrives here once, also after a
                 // failed wait; the store goes out only if all 128 rows are in
                 if (!ptx::bar_red_or(1 + t, 128, !ok) && r == 0) {
-                    for (int ch = 0; ch < C::kChunks; ++ch)
+                    for (int ch = 0; ch < D / 64; ++ch)      // O is bf16: D / 64 chunks
                         ptx::tma_store_3d(&p.tm_o, o_stage + ch * kChunkBytes, ch * 64, h,
                                      int(start + int64_t(qt) * BM));
                     ptx::bulk_commit_and_wait_read();
@@ -742,6 +800,55 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     if (rc != FA_OK || p.splits == 1)
         return rc;
     return launch_attention_combine(a, stream);
+}
+
+int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
+{
+    if (a.d != 128)
+        return FA_ERR_UNSUPPORTED;
+    Bf16Params p{};
+    const int64_t total = int64_t(a.B) * a.N;
+    if (!make_tmap_e4m3_rows(&p.tm_q, a.Qf, total, a.H, a.d) ||
+        !make_tmap_e4m3_rows(&p.tm_k, a.Kf, total, a.H, a.d) ||
+        !make_tmap_e4m3_vt(&p.tm_v, a.Vt, int64_t(a.B) * a.H * a.d, a.n_pad, a.d) ||
+        !make_tmap_bf16(&p.tm_o, a.O, total, a.H, a.d))
+        return FA_ERR_CUDA;
+    p.sq = a.sq;
+    p.sk = a.sk;
+    p.sv = a.sv;
+    p.n_tiles = (a.N + BM - 1) / BM;
+    p.Nk = a.N;
+    p.kv_off = 0;
+    p.splits = 1;
+    p.O_accum = nullptr;
+    p.lse_accum = nullptr;
+    p.O = static_cast<__nv_bfloat16 *>(a.O);
+    p.lse = a.lse;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.n_pairs = (p.n_tiles + 1) / 2;
+    p.total = total;
+    p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
+    p.causal = a.causal;
+    p.cu_seqlens = nullptr;
+    p.err_word = a.err_word;
+    const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H;
+    if (blocks == 0)
+        return FA_OK;
+    if (blocks > 0x7fffffffLL)
+        return FA_ERR_TOO_LARGE;
+    auto kern = attn_fwd_bf16_kernel<128, false, true>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(Cfg<128, true>::kSmemBytes));
+    });
+    if (attr_err != cudaSuccess)
+        return FA_ERR_CUDA;
+    kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<128, true>::kSmemBytes, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int choose_num_splits(int B, int H, int N, int Nk)

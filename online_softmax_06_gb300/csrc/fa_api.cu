@@ -131,6 +131,40 @@ int attention_common(const void *Q, const void *K, const void *V, void *O, float
     return bf16 ? launch_attention_bf16(a, t_stream) : launch_attention_f32(a, t_stream);
 }
 
+// Workspace of the FP8 forward: e4m3 Q', K' ([B*N, H, d]), the transposed
+// V' ([B, H, d, n_pad]), then the fp32 scales; every part 256-byte aligned.
+struct Fp8Layout {
+    int64_t qf, kf, vt, sq, sk, vamax, sv, bytes;
+    int n_tiles, n_pad;
+};
+
+Fp8Layout fp8_layout(int B, int H, int N, int d)
+{
+    auto up = [](int64_t x) { return (x + 255) & ~int64_t(255); };
+    Fp8Layout L;
+    L.n_tiles = (N + 127) / 128;
+    L.n_pad = L.n_tiles * 128;
+    const int64_t elems = int64_t(B) * N * H * d;
+    const int64_t tiles = int64_t(B) * H * L.n_tiles;
+    int64_t off = 0;
+    L.qf = off;
+    off = up(off + elems);
+    L.kf = off;
+    off = up(off + elems);
+    L.vt = off;
+    off = up(off + int64_t(B) * H * d * L.n_pad);
+    L.sq = off;
+    off = up(off + tiles * 4);
+    L.sk = off;
+    off = up(off + tiles * 4);
+    L.vamax = off;
+    off = up(off + tiles * 4);
+    L.sv = off;
+    off = up(off + int64_t(B) * H * 4);
+    L.bytes = off;
+    return L;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -270,6 +304,80 @@ int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O,
     a.causal = causal ? 1 : 0;
     a.err_word = dev->err_word;
     return fa::launch_attention_bwd(a, fa::t_stream);
+}
+
+int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return fa::fp8_layout(B, H, N, d).bytes;
+}
+
+int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                         int H, int N, int d, float scale, int causal, const float *signs,
+                         void *workspace, int64_t workspace_bytes)
+{
+    if (B < 0 || H < 0 || N < 0 || workspace_bytes < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0)
+        return FA_OK;
+    if (!Q || !K || !V || !O || !lse || !signs || !workspace)
+        return FA_ERR_NULL_POINTER;
+    if (!fa::aligned(Q, 16) || !fa::aligned(K, 16) || !fa::aligned(V, 16) ||
+        !fa::aligned(O, 16) || !fa::aligned(lse, 4) || !fa::aligned(signs, 4) ||
+        !fa::aligned(workspace, 256))
+        return FA_ERR_MISALIGNED;
+    const int64_t total = int64_t(B) * N;
+    if (total > (int64_t(1) << 31) - 512 || total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+        return FA_ERR_TOO_LARGE;
+    const fa::Fp8Layout L = fa::fp8_layout(B, H, N, d);
+    if (workspace_bytes < L.bytes)
+        return FA_ERR_BAD_SIZE;
+    fa::DeviceInfo *dev = fa::current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    fa::Fp8QuantArgs q;
+    q.Q = Q;
+    q.K = K;
+    q.V = V;
+    q.signs = signs;
+    q.Qf = ws + L.qf;
+    q.Kf = ws + L.kf;
+    q.Vt = ws + L.vt;
+    q.sq = reinterpret_cast<float *>(ws + L.sq);
+    q.sk = reinterpret_cast<float *>(ws + L.sk);
+    q.vamax = reinterpret_cast<float *>(ws + L.vamax);
+    q.sv = reinterpret_cast<float *>(ws + L.sv);
+    q.B = B;
+    q.H = H;
+    q.N = N;
+    q.d = d;
+    int rc = fa::launch_fp8_quantize(q, fa::t_stream);
+    if (rc != FA_OK)
+        return rc;
+    fa::AttnFp8Args a;
+    a.Qf = q.Qf;
+    a.Kf = q.Kf;
+    a.Vt = q.Vt;
+    a.sq = q.sq;
+    a.sk = q.sk;
+    a.sv = q.sv;
+    a.O = O;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.n_pad = L.n_pad;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.err_word = dev->err_word;
+    return fa::launch_attention_fp8(a, fa::t_stream);
 }
 
 int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,

@@ -47,6 +47,25 @@ int choose_num_splits(int B, int H, int N, int Nk);
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d,
                     int box_rows = 128);
 
+// TMA maps over the FP8 forward's e4m3 tensors: rows of Q' / K' ([total, H, d]
+// bytes, box d x 1 x 128, d = 128 so a row is one 128-byte swizzle span) and
+// the transposed V' ([rows = B*H*d, n_pad] bytes, box 128 keys x d rows).
+bool make_tmap_e4m3_rows(CUtensorMap *tm, const void *base, int64_t total, int H, int d);
+bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t n_pad, int d);
+
+// FP8 attention forward on the quantised tensors (dense; d = 128).
+struct AttnFp8Args {
+    const uint8_t *Qf, *Kf, *Vt;
+    const float *sq, *sk, *sv;
+    void *O;
+    float *lse;
+    int B, H, N, d, n_pad;
+    float scale;
+    int causal;
+    int *err_word;
+};
+int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream);
+
 // Backward of the bf16 attention (dense [B, N, H, d]); layouts as in fa.h.
 struct AttnBwdArgs {
     const void *Q, *K, *V, *O, *dO;
@@ -59,5 +78,17 @@ struct AttnBwdArgs {
     int *err_word;
 };
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
+
+// Quantisation pass of the FP8 forward (dense [B, N, H, d] bf16 inputs).
+struct Fp8QuantArgs {
+    const void *Q, *K, *V;
+    const float *signs;        // [d], +-1
+    uint8_t *Qf, *Kf;          // [B*N, H, d] e4m3 (Q M, K M over scales)
+    uint8_t *Vt;               // [B, H, d, n_pad] e4m3, n_pad = 128 * n_tiles
+    float *sq, *sk, *vamax;    // [B, H, n_tiles]
+    float *sv;                 // [B, H]
+    int B, H, N, d;
+};
+int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream);
 
 }  // namespace fa

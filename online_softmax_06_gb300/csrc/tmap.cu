@@ -51,4 +51,34 @@ bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_e4m3_rows(CUtensorMap *tm, const void *base, int64_t total, int H, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(total)};
+    const cuuint64_t strides[2] = {cuuint64_t(d), cuuint64_t(H) * d};
+    const cuuint32_t box[3] = {cuuint32_t(d), 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t n_pad, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t dims[2] = {cuuint64_t(n_pad), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(n_pad)};
+    const cuuint32_t box[2] = {128, cuuint32_t(d)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fa
