@@ -25,7 +25,7 @@ namespace fa {
 namespace {
 
 constexpr int kRows = 128;          // rows per tile
-constexpr int kWarps = 8;           // 16 rows per warp
+constexpr int kWarps = 16;          // 8 rows per warp: the rows stay in registers
 constexpr float kE4M3Max = 448.f;
 
 __device__ __forceinline__ float warp_max(float v)
@@ -111,9 +111,20 @@ __global__ void __launch_bounds__(kWarps * 32) fp8_qk_kernel(const QuantParams p
         const int row = tile * kRows + warp * kRowsPerWarp + rr;
         if (row < p.N) {
             const __nv_bfloat16 *rp = src + ((int64_t(b) * p.N + row) * p.H + h) * D + lane * E;
-#pragma unroll
-            for (int k = 0; k < E; ++k)
-                x[rr][k] = __bfloat162float(rp[k]);
+            // one 8-byte (d = 128) or 4-byte (d = 64) load per lane and row
+            if constexpr (E == 4) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(rp);
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+                const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+                x[rr][0] = a.x;
+                x[rr][1] = a.y;
+                x[rr][2] = c.x;
+                x[rr][3] = c.y;
+            } else {
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rp));
+                x[rr][0] = a.x;
+                x[rr][1] = a.y;
+            }
             if (which < 2)
                 rotate_row<D>(x[rr], sg, lane);
         } else {
