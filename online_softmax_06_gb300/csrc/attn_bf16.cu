@@ -16,7 +16,10 @@
 //   * warp 8 (one lane) issues TMA loads: Q0, K_0, Q1 (one barrier per Q tile,
 //     so the first Q0 K_0^T does not wait for Q1), then V_0, K_1, V_1, ...
 //     into a ring of shared-memory stages guarded by full/empty mbarriers;
-//   * warp 9 (one lane) owns the tensor memory and issues every tcgen05.mma:
+//   * warp 9 owns the tensor memory and issues every tcgen05.mma (the whole
+//     warp runs the issuing loop and its barrier waits converged, and one
+//     elected lane issues: the loop's descriptors stay warp-uniform, which
+//     keeps the issue rate at the tensor pipe's rate):
 //     S_t = Q_t K_j^T (bf16 x bf16 -> fp32, M=N=128, K=d) into TMEM, and
 //     O_t += P_t V_j with P_t read from TMEM (written there by the softmax
 //     threads over the upper half of S_t) and V_j from shared memory as an
@@ -316,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ======================= MMA issuer ================================
-        if (lane == 0) {
+        // ======================= MMA issuer (whole warp) =====================
+        {
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false);
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, true);
             constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_qk = [&](int t, uint64_t dk) {
                 const uint64_t dq = t == 0 ? dq0 : dq1;
                 const uint32_t ts = tmem + col_s(t);
+                if (ptx::elect_one()) {
                 if constexpr (FP8) {
                     // e4m3: K = 32 per MMA, 32 bytes along the 128-byte row
 #pragma unroll
@@ -347,10 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 ptx::mma_commit(&bar.s_full[t]);
+                }
+                __syncwarp();
             };
             auto issue_pv = [&](int t, uint64_t dv, bool accumulate) {
                 const uint32_t to = tmem + col_o<D>(t);
                 const uint32_t tp = tmem + col_s(t) + kColPinS;
+                if (ptx::elect_one()) {
                 if constexpr (FP8) {
                     // P' e4m3 in TMEM (4 per column), V'^T K-major (keys contiguous)
 #pragma unroll
@@ -363,6 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_ts(to, tp + kk * 8, dv + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
                                     (accumulate || kk > 0) ? 1u : 0u);
                 }
+                }
+                __syncwarp();
+            };
+            auto commit = [&](uint64_t *bar_) {
+                if (ptx::elect_one())
+                    ptx::mma_commit(bar_);
+                __syncwarp();
             };
 
             int stage = 0;
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // waits for the next ring stage; returns its K-major and MN-major
             // descriptors (the stage holds a K tile or a V tile)
             auto next_stage = [&](uint64_t &dk, uint64_t &dv) -> bool {
-                if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word))
+                if (!ptx::mbar_wait_warp(&bar.kv_full[stage], phase, abort_flag, p.err_word))
                     return false;
                 const uint32_t addr = ring_addr + stage * C::kTileBytes;
                 dk = ptx::smem_desc(desc_kmajor, addr);
@@ -396,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < 2 && q_ok; ++t) {
                     if ((t == 0 ? n0 : n1) == 0)
                         continue;
-                    q_ok = ptx::mbar_wait(&bar.q_full[t], 0, abort_flag, p.err_word);
+                    q_ok = ptx::mbar_wait_warp(&bar.q_full[t], 0, abort_flag, p.err_word);
                     if (q_ok) {
                         ptx::tc_fence_after_sync();
                         issue_qk(t, k_desc);
@@ -406,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     aborted = true;
                     break;
                 }
-                ptx::mma_commit(&bar.kv_empty[k_stage]);
+                commit(&bar.kv_empty[k_stage]);
 
                 for (int j = 0; j < n_max; ++j) {
                     uint64_t v_desc;
@@ -417,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int v_stage = stage;
                     advance();
                     if (j < n0) {
-                        if (!ptx::mbar_wait(&bar.p_full[0], uint32_t(j) & 1u, abort_flag,
+                        if (!ptx::mbar_wait_warp(&bar.p_full[0], uint32_t(j) & 1u, abort_flag,
                                             p.err_word)) {
                             aborted = true;
                             break;
@@ -425,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_after_sync();
                         issue_pv(0, v_desc, j > 0);
                         if (j == n0 - 1)
-                            ptx::mma_commit(&bar.o_full[0]);
+                            commit(&bar.o_full[0]);
                     }
                     const bool more = j + 1 < n_max;
                     if (more) {
@@ -440,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             issue_qk(0, k_desc);
                     }
                     if (j < n1) {
-                        if (!ptx::mbar_wait(&bar.p_full[1], uint32_t(j) & 1u, abort_flag,
+                        if (!ptx::mbar_wait_warp(&bar.p_full[1], uint32_t(j) & 1u, abort_flag,
                                             p.err_word)) {
                             aborted = true;
                             break;
@@ -448,20 +462,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_after_sync();
                         issue_pv(1, v_desc, j > 0);
                         if (j == n1 - 1)
-                            ptx::mma_commit(&bar.o_full[1]);
+                            commit(&bar.o_full[1]);
                     }
-                    ptx::mma_commit(&bar.kv_empty[v_stage]);
+                    commit(&bar.kv_empty[v_stage]);
                     if (more) {
                         if (j + 1 < n1)
                             issue_qk(1, k_desc);
-                        ptx::mma_commit(&bar.kv_empty[k_stage]);
+                        commit(&bar.kv_empty[k_stage]);
                     }
                 }
             } while (false);
             // Every MMA issued above has completed (and every commit has arrived)
             // once this last commit arrives.
-            ptx::mma_commit(bar.drain);
-            drain_wait(bar.drain, 0);
+            if (ptx::elect_one()) {
+                ptx::mma_commit(bar.drain);
+                drain_wait(bar.drain, 0);
+            }
         }
         __syncwarp();
     } else {

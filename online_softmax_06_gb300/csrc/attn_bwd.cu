@@ -12,29 +12,34 @@
 // its own pass over Q row blocks instead (no atomics, deterministic), at the
 // cost of recomputing S and dP there.
 //
-// Two kernels, launched in this order on one stream:
-//   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile).  Each
-//     query row is served by two threads (64 columns each): they form
-//     D_i = dO_i . O_i (stored for the second kernel), then for every visible key tile j
-//     turns S = Q K_j^T and dP = dO V_j^T (tcgen05, fp32 in TMEM) into
-//     dS = P o (dP - D_i) in bf16 in TMEM, and the MMA warp accumulates
-//     dQ += dS K_j in TMEM.
+// Two kernels, launched in this order on one stream; each keeps one 128-row
+// tile resident in shared memory and streams the other operand in 64-row
+// sub-tiles:
+//   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile), Q and
+//     dO resident.  Each query row is served by two threads (32 columns of a
+//     sub-tile each): they form D_i = dO_i . O_i (stored for the second kernel),
+//     then for every visible 64-key sub-tile j turn S = Q K_j^T and
+//     dP = dO V_j^T (tcgen05, fp32 in TMEM) into dS = P o (dP - D_i) in bf16 in
+//     TMEM, and the MMA warp accumulates dQ += dS K_j in TMEM.
 //   * attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key tile), K and
-//     V resident in shared memory.  For every query tile i that sees the keys,
+//     V resident.  For every 64-query sub-tile i that sees the keys,
 //     S^T = K Q_i^T and dP^T = V dO_i^T land in TMEM with one key per TMEM
-//     lane; the two threads of each key row form P^T and dS^T
-//     (bf16, in TMEM) from the query tile's logsumexp and D (staged in shared
-//     memory by the load warp), and the MMA warp accumulates dV += P^T dO_i and
-//     dK += dS^T Q_i.
-// The elementwise work (P, dS) needs no reduction along a row, so a row's 128
+//     lane; the two threads of each key row form P^T and dS^T (bf16, in TMEM)
+//     from the sub-tile's logsumexp and D (staged in shared memory by the load
+//     warp), and the MMA warp accumulates dV += P^T dO_i and dK += dS^T Q_i.
+// S and dP of a step live in one of two TMEM buffers (columns [0, 128) and
+// [128, 256)), so the MMA warp computes step s + 1's S and dP while the row
+// threads turn step s's into P / dS; the accumulators take columns [256, 512).
+// The elementwise work needs no reduction along a row, so a sub-tile row's 64
 // columns are split between two threads: warps 0-7 serve the rows (warp w:
-// TMEM lanes 32 (w % 4) .. + 31, columns 64 (w / 4) .. + 63), which hides
-// more of the exp and TMEM latencies than one thread per row.  Warp 8 issues
-// TMA loads into a ring of shared-memory stages and warp 9 owns the tensor
-// memory and issues every tcgen05.mma.  Every wait is
-// bounded; a wait that gives up raises the error word and the abort flag, the
-// roles leave their loops, in-flight copies and MMAs drain, and the CTA frees
-// its tensor memory.
+// TMEM lanes 32 (w % 4) .. + 31, columns 32 (w / 4) .. + 31 of the buffer).
+// Warp 8 issues TMA loads: one ring stage holds a step's pair of sub-tiles
+// behind one barrier, and each pair is prefetched into L2 a few steps before
+// its load.  Warp 9 owns the tensor memory and issues every tcgen05.mma: the
+// whole warp runs the issuing loop converged and one elected lane issues.
+// Every wait is bounded; a wait that gives up raises the error word and the
+// abort flag, the roles leave their loops, in-flight copies and MMAs drain,
+// and the CTA frees its tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,53 +56,66 @@
 namespace fa {
 namespace {
 
-constexpr int BT = 128;                     // rows of a Q, K, V or dO tile
+constexpr int BT = 128;                     // rows of the resident tile
+constexpr int BS = 64;                      // rows of a streamed sub-tile
 constexpr int G = 2;                        // threads per row (column groups)
-constexpr int kColsPerThread = BT / G;
+constexpr int kColsPerThread = BS / G;      // one 32-column block per step
 constexpr int kRowWarps = 4 * G;
 constexpr int kThreads = 32 * (kRowWarps + 2);
 constexpr int kWarpLoad = kRowWarps;
 constexpr int kWarpMma = kRowWarps + 1;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kChunkBytes = BT * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kResChunkBytes = BT * 128;  // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kSubChunkBytes = BS * 128;  // 64 rows x 128 bytes
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kL2Ahead = 4;                 // streamed sub-tiles are prefetched into L2
+                                            // this many steps before their load
 
 template <int D>
 struct Cfg {
     static constexpr int kChunks = D / 64;
-    static constexpr uint32_t kTileBytes = BT * D * 2;
-    static constexpr int kStages = 4;        // two per step (even / odd positions)
-    // shared memory: [A0][A1][ring x kStages][stats: 2 slots x (lse2, D) x 128
-    // floats][barriers, flags]
+    static constexpr uint32_t kResBytes = BT * D * 2;
+    static constexpr uint32_t kSubBytes = BS * D * 2;
+    // a ring stage holds one step's pair of sub-tiles, (K_j, V_j) or
+    // (Q_i, dO_i), behind one barrier
+    static constexpr int kStages = 4;
+    static constexpr uint32_t kStageBytes = 2 * kSubBytes;
+    // shared memory: [A0][A1][ring x kStages][stats: kStages slots x
+    // (lse2, D) x 64 floats][barriers, flags]
     static constexpr uint32_t kOffA0 = 0;
-    static constexpr uint32_t kOffA1 = kTileBytes;
-    static constexpr uint32_t kOffRing = 2 * kTileBytes;
-    static constexpr uint32_t kOffStat = kOffRing + kStages * kTileBytes;
-    static constexpr uint32_t kStatBytes = 2 * 2 * BT * 4;
+    static constexpr uint32_t kOffA1 = kResBytes;
+    static constexpr uint32_t kOffRing = 2 * kResBytes;
+    static constexpr uint32_t kOffStat = kOffRing + kStages * kStageBytes;
+    static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;
     static constexpr uint32_t kOffBar = kOffStat + kStatBytes;
-    // a_full, kv_full[S], kv_empty[S], s_full, p_full, o_full, drain
-    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 4);
+    // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full, drain
+    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 6);
     static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
-// TMEM columns: S (or S^T) [0, 128), dP (or dP^T) [128, 256), accumulators from
-// 256 (dQ; or dV then dK).  bf16 P / dS are packed into the region they are
-// formed from: the 32 values of each 32-column block go to the block's first 16
-// columns (two per column), so a thread only overwrites columns it has read.
-constexpr uint32_t kColS = 0, kColP = 128, kColAcc = 256;
+// TMEM columns: buffer b holds S (or S^T) in [128 b, 128 b + 64) and dP (or
+// dP^T) in [128 b + 64, 128 b + 128); accumulators from 256 (dQ; or dV then
+// dK).  bf16 P / dS are packed into the region they are formed from: the 32
+// values of each 32-column block go to the block's first 16 columns (two per
+// column), so a thread only overwrites columns it has read.
+constexpr uint32_t kColBuf = 128, kColDP = 64, kColAcc = 256;
 // Column of the packed bf16 operand for the MMA's K step kk (16 values).
 __host__ __device__ constexpr uint32_t packed_col(int kk)
 {
     return uint32_t(32 * (kk >> 1) + 8 * (kk & 1));
 }
 
+// The dQ kernel's resident pair is (Q, dO) and its streamed pair (K, V); the
+// dK/dV kernel's resident pair is (K, V) and its streamed pair (Q, dO).
 struct BwdParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;    // [B*N, H, d] bf16, box {64, 1, 128}
+    CUtensorMap tm_a0, tm_a1;               // resident, [B*N, H, d] bf16, box {64, 1, 128}
+    CUtensorMap tm_s0, tm_s1;               // streamed, box {64, 1, 64}
     const __nv_bfloat16 *O, *dO;
     const float *lse;                       // [B, H, N], natural log
     float *D;                               // [B, H, N]
     __nv_bfloat16 *dQ, *dK, *dV;
-    int B, H, N, n_tiles;
+    int B, H, N, n_tiles, n_sub;
     float scale, scale_log2;
     int causal;
     int *err_word;
@@ -116,10 +134,10 @@ __device__ __forceinline__ Bars carve(uint8_t *smem)
     r.a_full = b;
     r.kv_full = b + 1;
     r.kv_empty = b + 1 + C::kStages;
-    r.s_full = b + 1 + 2 * C::kStages;
-    r.p_full = r.s_full + 1;
-    r.o_full = r.s_full + 2;
-    r.drain = r.s_full + 3;
+    r.s_full = b + 1 + 2 * C::kStages;        // [2]
+    r.p_full = r.s_full + 2;                  // [2]
+    r.o_full = r.s_full + 4;
+    r.drain = r.s_full + 5;
     return r;
 }
 
@@ -134,12 +152,28 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// A row warp's wait: lane 0 polls the barrier and shares the outcome; the
+// warp-synchronous exchange orders the other lanes' later accesses after the
+// completed phase (the row warps arrive once per warp for the same reason:
+// 256 pollers and arrivals per step would contend with the tensor cores'
+// shared-memory reads).
+__device__ __forceinline__ bool row_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         int *err_word)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0)
+        ok = ptx::mbar_wait(bar, parity, abort, err_word) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 // Shared set-up of both kernels: barriers, tensor memory, tensor-map prefetch.
-// kv_full of odd ring positions counts `odd_arrivals` arrivals (the load warp's
-// lanes stage statistics with those tiles in the dK/dV kernel).
+// kv_full counts `kv_arrivals` arrivals (in the dK/dV kernel all lanes of the
+// load warp arrive: they stage the statistics with the tiles).
 template <int D>
-__device__ __forceinline__ uint32_t setup(const BwdParams &p, uint8_t *smem, const Bars &bar,
-                                          uint32_t odd_arrivals, volatile int *abort_flag,
+__device__ __forceinline__ uint32_t setup(const BwdParams &p, const Bars &bar,
+                                          uint32_t kv_arrivals, volatile int *abort_flag,
                                           uint32_t *tmem_slot)
 {
     using C = Cfg<D>;
@@ -147,11 +181,13 @@ __device__ __forceinline__ uint32_t setup(const BwdParams &p, uint8_t *smem, con
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar.a_full, 1);
         for (int s = 0; s < C::kStages; ++s) {
-            ptx::mbar_init(&bar.kv_full[s], (s & 1) ? odd_arrivals : 1u);
+            ptx::mbar_init(&bar.kv_full[s], kv_arrivals);
             ptx::mbar_init(&bar.kv_empty[s], 1);
         }
-        ptx::mbar_init(bar.s_full, 1);
-        ptx::mbar_init(bar.p_full, BT * G);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bar.s_full[b], 1);
+            ptx::mbar_init(&bar.p_full[b], kRowWarps);   // one arrival per row warp
+        }
         ptx::mbar_init(bar.o_full, 1);
         ptx::mbar_init(bar.drain, 1);
         *abort_flag = 0;
@@ -162,15 +198,14 @@ __device__ __forceinline__ uint32_t setup(const BwdParams &p, uint8_t *smem, con
         ptx::tmem_relinquish();
     }
     if (warp == kWarpLoad && lane == 0) {
-        ptx::prefetch_tmap(&p.tm_q);
-        ptx::prefetch_tmap(&p.tm_k);
-        ptx::prefetch_tmap(&p.tm_v);
-        ptx::prefetch_tmap(&p.tm_do);
+        ptx::prefetch_tmap(&p.tm_a0);
+        ptx::prefetch_tmap(&p.tm_a1);
+        ptx::prefetch_tmap(&p.tm_s0);
+        ptx::prefetch_tmap(&p.tm_s1);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
-    (void)smem;
     return *tmem_slot;
 }
 
@@ -184,13 +219,14 @@ __device__ __forceinline__ void teardown(uint32_t tmem)
         ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-// Row `r` of a 128-row tile's accumulator (32-bit TMEM columns [col, col + D))
-// scaled by `mul`, written as bf16 to dst (one row of D elements).
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t t_acc, float mul, __nv_bfloat16 *dst, bool ok)
+// Columns [32 c_begin, 32 c_end) of row `r` of a 128-row accumulator (32-bit
+// TMEM columns from t_acc) scaled by `mul`, written as bf16 to dst (the row's
+// first element).
+__device__ __forceinline__ void store_row(uint32_t t_acc, float mul, __nv_bfloat16 *dst, bool ok,
+                                          int c_begin, int c_end)
 {
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
         uint32_t o[32];
         ptx::tmem_ld32(t_acc + c * 32, o);
         ptx::tmem_wait_ld();
@@ -213,6 +249,13 @@ __device__ __forceinline__ void store_row(uint32_t t_acc, float mul, __nv_bfloat
     }
 }
 
+// Shared-memory descriptor offsets of the K step kk (16 bf16) in a K-major
+// 128B-swizzled tile whose 64-column chunks are `chunk_bytes` apart.
+__device__ __forceinline__ uint64_t kmajor_off(int kk, uint32_t chunk_bytes)
+{
+    return uint64_t(((kk >> 2) * chunk_bytes + (kk & 3) * 32) >> 4);
+}
+
 // =============================================================================
 // dQ (and D) -- one CTA per (sequence, head, query tile), heaviest tiles first
 // =============================================================================
@@ -233,49 +276,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
     const int64_t row0 = int64_t(b) * p.N;          // first row of the sequence
-    const int n_kv = p.causal ? qt + 1 : p.n_tiles;  // key tiles this query tile sees
+    // key sub-tiles this query tile sees (at least one)
+    const int n_kv = p.causal ? min(2 * qt + 2, p.n_sub) : p.n_sub;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const uint32_t tmem = setup<D>(p, smem, bar, 1u, abort_flag, tmem_slot);
+    const uint32_t tmem = setup<D>(p, bar, 1u, abort_flag, tmem_slot);
     bool aborted = false;
     uint8_t *tile_q = smem + C::kOffA0, *tile_do = smem + C::kOffA1;
     uint8_t *ring = smem + C::kOffRing;
 
     if (warp == kWarpLoad) {
         // ======================= TMA producer ==============================
+        // Ring stage of step j: K_j then V_j (64 keys each).
         if (lane == 0) {
             int last_phase[C::kStages];
             for (int s = 0; s < C::kStages; ++s)
                 last_phase[s] = -1;
-            ptx::mbar_arrive_expect_tx(bar.a_full, 2 * C::kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar.a_full, 2 * C::kResBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                ptx::tma_load_3d(tile_q + c * kChunkBytes, &p.tm_q, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_q + c * kResChunkBytes, &p.tm_a0, bar.a_full, c * 64, h,
                                  int(row0 + int64_t(qt) * BT));
-                ptx::tma_load_3d(tile_do + c * kChunkBytes, &p.tm_do, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_do + c * kResChunkBytes, &p.tm_a1, bar.a_full, c * 64, h,
                                  int(row0 + int64_t(qt) * BT));
             }
             int stage = 0;
             uint32_t phase = 0;
-            for (int j = 0; j < n_kv && !aborted; ++j) {
-                for (int kv = 0; kv < 2; ++kv) {
-                    if (!ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag,
-                                        p.err_word)) {
-                        aborted = true;
-                        break;
+            for (int j = 0; j < n_kv; ++j) {
+                if (!ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag, p.err_word))
+                    break;
+                uint8_t *dst = ring + stage * C::kStageBytes;
+                const int row = int(row0 + int64_t(j) * BS);
+                ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kStageBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    ptx::tma_load_3d(dst + c * kSubChunkBytes, &p.tm_s0, &bar.kv_full[stage],
+                                     c * 64, h, row);
+                    ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
+                                     &bar.kv_full[stage], c * 64, h, row);
+                }
+                if (j + kL2Ahead < n_kv)
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
+                        ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
                     }
-                    ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kTileBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes,
-                                         kv ? &p.tm_v : &p.tm_k, &bar.kv_full[stage], c * 64, h,
-                                         int(row0 + int64_t(j) * BT));
-                    last_phase[stage] = int(phase);
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                last_phase[stage] = int(phase);
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (aborted || *abort_flag) {
+            if (*abort_flag) {
                 drain_wait(bar.a_full, 0);
                 for (int s = 0; s < C::kStages; ++s)
                     if (last_phase[s] >= 0)
@@ -284,78 +333,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ======================= MMA issuer ================================
-        if (lane == 0) {
-            constexpr uint32_t idesc_ss = ptx::idesc_bf16_f32(BT, BT, false);
-            constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
-            constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
-            constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kChunkBytes, 1024);
-            const uint64_t dq = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_q));
-            const uint64_t ddo = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_do));
-            const uint32_t ring_addr = ptx::smem_u32(ring);
-            int stage = 0;
-            uint32_t phase = 0;
-            auto advance = [&]() {
-                if (++stage == C::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            do {
-                if (!ptx::mbar_wait(bar.a_full, 0, abort_flag, p.err_word)) {
+        // ======================= MMA issuer (whole warp) =====================
+        // Order: S_0, dP_0; then per step j: S_{j+1}, dP_{j+1} (other buffer),
+        // wait for dS_j, dQ += dS_j K_j.  The warp runs the loop converged and
+        // one elected lane issues the MMAs and commits.
+        constexpr uint32_t idesc_ss = ptx::idesc_bf16_f32(BT, BS, false);
+        constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
+        constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
+        constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kSubChunkBytes, 1024);
+        const uint64_t dq = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_q));
+        const uint64_t ddo = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_do));
+        const uint32_t ring_addr = ptx::smem_u32(ring);
+        int stage = 0;
+        uint32_t phase = 0;
+        int k_stage0 = 0, k_stage1 = 0;            // step's ring stage, per buffer
+        // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j & 1
+        auto issue_s = [&](int j) -> bool {
+            if (!ptx::mbar_wait_warp(&bar.kv_full[stage], phase, abort_flag, p.err_word))
+                return false;
+            (j & 1 ? k_stage1 : k_stage0) = stage;
+            const uint32_t kaddr = ring_addr + stage * C::kStageBytes;
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            ptx::tc_fence_after_sync();
+            const uint64_t dk = ptx::smem_desc(desc_kmajor, kaddr);
+            const uint64_t dv = ptx::smem_desc(desc_kmajor, kaddr + C::kSubBytes);
+            const uint32_t buf = tmem + uint32_t(j & 1) * kColBuf;
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(buf, dq + kmajor_off(kk, kResChunkBytes),
+                                dk + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(buf + kColDP, ddo + kmajor_off(kk, kResChunkBytes),
+                                dv + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&bar.s_full[j & 1]);
+            }
+            __syncwarp();
+            return true;
+        };
+        do {
+            if (!ptx::mbar_wait_warp(bar.a_full, 0, abort_flag, p.err_word) || !issue_s(0)) {
+                aborted = true;
+                break;
+            }
+            for (int j = 0; j < n_kv; ++j) {
+                if (j + 1 < n_kv && !issue_s(j + 1)) {
                     aborted = true;
                     break;
                 }
-                for (int j = 0; j < n_kv; ++j) {
-                    // S = Q K_j^T
-                    if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    const int k_stage = stage;
-                    const uint32_t k_addr = ring_addr + stage * C::kTileBytes;
-                    advance();
-                    ptx::tc_fence_after_sync();
-                    const uint64_t dk = ptx::smem_desc(desc_kmajor, k_addr);
+                // dQ += dS_j K_j   (dS: bf16 packed in buffer j & 1)
+                if (!ptx::mbar_wait_warp(&bar.p_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag,
+                                         p.err_word)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const int ks = (j & 1) ? k_stage1 : k_stage0;
+                const uint64_t dkn = ptx::smem_desc(desc_mnmajor, ring_addr + ks * C::kStageBytes);
+                const uint32_t a_tm = tmem + uint32_t(j & 1) * kColBuf;
+                if (ptx::elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(tmem + kColS, dq + off, dk + off, idesc_ss, kk > 0 ? 1u : 0u);
-                    }
-                    // dP = dO V_j^T
-                    if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    const int v_stage = stage;
-                    const uint64_t dv =
-                        ptx::smem_desc(desc_kmajor, ring_addr + stage * C::kTileBytes);
-                    advance();
-                    ptx::tc_fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(tmem + kColP, ddo + off, dv + off, idesc_ss, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(bar.s_full);
-                    ptx::mma_commit(&bar.kv_empty[v_stage]);
-                    // dQ += dS K_j   (dS: bf16 over the first 64 columns of S)
-                    if (!ptx::mbar_wait(bar.p_full, uint32_t(j) & 1u, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    ptx::tc_fence_after_sync();
-                    const uint64_t dkn = ptx::smem_desc(desc_mnmajor, k_addr);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + packed_col(kk),
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ts(tmem + kColAcc, a_tm + packed_col(kk),
                                     dkn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(&bar.kv_empty[k_stage]);
+                    ptx::mma_commit(&bar.kv_empty[ks]);
                 }
-                if (!aborted)
-                    ptx::mma_commit(bar.o_full);
-            } while (false);
+                __syncwarp();
+            }
+        } while (false);
+        if (ptx::elect_one()) {
+            if (!aborted)
+                ptx::mma_commit(bar.o_full);
             ptx::mma_commit(bar.drain);
             drain_wait(bar.drain, 0);
         }
@@ -367,8 +420,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = qt * BT + r;
         const bool row_ok = i < p.N;
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_bits + kColS;
-        const uint32_t tP = tmem + lane_bits + kColP;
         const int64_t stat = (int64_t(b) * p.H + h) * p.N + i;
         // D_i = dO_i . O_i (fp32); group 0 stores it for the dK/dV kernel
         float Di = 0.f, lse2 = 0.f;
@@ -395,55 +446,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             lse2 = p.lse[stat] * kLog2e;
         }
         const float sl = p.scale_log2;
+        const int col0 = g * kColsPerThread;
 
         for (int j = 0; j < n_kv; ++j) {
-            if (!ptx::mbar_wait(bar.s_full, uint32_t(j) & 1u, abort_flag, p.err_word)) {
+            if (!row_wait(&bar.s_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag,
+                                p.err_word)) {
                 aborted = true;
                 break;
             }
             ptx::tc_fence_after_sync();
-            // last visible column of this key tile for row i (causal diagonal,
-            // end of the sequence); rows past the end see nothing
-            const bool diag = p.causal && j == qt;
-            int lim = diag ? r : BT - 1;
-            const int lim_len = p.N - 1 - j * BT;
-            if (lim_len < lim)
-                lim = lim_len;
+            // last visible column of this key sub-tile for row i (causal
+            // diagonal, end of the sequence); rows past the end see nothing
+            int lim = BS - 1;
+            if (p.causal && i - j * BS < lim)
+                lim = i - j * BS;
+            if (p.N - 1 - j * BS < lim)
+                lim = p.N - 1 - j * BS;
             if (!row_ok)
                 lim = -1;
+            const uint32_t tS = tmem + lane_bits + uint32_t(j & 1) * kColBuf + col0;
+            uint32_t sv[32], dv[32], pk[16];
+            ptx::tmem_ld32(tS, sv);
+            ptx::tmem_ld32(tS + kColDP, dv);
+            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int blk = 0; blk < kColsPerThread / 32; ++blk) {
-                const int col0 = g * kColsPerThread + blk * 32;
-                uint32_t sv[32], dv[32], pk[16];
-                ptx::tmem_ld32(tS + col0, sv);
-                ptx::tmem_ld32(tP + col0, dv);
-                ptx::tmem_wait_ld();
+            for (int e = 0; e < 16; ++e) {
+                float ds[2];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float ds[2];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int c = col0 + 2 * e + k;
-                        const float x = __uint_as_float(sv[2 * e + k]);
-                        const float y = __uint_as_float(dv[2 * e + k]);
-                        // masked entries get exponent -inf: exp2 gives 0, no branch
-                        const float pv = ptx::ex2(c <= lim ? fmaf(x, sl, -lse2) : -INFINITY);
-                        ds[k] = pv * (y - Di);
-                    }
-                    pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
+                for (int k = 0; k < 2; ++k) {
+                    const int c = col0 + 2 * e + k;
+                    const float x = __uint_as_float(sv[2 * e + k]);
+                    const float y = __uint_as_float(dv[2 * e + k]);
+                    // masked entries get exponent -inf: exp2 gives 0, no branch
+                    const float pv = ptx::ex2(c <= lim ? fmaf(x, sl, -lse2) : -INFINITY);
+                    ds[k] = pv * (y - Di);
                 }
-                ptx::tmem_st16(tS + col0, pk);        // dS of this block, packed
+                pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
             }
+            ptx::tmem_st16(tS, pk);                   // dS of this block, packed
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar.p_full);
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&bar.p_full[j & 1]);
         }
-        // the epilogue reads each row's dQ once: group 0 stores it
+        // the two groups store half of each row's dQ each
         if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
-            if (g == 0)
-                store_row<D>(tmem + lane_bits + kColAcc, p.scale,
-                             p.dQ + ((row0 + i) * p.H + h) * D, row_ok);
+            store_row(tmem + lane_bits + kColAcc, p.scale, p.dQ + ((row0 + i) * p.H + h) * D,
+                      row_ok, g * (D / 64), (g + 1) * (D / 64));
         }
     }
     teardown<D>(tmem);
@@ -469,76 +520,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
     const int64_t row0 = int64_t(b) * p.N;
-    const int i0 = p.causal ? kt : 0;                // first query tile that sees the keys
-    const int n_q = p.n_tiles - i0;
+    // first query sub-tile that sees the keys; at least one sub-tile follows
+    const int i0 = p.causal ? 2 * kt : 0;
+    const int n_q = p.n_sub - i0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const uint32_t tmem = setup<D>(p, smem, bar, 32u, abort_flag, tmem_slot);
+    const uint32_t tmem = setup<D>(p, bar, 32u, abort_flag, tmem_slot);
     bool aborted = false;
     uint8_t *tile_k = smem + C::kOffA0, *tile_v = smem + C::kOffA1;
     uint8_t *ring = smem + C::kOffRing;
-    float *stats = reinterpret_cast<float *>(smem + C::kOffStat);   // slot x (lse2, D) x 128
+    float *stats = reinterpret_cast<float *>(smem + C::kOffStat);   // slot x (lse2, D) x 64
 
     if (warp == kWarpLoad) {
         // ======================= TMA producer (whole warp) ===================
-        // Ring positions 2s and 2s + 1 hold Q_i and dO_i of step s (i = i0 + s);
-        // with dO_i the warp's lanes also stage the tile's log2 logsumexp and D.
+        // Ring stage of step s (i = i0 + s): Q_i then dO_i; the warp's lanes
+        // also stage the sub-tile's log2 logsumexp and D in the stage's slot.
         int last_phase[C::kStages];
         for (int s = 0; s < C::kStages; ++s)
             last_phase[s] = -1;
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar.a_full, 2 * C::kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar.a_full, 2 * C::kResBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                ptx::tma_load_3d(tile_k + c * kChunkBytes, &p.tm_k, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_k + c * kResChunkBytes, &p.tm_a0, bar.a_full, c * 64, h,
                                  int(row0 + int64_t(kt) * BT));
-                ptx::tma_load_3d(tile_v + c * kChunkBytes, &p.tm_v, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_v + c * kResChunkBytes, &p.tm_a1, bar.a_full, c * 64, h,
                                  int(row0 + int64_t(kt) * BT));
             }
         }
         int stage = 0;
         uint32_t phase = 0;
         const int64_t stat0 = (int64_t(b) * p.H + h) * p.N;
-        for (int s = 0; s < n_q && !aborted; ++s) {
+        for (int s = 0; s < n_q; ++s) {
             const int i = i0 + s;
-            for (int kv = 0; kv < 2; ++kv) {
-                int ok = 1;
-                if (lane == 0)
-                    ok = ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag, p.err_word)
-                             ? 1
-                             : 0;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    aborted = true;
-                    break;
-                }
-                if (kv == 1) {
-                    float *slot = stats + (stage >> 1) * (2 * BT);
+            // the step's statistics: global loads in flight during the slot wait
+            float ls[BS / 32], ds[BS / 32];
 #pragma unroll
-                    for (int u = 0; u < BT / 32; ++u) {
-                        const int c = lane * (BT / 32) + u;
-                        const int q = i * BT + c;
-                        const bool v = q < p.N;
-                        slot[c] = v ? p.lse[stat0 + q] * kLog2e : 0.f;
-                        slot[BT + c] = v ? p.D[stat0 + q] : 0.f;
+            for (int u = 0; u < BS / 32; ++u) {
+                const int q = i * BS + lane * (BS / 32) + u;
+                const bool v = q < p.N;
+                ls[u] = v ? p.lse[stat0 + q] : 0.f;
+                ds[u] = v ? p.D[stat0 + q] : 0.f;
+            }
+            int ok = 1;
+            if (lane == 0)
+                ok = ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag, p.err_word) ? 1
+                                                                                             : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0))
+                break;
+            if (lane == 0) {
+                uint8_t *dst = ring + stage * C::kStageBytes;
+                const int row = int(row0 + int64_t(i) * BS);
+                ptx::mbar_expect_tx(&bar.kv_full[stage], C::kStageBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    ptx::tma_load_3d(dst + c * kSubChunkBytes, &p.tm_s0, &bar.kv_full[stage],
+                                     c * 64, h, row);
+                    ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
+                                     &bar.kv_full[stage], c * 64, h, row);
+                }
+                if (i + kL2Ahead < p.n_sub)
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
+                        ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
                     }
-                }
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kTileBytes);
-                    for (int c = 0; c < C::kChunks; ++c)
-                        ptx::tma_load_3d(ring + stage * C::kTileBytes + c * kChunkBytes,
-                                         kv ? &p.tm_do : &p.tm_q, &bar.kv_full[stage], c * 64, h,
-                                         int(row0 + int64_t(i) * BT));
-                    last_phase[stage] = int(phase);
-                } else if (kv == 1) {
-                    ptx::mbar_arrive(&bar.kv_full[stage]);
-                }
-                if (++stage == C::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                last_phase[stage] = int(phase);
+            }
+            float *slot = stats + stage * (2 * BS);
+#pragma unroll
+            for (int u = 0; u < BS / 32; ++u) {
+                slot[lane * (BS / 32) + u] = ls[u] * kLog2e;
+                slot[BS + lane * (BS / 32) + u] = ds[u];
+            }
+            ptx::mbar_arrive(&bar.kv_full[stage]);       // all 32 lanes, after their writes
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
             }
         }
-        if (lane == 0 && (aborted || *abort_flag)) {
+        if (lane == 0 && *abort_flag) {
             drain_wait(bar.a_full, 0);
             for (int s = 0; s < C::kStages; ++s)
                 if (last_phase[s] >= 0)
@@ -546,84 +604,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ======================= MMA issuer ================================
-        if (lane == 0) {
-            constexpr uint32_t idesc_ss = ptx::idesc_bf16_f32(BT, BT, false);
-            constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
-            constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
-            constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kChunkBytes, 1024);
-            const uint64_t dk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_k));
-            const uint64_t dvk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_v));
-            const uint32_t ring_addr = ptx::smem_u32(ring);
-            int stage = 0;
-            uint32_t phase = 0;
-            auto advance = [&]() {
-                if (++stage == C::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            };
-            do {
-                if (!ptx::mbar_wait(bar.a_full, 0, abort_flag, p.err_word)) {
+        // ======================= MMA issuer (whole warp) =====================
+        // Order: S^T_0, dP^T_0; then per step s: S^T_{s+1}, dP^T_{s+1} (other
+        // buffer), wait for P^T_s and dS^T_s, dV += P^T_s dO_s, dK += dS^T_s Q_s.
+        // The warp runs the loop converged; one elected lane issues.
+        constexpr uint32_t idesc_ss = ptx::idesc_bf16_f32(BT, BS, false);
+        constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
+        constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
+        constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kSubChunkBytes, 1024);
+        const uint64_t dk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_k));
+        const uint64_t dvk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_v));
+        const uint32_t ring_addr = ptx::smem_u32(ring);
+        int stage = 0;
+        uint32_t phase = 0;
+        int st0 = 0, st1 = 0;                       // step's ring stage, per buffer
+        // S^T_s = K Q_s^T and dP^T_s = V dO_s^T into buffer s & 1
+        auto issue_s = [&](int s) -> bool {
+            if (!ptx::mbar_wait_warp(&bar.kv_full[stage], phase, abort_flag, p.err_word))
+                return false;
+            (s & 1 ? st1 : st0) = stage;
+            const uint32_t qaddr = ring_addr + stage * C::kStageBytes;
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            ptx::tc_fence_after_sync();
+            const uint64_t dq = ptx::smem_desc(desc_kmajor, qaddr);
+            const uint64_t ddo = ptx::smem_desc(desc_kmajor, qaddr + C::kSubBytes);
+            const uint32_t buf = tmem + uint32_t(s & 1) * kColBuf;
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(buf, dk + kmajor_off(kk, kResChunkBytes),
+                                dq + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(buf + kColDP, dvk + kmajor_off(kk, kResChunkBytes),
+                                ddo + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&bar.s_full[s & 1]);
+            }
+            __syncwarp();
+            return true;
+        };
+        do {
+            if (!ptx::mbar_wait_warp(bar.a_full, 0, abort_flag, p.err_word) || !issue_s(0)) {
+                aborted = true;
+                break;
+            }
+            for (int s = 0; s < n_q; ++s) {
+                if (s + 1 < n_q && !issue_s(s + 1)) {
                     aborted = true;
                     break;
                 }
-                for (int s = 0; s < n_q; ++s) {
-                    // S^T = K Q_i^T
-                    if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    const int q_stage = stage;
-                    const uint32_t q_addr = ring_addr + stage * C::kTileBytes;
-                    advance();
-                    ptx::tc_fence_after_sync();
-                    const uint64_t dq = ptx::smem_desc(desc_kmajor, q_addr);
+                // dV += P^T_s dO_s,  dK += dS^T_s Q_s
+                if (!ptx::mbar_wait_warp(&bar.p_full[s & 1], uint32_t(s >> 1) & 1u, abort_flag,
+                                         p.err_word)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const int st = (s & 1) ? st1 : st0;
+                const uint32_t qaddr = ring_addr + st * C::kStageBytes;
+                const uint64_t dq_mn = ptx::smem_desc(desc_mnmajor, qaddr);
+                const uint64_t ddo_mn = ptx::smem_desc(desc_mnmajor, qaddr + C::kSubBytes);
+                const uint32_t a_tm = tmem + uint32_t(s & 1) * kColBuf;
+                if (ptx::elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(tmem + kColS, dk + off, dq + off, idesc_ss, kk > 0 ? 1u : 0u);
-                    }
-                    // dP^T = V dO_i^T
-                    if (!ptx::mbar_wait(&bar.kv_full[stage], phase, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    const int do_stage = stage;
-                    const uint32_t do_addr = ring_addr + stage * C::kTileBytes;
-                    advance();
-                    ptx::tc_fence_after_sync();
-                    const uint64_t ddo = ptx::smem_desc(desc_kmajor, do_addr);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
-                        ptx::mma_ss(tmem + kColP, dvk + off, ddo + off, idesc_ss, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(bar.s_full);
-                    // dV += P^T dO_i,  dK += dS^T Q_i
-                    if (!ptx::mbar_wait(bar.p_full, uint32_t(s) & 1u, abort_flag, p.err_word)) {
-                        aborted = true;
-                        break;
-                    }
-                    ptx::tc_fence_after_sync();
-                    const uint64_t ddo_mn = ptx::smem_desc(desc_mnmajor, do_addr);
-                    const uint64_t dq_mn = ptx::smem_desc(desc_mnmajor, q_addr);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc, tmem + kColS + packed_col(kk),
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ts(tmem + kColAcc, a_tm + packed_col(kk),
                                     ddo_mn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc + D, tmem + kColP + packed_col(kk),
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ts(tmem + kColAcc + D, a_tm + kColDP + packed_col(kk),
                                     dq_mn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
                                     (s > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(&bar.kv_empty[q_stage]);
-                    ptx::mma_commit(&bar.kv_empty[do_stage]);
+                    ptx::mma_commit(&bar.kv_empty[st]);
                 }
-                if (!aborted)
-                    ptx::mma_commit(bar.o_full);
-            } while (false);
+                __syncwarp();
+            }
+        } while (false);
+        if (ptx::elect_one()) {
+            if (!aborted)
+                ptx::mma_commit(bar.o_full);
             ptx::mma_commit(bar.drain);
             drain_wait(bar.drain, 0);
         }
@@ -634,82 +697,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = warp >> 2;                     // column group
         const int k = kt * BT + r;
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_bits + kColS;
-        const uint32_t tP = tmem + lane_bits + kColP;
         const float sl = p.scale_log2;
+        const int col0 = g * kColsPerThread;
         for (int s = 0; s < n_q; ++s) {
             const int i = i0 + s;
-            // the statistics arrive with dO_i at ring position 2s + 1
-            const int pos = 2 * s + 1;
-            const int st = pos % C::kStages;
-            if (!ptx::mbar_wait(bar.s_full, uint32_t(s) & 1u, abort_flag, p.err_word) ||
-                !ptx::mbar_wait(&bar.kv_full[st], uint32_t(pos / C::kStages) & 1u, abort_flag,
+            // the statistics arrive with the step's ring stage; they are read
+            // into registers before the wait for S^T_s
+            const int st = s % C::kStages;
+            if (!row_wait(&bar.kv_full[st], uint32_t(s / C::kStages) & 1u, abort_flag,
+                                p.err_word)) {
+                aborted = true;
+                break;
+            }
+            float lv[32], dd[32];
+            {
+                const float *lse2s = stats + st * (2 * BS) + col0;
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + 4 * e4);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(lse2s + BS + 4 * e4);
+                    lv[4 * e4] = l4.x;
+                    lv[4 * e4 + 1] = l4.y;
+                    lv[4 * e4 + 2] = l4.z;
+                    lv[4 * e4 + 3] = l4.w;
+                    dd[4 * e4] = d4.x;
+                    dd[4 * e4 + 1] = d4.y;
+                    dd[4 * e4 + 2] = d4.z;
+                    dd[4 * e4 + 3] = d4.w;
+                }
+            }
+            if (!row_wait(&bar.s_full[s & 1], uint32_t(s >> 1) & 1u, abort_flag,
                                 p.err_word)) {
                 aborted = true;
                 break;
             }
             ptx::tc_fence_after_sync();
-            const float *lse2s = stats + (st >> 1) * (2 * BT);
-            const float *Ds = lse2s + BT;
             // visible columns [lo, hi]: causal keeps queries >= the key; the
             // sequence ends at N
-            const int lo = (p.causal && i == kt) ? r : 0;
-            int hi = p.N - 1 - i * BT;
-            if (hi > BT - 1)
-                hi = BT - 1;
+            const int lo = p.causal ? k - i * BS : 0;
+            int hi = p.N - 1 - i * BS;
+            if (hi > BS - 1)
+                hi = BS - 1;
+            const uint32_t tS = tmem + lane_bits + uint32_t(s & 1) * kColBuf + col0;
+            uint32_t sv[32], dv[32], pk[16], dk[16];
+            ptx::tmem_ld32(tS, sv);
+            ptx::tmem_ld32(tS + kColDP, dv);
+            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int blk = 0; blk < kColsPerThread / 32; ++blk) {
-                const int col0 = g * kColsPerThread + blk * 32;
-                uint32_t sv[32], dv[32], pk[16], dk[16];
-                ptx::tmem_ld32(tS + col0, sv);
-                ptx::tmem_ld32(tP + col0, dv);
-                ptx::tmem_wait_ld();
+            for (int e2 = 0; e2 < 16; ++e2) {
+                float pv[2], ds[2];
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const int c0 = col0 + 4 * e4;
-                    const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + c0);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(Ds + c0);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], ds[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = c0 + u;
-                        const float x = __uint_as_float(sv[4 * e4 + u]);
-                        const float y = __uint_as_float(dv[4 * e4 + u]);
-                        // masked entries get exponent -inf: exp2 gives 0, no branch
-                        pv[u] = ptx::ex2((c >= lo && c <= hi) ? fmaf(x, sl, -lv[u]) : -INFINITY);
-                        ds[u] = pv[u] * (y - dd[u]);
-                    }
-                    pk[2 * e4] = ptx::pack_bf16x2(pv[0], pv[1]);
-                    pk[2 * e4 + 1] = ptx::pack_bf16x2(pv[2], pv[3]);
-                    dk[2 * e4] = ptx::pack_bf16x2(ds[0], ds[1]);
-                    dk[2 * e4 + 1] = ptx::pack_bf16x2(ds[2], ds[3]);
+                for (int u = 0; u < 2; ++u) {
+                    const int e = 2 * e2 + u;
+                    const int c = col0 + e;
+                    const float x = __uint_as_float(sv[e]);
+                    const float y = __uint_as_float(dv[e]);
+                    // masked entries get exponent -inf: exp2 gives 0, no branch
+                    pv[u] = ptx::ex2((c >= lo && c <= hi) ? fmaf(x, sl, -lv[e]) : -INFINITY);
+                    ds[u] = pv[u] * (y - dd[e]);
                 }
-                ptx::tmem_st16(tS + col0, pk);        // P^T of this block, packed
-                ptx::tmem_st16(tP + col0, dk);        // dS^T of this block, packed
+                pk[e2] = ptx::pack_bf16x2(pv[0], pv[1]);
+                dk[e2] = ptx::pack_bf16x2(ds[0], ds[1]);
             }
+            ptx::tmem_st16(tS, pk);                   // P^T of this block, packed
+            ptx::tmem_st16(tS + kColDP, dk);          // dS^T of this block, packed
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar.p_full);
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&bar.p_full[s & 1]);
         }
         if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
             const bool key_ok = k < p.N;
             // group 0 writes dV, group 1 writes dK
             if (g == 0)
-                store_row<D>(tmem + lane_bits + kColAcc, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
-                             key_ok);
-            if (g == 1)
-                store_row<D>(tmem + lane_bits + kColAcc + D, p.scale,
-                             p.dK + ((row0 + k) * p.H + h) * D, key_ok);
+                store_row(tmem + lane_bits + kColAcc, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
+                          key_ok, 0, D / 32);
+            else
+                store_row(tmem + lane_bits + kColAcc + D, p.scale,
+                          p.dK + ((row0 + k) * p.H + h) * D, key_ok, 0, D / 32);
         }
     }
     teardown<D>(tmem);
 }
 
 template <int D>
-int launch_bwd_d(const BwdParams &p, cudaStream_t stream)
+int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t stream)
 {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -724,12 +798,13 @@ int launch_bwd_d(const BwdParams &p, cudaStream_t stream)
     });
     if (attr_err != cudaSuccess)
         return FA_ERR_CUDA;
-    const int64_t blocks = int64_t(p.n_tiles) * p.B * p.H;
-    attn_bwd_dq_kernel<D><<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p);
+    const int64_t blocks = int64_t(p_dq.n_tiles) * p_dq.B * p_dq.H;
+    attn_bwd_dq_kernel<D>
+        <<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dq);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     attn_bwd_dkdv_kernel<D>
-        <<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p);
+        <<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dkdv);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -739,11 +814,6 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
 {
     BwdParams p;
     const int64_t total = int64_t(a.B) * a.N;
-    if (!make_tmap_bf16(&p.tm_q, a.Q, total, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_k, a.K, total, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_v, a.V, total, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_do, a.dO, total, a.H, a.d))
-        return FA_ERR_CUDA;
     p.O = static_cast<const __nv_bfloat16 *>(a.O);
     p.dO = static_cast<const __nv_bfloat16 *>(a.dO);
     p.lse = a.lse;
@@ -755,6 +825,7 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
     p.H = a.H;
     p.N = a.N;
     p.n_tiles = (a.N + BT - 1) / BT;
+    p.n_sub = (a.N + BS - 1) / BS;
     p.scale = a.scale;
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
@@ -764,7 +835,18 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
         return FA_OK;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
-    return a.d == 64 ? launch_bwd_d<64>(p, stream) : launch_bwd_d<128>(p, stream);
+    BwdParams p_dq = p, p_dkdv = p;
+    if (!make_tmap_bf16(&p_dq.tm_a0, a.Q, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p_dq.tm_a1, a.dO, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p_dq.tm_s0, a.K, total, a.H, a.d, BS) ||
+        !make_tmap_bf16(&p_dq.tm_s1, a.V, total, a.H, a.d, BS) ||
+        !make_tmap_bf16(&p_dkdv.tm_a0, a.K, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p_dkdv.tm_a1, a.V, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p_dkdv.tm_s0, a.Q, total, a.H, a.d, BS) ||
+        !make_tmap_bf16(&p_dkdv.tm_s1, a.dO, total, a.H, a.d, BS))
+        return FA_ERR_CUDA;
+    return a.d == 64 ? launch_bwd_d<64>(p_dq, p_dkdv, stream)
+                     : launch_bwd_d<128>(p_dq, p_dkdv, stream);
 }
 
 }  // namespace fa

@@ -48,6 +48,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Adds `bytes` to the transaction count of the current phase without arriving
+// (the arrivals come separately).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -66,18 +74,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Waits for the phase of `bar` with the given parity to complete.  Every wait is
-// bounded: it gives up after kWaitTimeoutNs of wall time (checked on the global
-// timer every 256 polls) or kWaitMaxPolls polls, or as soon as another role of
-// the CTA has raised *abort.  On giving up it ORs FA_DEVERR_WAIT_TIMEOUT into the
-// device error word, raises *abort and returns false; the caller then leaves
-// its loop.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort, int *err_word)
+// Slow path of mbar_wait (kept out of line: the inlined fast path is a single
+// try_wait, which keeps the MMA-issuing loops short).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                                   volatile int *abort, int *err_word)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
-    uint64_t t0 = globaltimer();
+    const uint64_t t0 = globaltimer();
     for (uint32_t it = 1; it < kWaitMaxPolls; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
@@ -91,6 +93,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     record_device_error(err_word, FA_DEVERR_WAIT_TIMEOUT);
     *abort = 1;
     return false;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Every wait is
+// bounded: it gives up after kWaitTimeoutNs of wall time (checked on the global
+// timer every 256 polls) or kWaitMaxPolls polls, or as soon as another role of
+// the CTA has raised *abort.  On giving up it ORs FA_DEVERR_WAIT_TIMEOUT into the
+// device error word, raises *abort and returns false; the caller then leaves
+// its loop.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort, int *err_word)
+{
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, err_word);
+}
+
+// mbar_wait by all 32 lanes of a warp; the lanes agree on the result (a wait
+// that gives up in one lane gives up in all), so the warp stays converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort, int *err_word)
+{
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err_word)) != 0;
+}
+
+// One lane of a converged warp (elect.sync over the full mask): the lane that
+// issues a warp's tcgen05.mma / commit instructions.  Running the issuing loop
+// on the whole warp keeps its operands warp-uniform.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -116,6 +152,14 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *t
         : "memory");
 }
 
+// Brings a tensor-map box into L2 ahead of its TMA load (no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *tmap, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap))

@@ -61,6 +61,8 @@ def normwise(g, ref):
     (1, 1, 1, 64, True),         # one token
     (1, 2, 385, 128, False),
     (2, 1, 640, 64, True),
+    (1, 2, 192, 128, True),      # last tile exactly one 64-row sub-tile
+    (1, 1, 65, 64, True),        # two sub-tiles, one tile
 ])
 def test_bwd_matches_oracle(dev, B, H, N, d, causal):
     Q, K, V, dO = make_inputs(B, H, N, d, seed=N * 7 + d + B)
