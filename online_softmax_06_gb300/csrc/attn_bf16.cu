@@ -533,12 +533,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (c * 32 + e > lim)
                             sr[c][e] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // row maximum: three-input maxes over four independent chains
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int q = 0; q < 16; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+                for (int k = 0; k < 4; ++k) {
+                    const int c = q * 8 + 2 * k;
+                    m4[k] = ptx::max3(m4[k], __uint_as_float(sr[c >> 5][c & 31]),
+                                      __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]));
+                }
+            const float mx = fmaxf(ptx::max3(m4[0], m4[1], m4[2]), m4[3]);
             // Conditional rescale (booklet §5.4): the row keeps a reference
             // maximum m and moves it only when the tile maximum exceeds it by
             // more than kRescaleLog2, so every p stays <= 2^kRescaleLog2 (far
@@ -558,7 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // exponent arguments are formed two at a time (packed fp32x2 FMA)
             const float2 sl2 = make_float2(slj, slj);
             const float2 nm2 = make_float2(-m_use, -m_use);
-            float rowsum = 0.f;
+            // the row sum is accumulated two lanes at a time (packed fp32x2 add)
+            float2 rowsum2 = make_float2(0.f, 0.f);
             if constexpr (FP8) {
                 // P' = e4m3(p) four per column over columns 64..95 of S_t (p <=
                 // 2^kRescaleLog2 < 448, so nothing saturates)
@@ -576,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sl2, nm2);
                     const float p0 = ptx::ex2(a.x), p1 = ptx::ex2(a.y);
                     const float p2 = ptx::ex2(c.x), p3 = ptx::ex2(c.y);
-                    rowsum += (p0 + p1) + (p2 + p3);
+                    rowsum2 = __fadd2_rn(rowsum2, __fadd2_rn(make_float2(p0, p1),
+                                                             make_float2(p2, p3)));
                     pk[q4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
                 }
                 ptx::tmem_st32(tS + kColPinS, pk);
@@ -591,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   __uint_as_float(sr[(col + 1) >> 5][(col + 1) & 31]));
                     const float2 arg = __ffma2_rn(sv, sl2, nm2);
                     const float p0 = ptx::ex2(arg.x), p1 = ptx::ex2(arg.y);
-                    rowsum += p0 + p1;
+                    rowsum2 = __fadd2_rn(rowsum2, make_float2(p0, p1));
                     pk[e] = ptx::pack_bf16x2(p0, p1);
                 }
                 ptx::tmem_st32(tS + kColPinS + half * 32, pk);
             }
-            l = l * corr + rowsum;
+            l = l * corr + (rowsum2.x + rowsum2.y);
             m = m_new;
 
             // rescale this row of O~ when its reference moved (never on the

@@ -442,6 +442,14 @@ __device__ __forceinline__ float ex2(float x)
 }
 
 // Packs two floats into bf16x2, round-to-nearest-even; `lo` lands in bits 0..15.
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
