@@ -16,9 +16,11 @@
 // tile resident in shared memory and streams the other operand in 64-row
 // sub-tiles:
 //   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile), Q and
-//     dO resident.  Each query row is served by two threads (32 columns of a
-//     sub-tile each): they form D_i = dO_i . O_i (stored for the second kernel),
-//     then for every visible 64-key sub-tile j turn S = Q K_j^T and
+//     dO resident.  The row warps first form D_i = dO_i . O_i together (O
+//     rows from global memory, dO from the resident tile; stored for the
+//     second kernel).  Each query row is then served by two threads (32
+//     columns of a sub-tile each): for every visible 64-key sub-tile j they
+//     turn S = Q K_j^T and
 //     dP = dO V_j^T (tcgen05, fp32 in TMEM) into dS = P o (dP - D_i) in bf16 in
 //     TMEM, and the MMA warp accumulates dQ += dS K_j in TMEM.
 //   * attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key tile), K and
@@ -421,30 +423,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = i < p.N;
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
         const int64_t stat = (int64_t(b) * p.H + h) * p.N + i;
-        // D_i = dO_i . O_i (fp32); group 0 stores it for the dK/dV kernel
-        float Di = 0.f, lse2 = 0.f;
-        if (row_ok) {
-            const uint4 *o4 = reinterpret_cast<const uint4 *>(p.O + ((row0 + i) * p.H + h) * D);
-            const uint4 *g4 = reinterpret_cast<const uint4 *>(p.dO + ((row0 + i) * p.H + h) * D);
-#pragma unroll 4
-            for (int u = 0; u < D / 8; ++u) {
-                const uint4 ov = o4[u], gv = g4[u];
-                const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+        // D_i = dO_i . O_i (fp32), computed by the row warps together: a warp
+        // takes 16 rows, D / 8 lanes per row, each lane 8 elements: O from
+        // global memory (whole rows per load instruction), dO from the
+        // resident shared-memory tile (128-byte swizzle: 16-byte unit u of row
+        // r sits at unit u ^ (r % 8) of the row's 128 bytes in its 64-column
+        // chunk).  The lanes of a row reduce with shuffles; the sums meet the
+        // row threads in shared memory.
+        constexpr int kLanesPerRow = D / 8, kRowsPerInst = 32 / kLanesPerRow;
+        constexpr int kRowsPerWarp = BT / kRowWarps;          // 16
+        float *xch = reinterpret_cast<float *>(smem + C::kOffStat);   // 128 sums
+        {
+            const int sub = lane / kLanesPerRow, lr = lane % kLanesPerRow;
+            uint4 ov[kRowsPerWarp / kRowsPerInst];
+#pragma unroll
+            for (int k = 0; k < kRowsPerWarp / kRowsPerInst; ++k) {
+                const int rr = warp * kRowsPerWarp + k * kRowsPerInst + sub;
+                const int qi = qt * BT + rr;
+                ov[k] = qi < p.N ? *reinterpret_cast<const uint4 *>(
+                                       p.O + ((row0 + qi) * p.H + h) * D + lr * 8)
+                                 : make_uint4(0, 0, 0, 0);
+            }
+            const bool a_ok = row_wait(bar.a_full, 0, abort_flag, p.err_word);
+#pragma unroll
+            for (int k = 0; k < kRowsPerWarp / kRowsPerInst; ++k) {
+                const int rr = warp * kRowsPerWarp + k * kRowsPerInst + sub;
+                const int u = lr & 7, chunk = lr >> 3;
+                const uint4 gv = a_ok ? *reinterpret_cast<const uint4 *>(
+                                            tile_do + chunk * kResChunkBytes + rr * 128 +
+                                            ((u ^ (rr & 7)) << 4))
+                                      : make_uint4(0, 0, 0, 0);
+                const uint32_t ow[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
                 const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                float part = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 of =
                         __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[e]));
                     const float2 gf =
                         __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gw[e]));
-                    Di = fmaf(of.x, gf.x, Di);
-                    Di = fmaf(of.y, gf.y, Di);
+                    part = fmaf(of.x, gf.x, part);
+                    part = fmaf(of.y, gf.y, part);
                 }
+#pragma unroll
+                for (int o = kLanesPerRow / 2; o > 0; o >>= 1)
+                    part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (lr == 0)
+                    xch[rr] = part;
             }
-            if (g == 0)
-                p.D[stat] = Di;
-            lse2 = p.lse[stat] * kLog2e;
         }
+        const float lse_raw = row_ok ? p.lse[stat] : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"n"(BT * G) : "memory");   // the row threads
+        const float Di = xch[r];
+        if (g == 0 && row_ok)
+            p.D[stat] = Di;
+        const float lse2 = lse_raw * kLog2e;
         const float sl = p.scale_log2;
         const int col0 = g * kColsPerThread;
 

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "../../include/fa.h"
 #include "launch.h"
@@ -25,7 +26,9 @@ namespace fa {
 namespace {
 
 constexpr int kRows = 128;          // rows per tile
-constexpr int kWarps = 16;          // 8 rows per warp: the rows stay in registers
+// 32 warps of 4 rows each, two CTAs per SM (32 registers a thread): loads of
+// one CTA overlap the other's arithmetic; the rows stay in registers
+constexpr int kWarps = 32;
 constexpr float kE4M3Max = 448.f;
 
 __device__ __forceinline__ float warp_max(float v)
@@ -67,11 +70,12 @@ __device__ __forceinline__ void rotate_row(float (&x)[D / 32], const float (&sg)
     }
 #pragma unroll
     for (int b = 0; b < 5; ++b) {                  // partners in other lanes
-        const bool upper = (lane >> b) & 1;
+        // the lower lane keeps x + y, the upper y - x: fma(x, +-1, y)
+        const float sgn = ((lane >> b) & 1) ? -1.f : 1.f;
 #pragma unroll
         for (int k = 0; k < E; ++k) {
             const float y = __shfl_xor_sync(0xffffffffu, x[k], 1 << b);
-            x[k] = upper ? (y - x[k]) : (x[k] + y);
+            x[k] = fmaf(x[k], sgn, y);
         }
     }
     const float inv = rsqrtf(float(D));
@@ -90,7 +94,7 @@ struct QuantParams {
 
 // blockIdx: x = tile, y = b * H + h, z = 0 (Q), 1 (K), 2 (V amax only).
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) fp8_qk_kernel(const QuantParams p)
+__global__ void __launch_bounds__(kWarps * 32, 2) fp8_qk_kernel(const QuantParams p)
 {
     constexpr int E = D / 32;
     constexpr int kRowsPerWarp = kRows / kWarps;
@@ -105,33 +109,34 @@ __global__ void __launch_bounds__(kWarps * 32) fp8_qk_kernel(const QuantParams p
         sg[k] = p.signs[lane * E + k];
 
     float x[kRowsPerWarp][E];
-    float amax = 0.f;
+    // every row's load is issued before any arithmetic
+    using Raw = typename std::conditional<E == 4, uint2, uint32_t>::type;
+    Raw raw[kRowsPerWarp];
 #pragma unroll
     for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const int row = tile * kRows + warp * kRowsPerWarp + rr;
-        if (row < p.N) {
-            const __nv_bfloat16 *rp = src + ((int64_t(b) * p.N + row) * p.H + h) * D + lane * E;
-            // one 8-byte (d = 128) or 4-byte (d = 64) load per lane and row
-            if constexpr (E == 4) {
-                const uint2 u = *reinterpret_cast<const uint2 *>(rp);
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-                const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-                x[rr][0] = a.x;
-                x[rr][1] = a.y;
-                x[rr][2] = c.x;
-                x[rr][3] = c.y;
-            } else {
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(rp));
-                x[rr][0] = a.x;
-                x[rr][1] = a.y;
-            }
-            if (which < 2)
-                rotate_row<D>(x[rr], sg, lane);
-        } else {
+        const __nv_bfloat16 *rp = src + ((int64_t(b) * p.N + row) * p.H + h) * D + lane * E;
+        raw[rr] = row < p.N ? *reinterpret_cast<const Raw *>(rp) : Raw{};
+    }
+    float amax = 0.f;
 #pragma unroll
-            for (int k = 0; k < E; ++k)
-                x[rr][k] = 0.f;
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        if constexpr (E == 4) {
+            const uint2 u = raw[rr];
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            x[rr][0] = a.x;
+            x[rr][1] = a.y;
+            x[rr][2] = c.x;
+            x[rr][3] = c.y;
+        } else {
+            const uint32_t u = raw[rr];
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+            x[rr][0] = a.x;
+            x[rr][1] = a.y;
         }
+        if (which < 2)
+            rotate_row<D>(x[rr], sg, lane);
 #pragma unroll
         for (int k = 0; k < E; ++k)
             amax = fmaxf(amax, fabsf(x[rr][k]));
@@ -140,10 +145,7 @@ __global__ void __launch_bounds__(kWarps * 32) fp8_qk_kernel(const QuantParams p
     if (lane == 0)
         red[warp] = amax;
     __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w)
-        amax = fmaxf(amax, red[w]);
+    amax = warp_max(red[lane]);             // one partial per warp, 32 warps
     const int64_t sidx = int64_t(bh) * p.n_tiles + tile;
     if (which == 2) {
         if (threadIdx.x == 0)
