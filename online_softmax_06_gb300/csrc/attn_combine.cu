@@ -46,25 +46,32 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int64_t split_stride_lse = int64_t(B) * H * N;
     const int64_t lse_off = (int64_t(b) * H + h) * N + i;
 
-    // m = max_s lse_s; lse = m + ln sum_s exp(lse_s - m)   (log2 units inside)
-    float mx = -INFINITY;
-    for (int s = lane; s < splits; s += 32)
+    // m = max_s lse_s; lse = m + ln sum_s exp(lse_s - m)   (log2 units inside).
+    // Lane l keeps lse of split l (the first chunk of 32) in a register, so
+    // with up to 32 splits every lse is read once.
+    const float x0 = lane < splits ? lse_accum[lane * split_stride_lse + lse_off] * kLog2e
+                                   : -INFINITY;
+    float mx = x0;
+    for (int s = lane + 32; s < splits; s += 32)
         mx = fmaxf(mx, lse_accum[s * split_stride_lse + lse_off] * kLog2e);
     for (int o = 16; o > 0; o >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float sum = 0.f;
-    if (mx != -INFINITY)
-        for (int s = lane; s < splits; s += 32)
+    if (mx != -INFINITY) {
+        sum = ptx::ex2(x0 - mx);                     // 0 past the last split
+        for (int s = lane + 32; s < splits; s += 32)
             sum += ptx::ex2(lse_accum[s * split_stride_lse + lse_off] * kLog2e - mx);
+    }
     for (int o = 16; o > 0; o >>= 1)
         sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float total = (mx == -INFINITY) ? -INFINITY : mx + log2f(sum);   // log2 units
 
     // O = sum_s w_s O_s with w_s = exp(lse_s - lse).  Lane l holds w of split
-    // c0 + l of the current chunk of 32; the splits are taken eight at a time
-    // with their loads issued before the FMAs, so a warp keeps eight 128-bit
+    // c0 + l of the current chunk of 32; the splits are taken sixteen at a time
+    // with their loads issued before the FMAs, so a warp keeps sixteen 128-bit
     // loads per lane in flight.  A split with w = 0 (lse_s = -inf: it saw no
     // key of the row, its O_s was never written) is not read.
+    constexpr int kBatch = 16;
     using Vec = typename std::conditional<kPerLane == 4, float4, float2>::type;
     float acc[kPerLane];
 #pragma unroll
@@ -75,19 +82,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     if (total != -INFINITY) {
         for (int c0 = 0; c0 < splits; c0 += 32) {
             const int s_l = c0 + lane;
-            const float w_l = s_l < splits
-                                  ? ptx::ex2(lse_accum[s_l * split_stride_lse + lse_off] * kLog2e -
-                                             total)
-                                  : 0.f;
+            const float x_l = c0 == 0 ? x0
+                                      : (s_l < splits
+                                             ? lse_accum[s_l * split_stride_lse + lse_off] * kLog2e
+                                             : -INFINITY);
+            const float w_l = ptx::ex2(x_l - total);   // 0 past the last split
             const int n = splits - c0 < 32 ? splits - c0 : 32;
-            for (int u0 = 0; u0 < n; u0 += 8) {
-                float w[8];
-                Vec v[8];
+            for (int u0 = 0; u0 < n; u0 += kBatch) {
+                float w[kBatch];
+                Vec v[kBatch];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    w[u] = __shfl_sync(0xffffffffu, w_l, u0 + u);   // 0 past the last split
+                for (int u = 0; u < kBatch; ++u)
+                    w[u] = __shfl_sync(0xffffffffu, w_l, (u0 + u) & 31);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kBatch; ++u) {
+                    if (u0 + u >= n)
+                        w[u] = 0.f;
                     const Vec *src = reinterpret_cast<const Vec *>(
                         O_accum + (c0 + u0 + u) * split_stride_o + o_off);
                     if (w[u] != 0.f)
@@ -96,7 +106,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                         v[u] = Vec{};
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kBatch; ++u) {
                     const float *f = reinterpret_cast<const float *>(&v[u]);
 #pragma unroll
                     for (int e = 0; e < kPerLane; ++e)

@@ -101,7 +101,7 @@ def test_f32_varlen(dev, causal):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 256, 300, 513, 1024])
+@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 256, 300, 513, 1024, 1500])
 def test_bf16_dense_shapes(dev, N, d, causal):
     Q, K, V = workloads.attention_inputs((2, N, 3, d), seed=1000 * d + N + causal)
     O, lse = gpu_dense(Q, K, V, causal, dev)
