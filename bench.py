@@ -278,35 +278,48 @@ def time_attention(fa, w, dev, steps, warmup, dist, clocks):
 
 
 def time_e2e(fa, w, dev, steps, warmup):
-    """Same metric through the C ABI with host buffers: every step copies Q, K, V
-    from pinned host memory, runs the kernel and copies O and lse back."""
+    """Same metric through the C ABI with host buffers: every step takes Q, K, V
+    from pinned host memory and leaves O and lse in pinned host memory.  Dense
+    workloads call fa_attention_fwd_host (the library copies head group by
+    head group and overlaps the copies with the kernels); packed batches copy
+    with torch around fa_attention_fwd_varlen."""
     import torch
     Q, K, V = w.inputs()
     hq, hk, hv = (t.pin_memory() for t in (Q, K, V))
-    q, k, v = (torch.empty_like(t, device=dev) for t in (Q, K, V))
-    o = torch.empty_like(q)
     lse_shape = (w.H, w.total) if w.varlen else (w.B, w.H, w.N)
-    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     ho = torch.empty_like(Q).pin_memory()
     hl = torch.empty(lse_shape, dtype=torch.float32).pin_memory()
-    cu = torch.from_numpy(w.cu_seqlens()).to(dev) if w.varlen else None
     stream = torch.cuda.current_stream(dev)
     fa.fa_set_stream(stream.cuda_stream)
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+    if w.varlen:
+        q, k, v = (torch.empty_like(t, device=dev) for t in (Q, K, V))
+        o = torch.empty_like(q)
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+        cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+        args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
 
-    def step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        if w.varlen:
+        def step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
             rc = fa.fa_attention_fwd_varlen(*args, w.B, w.H, w.N, w.total, w.d, w.scale,
                                             int(w.causal), cu.data_ptr())
-        else:
-            rc = fa.fa_attention_fwd(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal), None)
-        if rc != 0:
-            raise RuntimeError(fa.strerror(rc))
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+            if rc != 0:
+                raise RuntimeError(fa.strerror(rc))
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        api = "fa_attention_fwd_varlen (torch copies around it)"
+    else:
+        nbytes = fa.fa_attention_host_workspace_bytes(w.B, w.H, w.N, w.d)
+        ws = torch.empty(int(nbytes), dtype=torch.uint8, device=dev)
+        args = (hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(),
+                w.B, w.H, w.N, w.d, w.scale, int(w.causal), ws.data_ptr(), int(nbytes))
+
+        def step():
+            rc = fa.fa_attention_fwd_host(*args)
+            if rc != 0:
+                raise RuntimeError(fa.strerror(rc))
+        api = "fa_attention_fwd_host"
 
     for _ in range(warmup):
         step()
@@ -322,7 +335,7 @@ def time_e2e(fa, w, dev, steps, warmup):
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
     return {"value": w.flops() * steps / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps, "api": api}
 
 
 def time_softmax(fa, dev, Ns, reps, peaks, clocks):

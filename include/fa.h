@@ -196,6 +196,40 @@ FA_API int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, voi
 FA_API int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * bf16 attention forward on HOST buffers: the same result as fa_attention_fwd
+ * on a dense batch (bit for bit: the same kernel runs on each head), with the
+ * host <-> device copies inside the call and overlapped with the work.  The
+ * pages' method is unchanged; they say nothing of where the tensors live, so
+ * this entry point is the library's own (offload of whole batches).
+ *   Q, K, V: HOST bf16 [B, N, H, d], read; O: HOST bf16 [B, N, H, d] and lse:
+ *   HOST fp32 [B, H, N], written.  Page-locked (pinned) host memory is needed
+ *   for the copies to overlap anything; pageable memory still works.
+ *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
+ *   fa_attention_host_workspace_bytes(B, H, N, d) bytes (device copies of Q,
+ *   K, V, O and lse); contents on entry are ignored.
+ *   d: 64 or 128.
+ * The heads are taken in groups: for each group a strided copy brings its
+ * slices of Q, K and V to the device (one stream), the attention kernel runs
+ * on that head range (the library stream), and its slices of O and lse go
+ * back (a third stream), so the copies of one group overlap the work and the
+ * copies of the others.  Every operation is ordered after the work already on
+ * the library stream, and the library stream waits for the last copy: the
+ * call is asynchronous like the others, and O and lse are complete once the
+ * library stream has been synchronised.  The helper streams and events are
+ * created once per device; concurrent calls from several threads must not
+ * overlap.
+ * Errors: FA_ERR_NULL_POINTER, FA_ERR_BAD_SIZE (also a workspace that is too
+ * small), FA_ERR_UNSUPPORTED (d), FA_ERR_MISALIGNED (workspace), FA_ERR_TOO_LARGE,
+ * FA_ERR_NO_DEVICE, FA_ERR_CUDA.
+ */
+FA_API int fa_attention_fwd_host(const void *Q, const void *K, const void *V, void *O, float *lse,
+                                 int B, int H, int N, int d, float scale, int causal,
+                                 void *workspace, int64_t workspace_bytes);
+
+/* Workspace bytes fa_attention_fwd_host needs, or a negative FA_ERR_* code. */
+FA_API int64_t fa_attention_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * The split count fa_attention_fwd_splitkv uses for num_splits = 0 on the
  * current device: as many splits as fill the SMs in one wave (floor of SMs /
  * 256-query blocks, 1 when the blocks alone fill more than half of the SMs),

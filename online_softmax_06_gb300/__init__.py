@@ -10,7 +10,8 @@ Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
 ``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_fwd_fp8``,
-``fa_attention_fp8_workspace_bytes``,
+``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
+``fa_attention_host_workspace_bytes``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
 ``fa_version``.
 Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
@@ -67,6 +68,10 @@ def lib():
                                            vp, i64]
         L.fa_attention_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.fa_attention_fp8_workspace_bytes.restype = i64
+        L.fa_attention_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp,
+                                            i64]
+        L.fa_attention_host_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.fa_attention_host_workspace_bytes.restype = i64
         L.fa_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                        i32, f32, i32]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -81,6 +86,7 @@ def lib():
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
                      "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd", "fa_attention_fwd_fp8",
+                     "fa_attention_fwd_host",
                      "fa_set_stream", "fa_get_device_error", "fa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -143,6 +149,16 @@ def fa_attention_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, causal, signs, work
 
 def fa_attention_fp8_workspace_bytes(B, H, N, d) -> int:
     return lib().fa_attention_fp8_workspace_bytes(B, H, N, d)
+
+
+def fa_attention_fwd_host(q, k, v, o, lse, B, H, N, d, scale, causal, workspace,
+                          workspace_bytes) -> int:
+    return lib().fa_attention_fwd_host(q, k, v, o, lse, B, H, N, d, scale, causal, workspace,
+                                       workspace_bytes)
+
+
+def fa_attention_host_workspace_bytes(B, H, N, d) -> int:
+    return lib().fa_attention_host_workspace_bytes(B, H, N, d)
 
 
 def fa_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale, causal) -> int:
@@ -317,6 +333,48 @@ def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None 
                               float(scale), int(bool(causal)), _ptr(signs), _ptr(workspace),
                               workspace.numel())
     _check(rc, "fa_attention_fwd_fp8")
+    return o, lse, workspace
+
+
+def attention_fwd_host(q, k, v, causal: bool = False, scale: float | None = None,
+                       workspace=None, device=None, out=None):
+    """bf16 attention forward on HOST tensors through the C ABI (dense
+    [B, N, H, d]); the library copies to and from the device itself, head
+    group by head group, overlapping the copies with the kernels.
+
+    ``q``, ``k``, ``v``: contiguous bf16 CPU tensors (pinned for overlap).
+    The DEVICE workspace (uint8, fa_attention_host_workspace_bytes) is
+    allocated here on ``device`` (default cuda:current) unless given; ``out``
+    may pass preallocated (O, lse) CPU tensors.  The call returns after the
+    library stream has been synchronised.  Returns (O, lse, workspace).
+    """
+    import torch
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v must be contiguous bf16 CPU tensors")
+        if t.shape != q.shape:
+            raise ValueError("q, k, v must have one shape")
+    B, N, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    nbytes = fa_attention_host_workspace_bytes(B, H, N, d)
+    if nbytes < 0:
+        raise FaError(int(nbytes), "fa_attention_host_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=dev)
+    if out is None:
+        pin = q.is_pinned()
+        o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    else:
+        o, lse = out
+    _use_current_stream(dev)
+    rc = fa_attention_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                               float(scale), int(bool(causal)), _ptr(workspace),
+                               workspace.numel())
+    _check(rc, "fa_attention_fwd_host")
+    torch.cuda.current_stream(dev).synchronize()
     return o, lse, workspace
 
 

@@ -98,6 +98,7 @@ struct Bf16Params {
     __nv_bfloat16 *O;
     float *lse;
     int B, H, N;                     // N: queries per sequence (dense) / longest sequence
+    int H_row;                       // heads per token row of Q/K/V/O and per (b) in lse
     int Nk;                          // keys per sequence (dense); packed batches use L
     int n_pairs;                     // Q-tile pairs per (sequence, head) at length N
     int64_t total;                   // query rows of Q / O
@@ -637,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool row_ok = i < L;
                     const bool empty = !(l > 0.f);
                     const float inv = empty ? 0.f : 1.f / l;
-                    __nv_bfloat16 *orow = p.O + ((start + i) * p.H + h) * D;
+                    __nv_bfloat16 *orow = p.O + ((start + i) * p.H_row + h) * D;
                     float *arow = p.O_accum +
                                   (((int64_t(split) * p.B + b) * p.N + i) * p.H + h) * D;
 #pragma unroll
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n_splits > 1)
                             p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = lse;
                         else
-                            p.lse[(int64_t(b) * p.H + h) * p.N + i] = lse;
+                            p.lse[(int64_t(b) * p.H_row + h) * p.N + i] = lse;
                     }
                 }
             } else if (!aborted && n_splits > 1 && i < L) {
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after_sync();
                 const float inv = (FP8 ? p.sv[int64_t(b) * p.H + h] : 1.f) / l;
                 const bool row_ok = i < L;
-                __nv_bfloat16 *orow = p.O + ((start + i) * p.H + h) * D;
+                __nv_bfloat16 *orow = p.O + ((start + i) * p.H_row + h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -736,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (p.cu_seqlens != nullptr)
                         p.lse[int64_t(h) * p.total + start + i] = lse;
                     else
-                        p.lse[(int64_t(b) * p.H + h) * p.N + i] = lse;
+                        p.lse[(int64_t(b) * p.H_row + h) * p.N + i] = lse;
                 }
             }
             if (full_tile) {
@@ -787,11 +788,13 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     Bf16Params p;
     const int Nk = a.Nk > 0 ? a.Nk : a.N;
     const int64_t total_k = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
-    if (!make_tmap_bf16(&p.tm_q, a.Q, a.total, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_k, a.K, total_k, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_v, a.V, total_k, a.H, a.d) ||
-        !make_tmap_bf16(&p.tm_o, a.O, a.total, a.H, a.d))
+    const int H_row = a.H_row > 0 ? a.H_row : a.H;
+    if (!make_tmap_bf16(&p.tm_q, a.Q, a.total, a.H, a.d, 128, H_row) ||
+        !make_tmap_bf16(&p.tm_k, a.K, total_k, a.H, a.d, 128, H_row) ||
+        !make_tmap_bf16(&p.tm_v, a.V, total_k, a.H, a.d, 128, H_row) ||
+        !make_tmap_bf16(&p.tm_o, a.O, a.total, a.H, a.d, 128, H_row))
         return FA_ERR_CUDA;
+    p.H_row = H_row;
     p.Nk = Nk;
     p.kv_off = a.kv_off;
     p.splits = a.splits > 0 ? a.splits : 1;
@@ -839,6 +842,7 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     p.sq = a.sq;
     p.sk = a.sk;
     p.sv = a.sv;
+    p.H_row = a.H;
     p.n_tiles = (a.N + BM - 1) / BM;
     p.Nk = a.N;
     p.kv_off = 0;

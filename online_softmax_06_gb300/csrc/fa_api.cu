@@ -165,6 +165,93 @@ Fp8Layout fp8_layout(int B, int H, int N, int d)
     return L;
 }
 
+// fa_attention_fwd_host: device copies of Q, K, V, O and lse in the caller's
+// workspace, each part 256-byte aligned.
+struct HostLayout {
+    int64_t q, k, v, o, lse, bytes;
+};
+
+HostLayout host_layout(int B, int H, int N, int d)
+{
+    auto up = [](int64_t x) { return (x + 255) & ~int64_t(255); };
+    const int64_t t = int64_t(B) * N * H * d * 2;
+    HostLayout L;
+    L.q = 0;
+    L.k = L.q + up(t);
+    L.v = L.k + up(t);
+    L.o = L.v + up(t);
+    L.lse = L.o + up(t);
+    L.bytes = L.lse + up(int64_t(B) * H * N * 4);
+    return L;
+}
+
+// Streams and events of the host-buffer pipeline, created once per device.
+constexpr int kHostGroups = 24;   // head groups a call is cut into (at most)
+
+// Head-group sizes of the host pipeline: about eight groups of hg = H / 8
+// heads, with groups of 1, 2, 4, ... heads at both ends, so that the first
+// group's copy in (before any work) and the last group's copy out (after all
+// work) are short.  Returns the number of groups (sizes sum to H).
+int plan_head_groups(int H, int *sizes)
+{
+    const int hg = (H + 7) / 8;
+    int n = 0, used = 0, nd = 0, dsum = 0;
+    int down[16];
+    for (int s = 1; s < hg && used + s <= H && n < 8; s *= 2) {
+        sizes[n++] = s;
+        used += s;
+    }
+    for (int s = 1; s < hg && used + dsum + s <= H && nd < 8; s *= 2) {
+        down[nd++] = s;
+        dsum += s;
+    }
+    int mid = H - used - dsum;
+    while (mid > 0 && n < kHostGroups - nd) {
+        const int s = mid < hg ? mid : hg;
+        sizes[n++] = s;
+        mid -= s;
+    }
+    if (mid > 0) {                     // does not fit: equal groups instead
+        n = 0;
+        for (int h0 = 0; h0 < H; h0 += hg)
+            sizes[n++] = H - h0 < hg ? H - h0 : hg;
+        return n;
+    }
+    for (int i = nd - 1; i >= 0; --i)
+        sizes[n++] = down[i];
+    return n;
+}
+struct HostPipe {
+    std::once_flag once;
+    int ok = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kHostGroups] = {}, comp[kHostGroups] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+HostPipe *host_pipe()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    HostPipe *pp = &g_pipe[dev];
+    std::call_once(pp->once, [pp] {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&pp->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&pp->s_out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&pp->start, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&pp->done, ef) != cudaSuccess)
+            return;
+        for (int g = 0; g < kHostGroups; ++g)
+            if (cudaEventCreateWithFlags(&pp->in[g], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&pp->comp[g], ef) != cudaSuccess)
+                return;
+        pp->ok = 1;
+    });
+    return pp->ok ? pp : nullptr;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -378,6 +465,94 @@ int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, f
     a.causal = causal ? 1 : 0;
     a.err_word = dev->err_word;
     return fa::launch_attention_fp8(a, fa::t_stream);
+}
+
+int64_t fa_attention_host_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return fa::host_layout(B, H, N, d).bytes;
+}
+
+int fa_attention_fwd_host(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                          int H, int N, int d, float scale, int causal, void *workspace,
+                          int64_t workspace_bytes)
+{
+    if (B < 0 || H < 0 || N < 0 || workspace_bytes < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || N == 0)
+        return FA_OK;
+    if (!Q || !K || !V || !O || !lse || !workspace)
+        return FA_ERR_NULL_POINTER;
+    if (!fa::aligned(workspace, 256))
+        return FA_ERR_MISALIGNED;
+    const int64_t total = int64_t(B) * N;
+    if (total > (int64_t(1) << 31) - 512 || total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+        return FA_ERR_TOO_LARGE;
+    const fa::HostLayout L = fa::host_layout(B, H, N, d);
+    if (workspace_bytes < L.bytes)
+        return FA_ERR_BAD_SIZE;
+    fa::DeviceInfo *dev = fa::current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    fa::HostPipe *pp = fa::host_pipe();
+    if (pp == nullptr)
+        return FA_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *dq = ws + L.q, *dk = ws + L.k, *dv = ws + L.v, *dout = ws + L.o;
+    float *dl = reinterpret_cast<float *>(ws + L.lse);
+    const uint8_t *hq = static_cast<const uint8_t *>(Q), *hk = static_cast<const uint8_t *>(K),
+                  *hv = static_cast<const uint8_t *>(V);
+    uint8_t *ho = static_cast<uint8_t *>(O);
+    // head groups; a group's slice of a token row is hn * d * 2 contiguous
+    // bytes of the row's H * d * 2
+    int sizes[fa::kHostGroups];
+    const int n_groups = fa::plan_head_groups(H, sizes);
+    const size_t row = size_t(H) * d * 2, lse_row = size_t(H) * N * 4;
+    const cudaStream_t s_main = fa::t_stream;
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    if (!ok(cudaEventRecord(pp->start, s_main)) || !ok(cudaStreamWaitEvent(pp->s_in, pp->start, 0)) ||
+        !ok(cudaStreamWaitEvent(pp->s_out, pp->start, 0)))
+        return FA_ERR_CUDA;
+    for (int g = 0, h0 = 0; g < n_groups; h0 += sizes[g], ++g) {
+        const int hn = sizes[g];
+        const size_t off = size_t(h0) * d * 2, width = size_t(hn) * d * 2;
+        if (!ok(cudaMemcpy2DAsync(dq + off, row, hq + off, row, width, size_t(total),
+                                  cudaMemcpyHostToDevice, pp->s_in)) ||
+            !ok(cudaMemcpy2DAsync(dk + off, row, hk + off, row, width, size_t(total),
+                                  cudaMemcpyHostToDevice, pp->s_in)) ||
+            !ok(cudaMemcpy2DAsync(dv + off, row, hv + off, row, width, size_t(total),
+                                  cudaMemcpyHostToDevice, pp->s_in)) ||
+            !ok(cudaEventRecord(pp->in[g], pp->s_in)) ||
+            !ok(cudaStreamWaitEvent(s_main, pp->in[g], 0)))
+            return FA_ERR_CUDA;
+        fa::AttnArgs a;
+        int rc = fa::check_attention(dq + off, dk + off, dv + off, dout + off, dl + size_t(h0) * N,
+                                     B, hn, N, d, causal, nullptr, total, true, &a);
+        if (rc != FA_OK)
+            return rc;
+        a.H_row = H;
+        a.scale = scale;
+        a.err_word = dev->err_word;
+        rc = fa::launch_attention_bf16(a, s_main);
+        if (rc != FA_OK)
+            return rc;
+        if (!ok(cudaEventRecord(pp->comp[g], s_main)) ||
+            !ok(cudaStreamWaitEvent(pp->s_out, pp->comp[g], 0)) ||
+            !ok(cudaMemcpy2DAsync(ho + off, row, dout + off, row, width, size_t(total),
+                                  cudaMemcpyDeviceToHost, pp->s_out)) ||
+            !ok(cudaMemcpy2DAsync(lse + size_t(h0) * N, lse_row, dl + size_t(h0) * N, lse_row,
+                                  size_t(hn) * N * 4, size_t(B), cudaMemcpyDeviceToHost,
+                                  pp->s_out)))
+            return FA_ERR_CUDA;
+    }
+    if (!ok(cudaEventRecord(pp->done, pp->s_out)) || !ok(cudaStreamWaitEvent(s_main, pp->done, 0)))
+        return FA_ERR_CUDA;
+    return FA_OK;
 }
 
 int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *O, float *lse,

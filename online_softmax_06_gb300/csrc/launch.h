@@ -17,6 +17,9 @@ struct AttnArgs {
     void *O;
     float *lse;
     int B, H, N, d;
+    int H_row = 0;            // heads per token row in memory (0: H); > H for a
+                              // view of heads [h0, h0 + H): Q/K/V/O point at head
+                              // h0 of row 0, lse at head h0's first entry
     int64_t total;            // packed token count (B * N when dense)
     float scale;
     int causal;
@@ -43,9 +46,11 @@ int choose_num_splits(int B, int H, int N, int Nk);
 
 // 3-D TMA map over a [total, H, d] bf16 tensor: box = 64 head-dim elements
 // (128 bytes, the 128-byte swizzle span) x 1 head x box_rows rows (128 unless
-// given); rows past `total` read as zero.  False if the driver refuses the map.
+// given); rows past `total` read as zero.  With H_row > 0 the map covers H
+// heads of rows that hold H_row heads (a head-range view; base points at its
+// first head).  False if the driver refuses the map.
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d,
-                    int box_rows = 128);
+                    int box_rows = 128, int H_row = 0);
 
 // TMA maps over the FP8 forward's e4m3 tensors: rows of Q' / K' ([total, H, d]
 // bytes, box d x 1 x 128, d = 128 so a row is one 128-byte swizzle span) and

@@ -36,13 +36,16 @@ EncodeTiledFn encode_fn()
 
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d, int box_rows)
+bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int d, int box_rows,
+                    int H_row)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
         return false;
+    if (H_row <= 0)
+        H_row = H;
     const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(total)};
-    const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(H) * d * 2};
+    const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(H_row) * d * 2};
     const cuuint32_t box[3] = {64, 1, cuuint32_t(box_rows)};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,

@@ -75,6 +75,19 @@ def test_host_validation_without_gpu(lib):
                                0, 1, 8, 64, 1.0, 0) == 0
     assert fa.fa_attention_bwd(None, None, None, None, None, None, None, None, None, None,
                                1, 1, 8, 64, 1.0, 0) == -1
+    hw = fa.fa_attention_host_workspace_bytes
+    assert hw(-1, 1, 1, 64) == -2
+    assert hw(1, 1, 1, 96) == -3
+    # four bf16 [2, 5, 3, 64] tensors (3840 bytes each) and lse [2, 3, 5] fp32,
+    # every part rounded up to 256 bytes
+    assert hw(2, 3, 5, 64) == 4 * 3840 + 256
+    fh = fa.fa_attention_fwd_host
+    assert fh(None, None, None, None, None, -1, 1, 1, 64, 1.0, 0, None, 0) == -2
+    assert fh(None, None, None, None, None, 1, 1, 1, 96, 1.0, 0, None, 0) == -3
+    assert fh(None, None, None, None, None, 0, 1, 1, 64, 1.0, 0, None, 0) == 0
+    assert fh(None, None, None, None, None, 1, 1, 1, 64, 1.0, 0, None, 0) == -1
+    assert fh(16, 16, 16, 16, 16, 1, 1, 1, 64, 1.0, 0, 8, 1 << 20) == -4      # workspace alignment
+    assert fh(16, 16, 16, 16, 16, 1, 1, 1, 64, 1.0, 0, 256, 1) == -2          # workspace size
     nl = fa.fa_attention_fwd_splitkv_noalloc
     assert nl(None, None, None, None, None, 1, 1, -1, 8, 64, 1.0, 0, 0) == -2
     assert nl(None, None, None, None, None, 1, 1, 9, 8, 64, 1.0, 1, 0) == -2   # causal Nk < Nq
