@@ -199,18 +199,24 @@ __global__ void __launch_bounds__(256) fp8_vt_kernel(const VtParams p)
     if (tile == 0 && threadIdx.x == 0)
         p.sv[bh] = scale;
     const float inv = 1.f / scale;
-    // load: thread -> (key r, head-dim pair c, c + 1)
-    for (int e = threadIdx.x; e < kRows * D / 2; e += blockDim.x) {
+    // load: thread -> (key r, head-dim pair c, c + 1); every load of the
+    // thread is issued before the first conversion
+    constexpr int kPairs = kRows * D / 2 / 256;       // per thread (256 threads)
+    __nv_bfloat162 raw[kPairs];
+#pragma unroll
+    for (int u = 0; u < kPairs; ++u) {
+        const int e = u * 256 + int(threadIdx.x);
         const int r = e / (D / 2), c = (e % (D / 2)) * 2;
         const int row = tile * kRows + r;
-        float v0 = 0.f, v1 = 0.f;
-        if (row < p.N) {
-            const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162 *>(
-                p.V + ((int64_t(b) * p.N + row) * p.H + h) * D + c);
-            v0 = __bfloat162float(v2.x);
-            v1 = __bfloat162float(v2.y);
-        }
-        const uint32_t w = e4m3x2(v0 * inv, v1 * inv);
+        raw[u] = row < p.N ? *reinterpret_cast<const __nv_bfloat162 *>(
+                                 p.V + ((int64_t(b) * p.N + row) * p.H + h) * D + c)
+                           : __floats2bfloat162_rn(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kPairs; ++u) {
+        const int e = u * 256 + int(threadIdx.x);
+        const int r = e / (D / 2), c = (e % (D / 2)) * 2;
+        const uint32_t w = e4m3x2(__low2float(raw[u]) * inv, __high2float(raw[u]) * inv);
         tileT[c * kPitch + r] = uint8_t(w & 0xffu);
         tileT[(c + 1) * kPitch + r] = uint8_t(w >> 8);
     }
