@@ -107,6 +107,39 @@ def test_fp8_matches_reference(dev, B, H, N, causal):
     device_error_clear()
 
 
+def test_fp8_full_size_sampled(dev):
+    """The benchmark's FP8 launch (causal B=2 H=32 N=4096 d=128): every tile
+    scale of Q M and K M against the reference's, and O and lse on sampled
+    (token, head) rows against the reference attention on the dequantised
+    inputs (the reference row by row: the oracle's per-row attention)."""
+    import workloads
+    B, H, N, d = 2, 32, 4096, 128
+    qkv, signs = make(B, H, N, d, seed=4096)
+    O, lse, ws = run(qkv, signs, True, dev)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(lse))
+    Q, K, V = (t.float().numpy() for t in qkv)
+    L = layout(B, H, N, d)
+    for name, X, soff in (("Q", Q, L["sq"]), ("K", K, L["sk"])):
+        _, ref_scales = fp8.blockwise_qk(fp8.rotate(X, signs))
+        got = ws[soff:soff + B * H * L["T"] * 4].view(np.float32).reshape(B, H, L["T"])
+        assert np.allclose(got, ref_scales, rtol=1e-5), name
+    Qd, Kd, Vd = (x.reshape(B * N, H, d).astype(np.float32) for x in fp8.fp8_inputs(Q, K, V, signs))
+    must = list(range(0, 130)) + list(range(N - 130, N + 130)) + list(range(B * N - 130, B * N))
+    tok, head = workloads.sample_rows(B * N, H, 2000, seed=4097)
+    tok = np.concatenate([tok, np.asarray(must, np.int64)])
+    head = np.concatenate([head, np.asarray(must, np.int64) % H])
+    cu = np.arange(B + 1, dtype=np.int32) * N
+    Or, lr = oracle.attention_rows(Qd, Kd, Vd, cu, 1 / math.sqrt(d), True, tok, head)
+    Op = O.reshape(B * N, H, d)[tok, head]
+    lp = lse.transpose(1, 0, 2).reshape(H, B * N)[head, tok]
+    rmse = float(np.sqrt(np.mean((Op - Or) ** 2)))
+    mx = float(np.abs(Op - Or).max())
+    print(f"full size: rmse {rmse:.2e} max {mx:.2e} lse {np.abs(lp - lr).max():.2e}")
+    assert rmse <= FP8_O_RMSE and mx <= 2.0 ** -4 * float(np.abs(V).max())
+    assert float(np.abs(lp - lr).max()) <= FP8_LSE_MAX
+    device_error_clear()
+
+
 def test_fp8_outliers_pages_experiment(dev):
     """The pages' outlier test ([FG] §4.6): RMSE against exact attention,
     below per-tensor FP8 (emulated on the CPU from its definition)."""
