@@ -54,6 +54,18 @@ def test_host_matches_device(dev, B, N, H, d, causal, pinned):
     device_error_clear()
 
 
+def test_host_full_size_matches_device(dev):
+    """The benchmark's e2e call (causal B=2 H=32 N=4096 d=128, pinned buffers)."""
+    w = workloads.WORKLOADS["attn_bf16_causal_b2h32n4096d128"]
+    Q, K, V = (t.contiguous().pin_memory() for t in w.inputs())
+    O_h, lse_h, _ = fa.attention_fwd_host(Q, K, V, causal=True, device=dev)
+    O_d, lse_d = fa.attention_fwd(Q.to(dev), K.to(dev), V.to(dev), causal=True)
+    torch.cuda.synchronize(dev)
+    assert torch.equal(O_h.view(torch.int16), O_d.cpu().view(torch.int16))
+    assert torch.equal(lse_h, lse_d.cpu())
+    device_error_clear()
+
+
 def test_host_against_oracle(dev):
     B, N, H, d = 2, 257, 5, 128
     Q, K, V = host_inputs((B, N, H, d), seed=77, pinned=True)
