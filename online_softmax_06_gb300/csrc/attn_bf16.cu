@@ -769,13 +769,8 @@ template <int D, bool SPLIT>
 int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 {
     auto kern = attn_fwd_bf16_kernel<D, SPLIT>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        int(Cfg<D>::kSmemBytes));
-    });
-    if (attr_err != cudaSuccess)
+    static PerDeviceOnce once;
+    if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern), int(Cfg<D>::kSmemBytes)))
         return FA_ERR_CUDA;
     kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -866,13 +861,9 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
     auto kern = attn_fwd_bf16_kernel<128, false, true>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        int(Cfg<128, true>::kSmemBytes));
-    });
-    if (attr_err != cudaSuccess)
+    static PerDeviceOnce once;
+    if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern),
+                              int(Cfg<128, true>::kSmemBytes)))
         return FA_ERR_CUDA;
     kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<128, true>::kSmemBytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;

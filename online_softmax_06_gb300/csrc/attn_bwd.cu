@@ -818,18 +818,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t stream)
 {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        int(Cfg<D>::kSmemBytes));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            int(Cfg<D>::kSmemBytes));
-    });
-    if (attr_err != cudaSuccess)
+    static PerDeviceOnce once_dq, once_dkdv;
+    if (!set_max_dynamic_smem(once_dq, reinterpret_cast<const void *>(attn_bwd_dq_kernel<D>),
+                              int(Cfg<D>::kSmemBytes)) ||
+        !set_max_dynamic_smem(once_dkdv, reinterpret_cast<const void *>(attn_bwd_dkdv_kernel<D>),
+                              int(Cfg<D>::kSmemBytes)))
         return FA_ERR_CUDA;
     const int64_t blocks = int64_t(p_dq.n_tiles) * p_dq.B * p_dq.H;
     attn_bwd_dq_kernel<D>

@@ -5,8 +5,30 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 namespace fa {
+
+// A kernel's dynamic shared-memory limit is raised once per device (the
+// attribute belongs to the current device's context): one PerDeviceOnce per
+// kernel and call site.
+struct PerDeviceOnce {
+    static constexpr int kDevices = 64;
+    std::once_flag flag[kDevices];
+    cudaError_t err[kDevices] = {};
+};
+
+inline bool set_max_dynamic_smem(PerDeviceOnce &o, const void *kernel, int bytes)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= PerDeviceOnce::kDevices)
+        return false;
+    std::call_once(o.flag[dev], [&] {
+        o.err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          bytes);
+    });
+    return o.err[dev] == cudaSuccess;
+}
 
 // Row softmax of x [rows, N] into y (y may equal x).
 int launch_softmax_rows(const float *x, float *y, int64_t rows, int64_t N, cudaStream_t stream);
