@@ -444,6 +444,7 @@ int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, f
     q.H = H;
     q.N = N;
     q.d = d;
+    q.err_word = dev->err_word;
     int rc = fa::launch_fp8_quantize(q, fa::t_stream);
     if (rc != FA_OK)
         return rc;

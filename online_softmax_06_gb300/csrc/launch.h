@@ -79,6 +79,10 @@ bool make_tmap_bf16(CUtensorMap *tm, const void *base, int64_t total, int H, int
 // the transposed V' ([rows = B*H*d, n_pad] bytes, box 128 keys x d rows).
 bool make_tmap_e4m3_rows(CUtensorMap *tm, const void *base, int64_t total, int H, int d);
 bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t n_pad, int d);
+// 4-D TMA map over a dense [B, N, H, d] tensor (bf16, or e4m3 bytes): box = one
+// 128-byte row segment (64 bf16 or 128 e4m3) x 1 head x 128 rows x 1 sequence,
+// 128-byte swizzle.  Rows past N of a sequence read as zero and are not stored.
+bool make_tmap_seq_4d(CUtensorMap *tm, const void *base, bool e4m3, int B, int N, int H, int d);
 
 // FP8 attention forward on the quantised tensors (dense; d = 128).
 struct AttnFp8Args {
@@ -115,6 +119,7 @@ struct Fp8QuantArgs {
     float *sq, *sk, *vamax;    // [B, H, n_tiles]
     float *sv;                 // [B, H]
     int B, H, N, d;
+    int *err_word;             // device error word (bounded waits)
 };
 int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream);
 

@@ -152,6 +152,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *t
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *tmap,
+                                            uint64_t *bar, int x, int y, int z, int w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Brings a tensor-map box into L2 ahead of its TMA load (no completion).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *tmap, int x, int y, int z)
 {
@@ -195,6 +206,24 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *tmap, const void
         "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(tmap)),
         "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tmap, const void *smem_src, int x,
+                                             int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *tmap, const void *smem_src, int x,
+                                             int y, int z, int w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
 __device__ __forceinline__ void bulk_commit_and_wait_read()
@@ -441,7 +470,6 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Packs two floats into bf16x2, round-to-nearest-even; `lo` lands in bits 0..15.
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
@@ -450,6 +478,7 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return r;
 }
 
+// Packs two floats into bf16x2, round-to-nearest-even; `lo` lands in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;

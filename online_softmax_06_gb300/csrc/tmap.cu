@@ -69,6 +69,23 @@ bool make_tmap_e4m3_rows(CUtensorMap *tm, const void *base, int64_t total, int H
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_seq_4d(CUtensorMap *tm, const void *base, bool e4m3, int B, int N, int H, int d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint64_t eb = e4m3 ? 1 : 2;
+    const cuuint64_t dims[4] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(N), cuuint64_t(B)};
+    const cuuint64_t strides[3] = {cuuint64_t(d) * eb, cuuint64_t(H) * d * eb,
+                                   cuuint64_t(N) * H * d * eb};
+    const cuuint32_t box[4] = {cuuint32_t(128 / eb), 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(tm, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t n_pad, int d)
 {
     EncodeTiledFn fn = encode_fn();
