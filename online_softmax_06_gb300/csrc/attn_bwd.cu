@@ -90,15 +90,15 @@ struct Cfg {
     static constexpr uint32_t kOffStat = kOffRing + kStages * kStageBytes;
     static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;
     static constexpr uint32_t kOffBar = kOffStat + kStatBytes;
-    // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full, drain
-    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 6);
+    // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full, drain, a_tm
+    static constexpr uint32_t kBarBytes = 8 * (1 + 2 * kStages + 7);
     static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 // TMEM columns: buffer b holds S (or S^T) in [128 b, 128 b + 64) and dP (or
-// dP^T) in [128 b + 64, 128 b + 128); accumulators from 256 (dQ; or dV then
-// dK).  bf16 P / dS are packed into the region they are formed from: the 32
+// dP^T) in [128 b + 64, 128 b + 128); accumulators from 256 (dQ, then Q and
+// dO as bf16 A operands; or dV then dK).  bf16 P / dS are packed into the region they are formed from: the 32
 // values of each 32-column block go to the block's first 16 columns (two per
 // column), so a thread only overwrites columns it has read.
 constexpr uint32_t kColBuf = 128, kColDP = 64, kColAcc = 256;
@@ -125,6 +125,7 @@ struct BwdParams {
 
 struct Bars {
     uint64_t *a_full, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *drain;
+    uint64_t *a_tm;                          // dQ kernel: Q and dO copied into TMEM
 };
 
 template <int D>
@@ -140,6 +141,7 @@ __device__ __forceinline__ Bars carve(uint8_t *smem)
     r.p_full = r.s_full + 2;                  // [2]
     r.o_full = r.s_full + 4;
     r.drain = r.s_full + 5;
+    r.a_tm = r.s_full + 6;
     return r;
 }
 
@@ -192,6 +194,7 @@ __device__ __forceinline__ uint32_t setup(const BwdParams &p, const Bars &bar,
         }
         ptx::mbar_init(bar.o_full, 1);
         ptx::mbar_init(bar.drain, 1);
+        ptx::mbar_init(bar.a_tm, kRowWarps);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -266,6 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
     using C = Cfg<D>;
+    // Q and dO as bf16 pairs in TMEM after the dQ accumulator (D / 2 columns
+    // each): the A operands of S = Q K^T and dP = dO V^T
+    constexpr uint32_t kColQA = kColAcc + D;
+    static_assert(kColQA + D <= kTmemCols, "tensor memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -343,8 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
         constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
         constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kSubChunkBytes, 1024);
-        const uint64_t dq = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_q));
-        const uint64_t ddo = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_do));
         const uint32_t ring_addr = ptx::smem_u32(ring);
         int stage = 0;
         uint32_t phase = 0;
@@ -364,13 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = ptx::smem_desc(desc_kmajor, kaddr + C::kSubBytes);
             const uint32_t buf = tmem + uint32_t(j & 1) * kColBuf;
             if (ptx::elect_one()) {
+                // A = Q, dO from TMEM (K step kk: 8 columns of bf16 pairs)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(buf, dq + kmajor_off(kk, kResChunkBytes),
-                                dk + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
+                    ptx::mma_ts(buf, tmem + kColQA + 8 * kk, dk + kmajor_off(kk, kSubChunkBytes),
+                                idesc_ss, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(buf + kColDP, ddo + kmajor_off(kk, kResChunkBytes),
+                    ptx::mma_ts(buf + kColDP, tmem + kColQA + D / 2 + 8 * kk,
                                 dv + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
                 ptx::mma_commit(&bar.s_full[j & 1]);
             }
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         do {
-            if (!ptx::mbar_wait_warp(bar.a_full, 0, abort_flag, p.err_word) || !issue_s(0)) {
+            if (!ptx::mbar_wait_warp(bar.a_tm, 0, abort_flag, p.err_word) || !issue_s(0)) {
                 aborted = true;
                 break;
             }
@@ -445,6 +451,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : make_uint4(0, 0, 0, 0);
             }
             const bool a_ok = row_wait(bar.a_full, 0, abort_flag, p.err_word);
+            if (a_ok) {
+                // this thread's half of row r of Q and of dO into TMEM, as the
+                // bf16 pairs of the S and dP products' A operands (shared-memory
+                // unit u of row r sits at unit u ^ (r % 8) of its 128 bytes)
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const uint8_t *tile = t == 0 ? tile_q : tile_do;
+                    uint32_t w[D / 4];
+#pragma unroll
+                    for (int ul = 0; ul < D / 16; ++ul) {
+                        const int e0 = g * (D / 2) + ul * 8;          // first element
+                        const int u = (e0 & 63) >> 3;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(
+                            tile + (e0 >> 6) * kResChunkBytes + r * 128 + ((u ^ (r & 7)) << 4));
+                        w[4 * ul + 0] = v.x;
+                        w[4 * ul + 1] = v.y;
+                        w[4 * ul + 2] = v.z;
+                        w[4 * ul + 3] = v.w;
+                    }
+                    const uint32_t dst = tmem + lane_bits + kColQA + uint32_t(t * (D / 2) + g * (D / 4));
+                    if constexpr (D == 128)
+                        ptx::tmem_st32(dst, w);
+                    else
+                        ptx::tmem_st16(dst, w);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar.a_tm);
+            }
 #pragma unroll
             for (int k = 0; k < kRowsPerWarp / kRowsPerInst; ++k) {
                 const int rr = warp * kRowsPerWarp + k * kRowsPerInst + sub;

@@ -58,14 +58,19 @@ def layout(B, H, N, d):
     vt = up(kf + elems)
     sq = up(vt + B * H * d * 128 * T)
     sk = up(sq + B * H * T * 4)
-    return dict(qf=qf, kf=kf, vt=vt, sq=sq, sk=sk, T=T)
+    vamax = up(sk + B * H * T * 4)
+    sv = up(vamax + B * H * T * 4)
+    return dict(qf=qf, kf=kf, vt=vt, sq=sq, sk=sk, vamax=vamax, sv=sv, T=T)
 
 
 def e4m3_decode(codes):
     return torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
-@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 256, False), (2, 1, 300, True)])
+# the last case has 960 work items (Q, K, V tiles), several per CTA of the
+# persistent quantisation kernel, and a ragged last tile per sequence
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 256, False), (2, 1, 300, True),
+                                          (2, 16, 1200, True)])
 def test_fp8_quantisation_matches_reference(dev, B, H, N, causal):
     d = 128
     (Q, K, V), signs = make(B, H, N, d, seed=N + B)
@@ -86,6 +91,22 @@ def test_fp8_quantisation_matches_reference(dev, B, H, N, causal):
         assert diff.mean() < 1e-3, name
         rel = np.abs(got - ref)[diff] / np.maximum(np.abs(ref)[diff], 2.0 ** -9)
         assert np.all(rel <= 2.0 ** -3 + 1e-9), name
+    # V': one scale per (sequence, head), codes transposed to [B, H, d, n_pad],
+    # zero codes past N
+    Vn = V.float().numpy().astype(np.float64)
+    _, ref_sv = fp8.per_head_v(Vn)
+    got_sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H)
+    assert np.allclose(got_sv, ref_sv, rtol=1e-6)
+    n_pad = 128 * L["T"]
+    codes = ws[L["vt"]:L["vt"] + B * H * d * n_pad].reshape(B, H, d, n_pad)
+    assert not np.any(codes[..., N:]), "padding keys must hold zero codes"
+    got = e4m3_decode(np.ascontiguousarray(codes[..., :N]))
+    ref = fp8.e4m3_round(Vn.transpose(0, 2, 3, 1) / got_sv[:, :, None, None].astype(np.float64))
+    diff = got != ref
+    print(f"V: {diff.mean():.2e} of codes differ")
+    assert diff.mean() < 1e-3
+    rel = np.abs(got - ref)[diff] / np.maximum(np.abs(ref)[diff], 2.0 ** -9)
+    assert np.all(rel <= 2.0 ** -3 + 1e-9)
 
 
 @pytest.mark.parametrize("B,H,N,causal", [(1, 2, 256, False), (2, 2, 512, True), (1, 3, 300, True),
