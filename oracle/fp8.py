@@ -49,10 +49,23 @@ def rotate(X, signs) -> np.ndarray:
 
 
 def e4m3_round(x) -> np.ndarray:
-    """Round float64 values to e4m3 (nearest even, saturating at +-448)."""
-    import torch
-    t = torch.from_numpy(np.clip(np.asarray(x, dtype=np.float64), -E4M3_MAX, E4M3_MAX))
-    return t.to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    """Round float64 values to e4m3 (nearest, ties to even, saturating at
+    +-448) in one step from the float64 value.
+
+    e4m3 has 3 fraction bits: in the binade [2^e, 2^(e+1)) the spacing is
+    2^(e-3), and below the smallest normal 2^-6 the subnormal spacing is 2^-9;
+    so a value is rounded to an integer multiple of its spacing (an exact
+    power-of-two scaling in float64; numpy rounds halves to even).  Going
+    through float32 first would round twice: a value just above a half-way
+    point can become the half-way point and then go to the even neighbour.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(a)                       # a = m 2^ex, m in [0.5, 1): binade ex - 1
+    e = np.maximum(ex - 1, -6)
+    ulp = np.ldexp(1.0, e - 3)
+    q = np.minimum(np.round(a / ulp) * ulp, E4M3_MAX)
+    return np.copysign(q, x)
 
 
 def _scale_of(amax):
@@ -84,6 +97,21 @@ def per_head_v(V):
     sc = _scale_of(np.abs(V).max(axis=(1, 3)))
     s4 = sc[:, None, :, None]
     return e4m3_round(V / s4) * s4, sc
+
+
+def per_head_v_fp32(V):
+    """V's e4m3 codes with the rounding decision taken in float32, as the GPU
+    takes it (the pages fix no precision): sv = amax / 448 and 1 / sv rounded
+    to float32, x = v * (1 / sv) rounded to float32, then one rounding to e4m3.
+    A code is an integer decided by floating point, so both sides decide it in
+    the same precision.  Returns (codes as float64 values [B, N, H, d],
+    sv [B, H] float32)."""
+    V32 = np.asarray(V, dtype=np.float32)
+    amax = np.abs(V32).max(axis=(1, 3))
+    sv = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(1.0) / sv).astype(np.float32)
+    x = (V32 * inv[:, None, :, None]).astype(np.float32)
+    return e4m3_round(x.astype(np.float64)), sv
 
 
 def per_tensor(X):

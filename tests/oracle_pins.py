@@ -538,18 +538,23 @@ def _e4m3_table():
 
 
 def pin_fp8_e4m3_brute_force(lib):
-    """torch's e4m3 rounding (the reference's quantiser) against a brute-force
-    nearest-value search over the format's code table, ties to the even code,
-    saturating at +-448."""
+    """The reference's e4m3 rounding against a brute-force nearest-value
+    search over the format's code table, ties to the even code, saturating at
+    +-448."""
     from oracle import fp8
     vals, codes = _e4m3_table()
     rng = np.random.default_rng(40)
     x = np.concatenate([rng.uniform(-500, 500, 4000), rng.uniform(-0.05, 0.05, 4000),
                         vals, (vals[:-1] + vals[1:]) / 2 if False else [],
                         [3.14159, 460.0, -460.0, 2.0 ** -10, 2.0 ** -9, 0.0]])
-    # midpoints between neighbouring positive values exercise ties-to-even
+    # midpoints between neighbouring positive values exercise ties-to-even;
+    # values a hair (2^-30 relative, far below float32's resolution) off a
+    # midpoint must go to the nearer neighbour: rounding through float32
+    # first would make them ties
     pos = np.unique(np.abs(vals))
-    x = np.concatenate([x, (pos[:-1] + pos[1:]) / 2, -(pos[:-1] + pos[1:]) / 2])
+    mid = (pos[:-1] + pos[1:]) / 2
+    x = np.concatenate([x, mid, -mid, mid * (1 + 2.0 ** -30), mid * (1 - 2.0 ** -30),
+                        -mid * (1 + 2.0 ** -30), [84.0000035, 83.9999965]])
     got = fp8.e4m3_round(x)
     xc = np.clip(x, -448.0, 448.0)
     d = np.abs(xc[:, None] - vals[None, :])
@@ -563,6 +568,36 @@ def pin_fp8_e4m3_brute_force(lib):
     expect = np.where(expect == 0, 0.0, expect)
     assert np.array_equal(np.abs(got), np.abs(expect)) and np.all(
         (got == 0) | (np.sign(got) == np.sign(xc))), "e4m3 rounding differs from the table"
+
+
+def pin_fp8_v_codes_fp32(lib):
+    """V's float32-decided codes: (1) when amax = 1.75 * 2^k the scale
+    2^(k-8) and its reciprocal are exact, so the codes are the e4m3 rounding of
+    the exact V / sv; (2) in general they equal the float64 method's codes
+    except within float32 rounding of a half-way point, where they are the
+    neighbouring code; (3) the scale is amax / 448."""
+    from oracle import fp8
+    rng = np.random.default_rng(44)
+    target = 1.75 * 2.0 ** np.arange(-3, 3).reshape(2, 3)              # amax per (b, h)
+    V = (rng.uniform(-0.99, 0.99, (2, 300, 3, 128)) * target[:, None, :, None]).astype(np.float32)
+    V[:, 7, :, 5] = -target
+    amax = np.abs(V).max(axis=(1, 3)).astype(np.float64)
+    m, _ = np.frexp(amax)
+    assert np.all(m == 0.875), "amax must be 1.75 * 2^k for this case"
+    codes, sv = fp8.per_head_v_fp32(V)
+    assert np.array_equal(sv.astype(np.float64), amax / 448.0)
+    exact = fp8.e4m3_round(V.astype(np.float64) / (amax / 448.0)[:, None, :, None])
+    assert np.array_equal(codes, exact)
+    W = rng.standard_normal((2, 500, 4, 128)).astype(np.float32) * 3
+    c32, sv32 = fp8.per_head_v_fp32(W)
+    _, sv64 = fp8.per_head_v(W.astype(np.float64))        # the float64 method's scales
+    assert np.allclose(sv32, sv64, rtol=1e-7)
+    c64 = fp8.e4m3_round(W.astype(np.float64) / sv64[:, None, :, None])
+    diff = c32 != c64
+    assert diff.mean() < 1e-2
+    step = np.abs(c32 - c64)[diff]
+    spacing = np.ldexp(1.0, np.maximum(np.frexp(np.maximum(np.abs(c32), np.abs(c64)))[1] - 1, -6) - 3)
+    assert np.all(step <= spacing[diff] * (1 + 1e-12)), "only neighbouring codes may differ"
 
 
 def pin_fp8_hadamard_vs_scipy(lib):
