@@ -13,32 +13,33 @@
 // cost of recomputing S and dP there.
 //
 // Two kernels, launched in this order on one stream; each keeps one 128-row
-// tile resident in shared memory and streams the other operand in 64-row
-// sub-tiles:
-//   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile), Q and
-//     dO resident.  The row warps first form D_i = dO_i . O_i together (O
-//     rows from global memory, dO from the resident tile; stored for the
-//     second kernel).  Each query row is then served by two threads (32
-//     columns of a sub-tile each): for every visible 64-key sub-tile j they
-//     turn S = Q K_j^T and
-//     dP = dO V_j^T (tcgen05, fp32 in TMEM) into dS = P o (dP - D_i) in bf16 in
-//     TMEM, and the MMA warp accumulates dQ += dS K_j in TMEM.
+// tile resident and streams the other operand:
+//   * attn_bwd_dq_kernel: one CTA per (sequence, head, 128-query tile).  The
+//     row warps first copy Q and dO from their resident shared-memory tiles
+//     into TMEM (the A operands of S = Q K_j^T and dP = dO V_j^T) and form
+//     D_i = dO_i . O_i together (O rows from global memory; stored for the
+//     second kernel).  Keys stream in 128-row steps through a 3-stage ring
+//     (the third stage reuses the Q / dO region once the prologue is done);
+//     S and dP are single-buffered in TMEM and the MMA warp issues S_{j+1} as
+//     soon as the rows have read S_j, dQ += dS_j K_j once they have stored
+//     dS_j (bf16, in TMEM), then dP_{j+1}.  Each query row is served by two
+//     threads (64 columns of a step each).
 //   * attn_bwd_dkdv_kernel: one CTA per (sequence, head, 128-key tile), K and
-//     V resident.  For every 64-query sub-tile i that sees the keys,
-//     S^T = K Q_i^T and dP^T = V dO_i^T land in TMEM with one key per TMEM
-//     lane; the two threads of each key row form P^T and dS^T (bf16, in TMEM)
-//     from the sub-tile's logsumexp and D (staged in shared memory by the load
-//     warp), and the MMA warp accumulates dV += P^T dO_i and dK += dS^T Q_i.
-// S and dP of a step live in one of two TMEM buffers (columns [0, 128) and
-// [128, 256)), so the MMA warp computes step s + 1's S and dP while the row
-// threads turn step s's into P / dS; the accumulators take columns [256, 512).
-// The elementwise work needs no reduction along a row, so a sub-tile row's 64
-// columns are split between two threads: warps 0-7 serve the rows (warp w:
-// TMEM lanes 32 (w % 4) .. + 31, columns 32 (w / 4) .. + 31 of the buffer).
-// Warp 8 issues TMA loads: one ring stage holds a step's pair of sub-tiles
-// behind one barrier, and each pair is prefetched into L2 a few steps before
-// its load.  Warp 9 owns the tensor memory and issues every tcgen05.mma: the
-// whole warp runs the issuing loop converged and one elected lane issues.
+//     V resident, queries streamed in 64-row sub-tiles.  For every sub-tile i
+//     that sees the keys, S^T = K Q_i^T and dP^T = V dO_i^T land in TMEM with
+//     one key per TMEM lane; the two threads of each key row form P^T and
+//     dS^T (bf16, in TMEM) from the sub-tile's logsumexp and D (staged in
+//     shared memory by the load warp), and the MMA warp accumulates
+//     dV += P^T dO_i and dK += dS^T Q_i.  S^T and dP^T of a step live in one
+//     of two TMEM buffers (columns [0, 128) and [128, 256)), so the MMA warp
+//     computes step s + 1's while the row threads turn step s's into P^T and
+//     dS^T; the accumulators take columns [256, 512).  A sub-tile row's 64
+//     columns are split between two threads: warp w serves TMEM lanes
+//     32 (w % 4) .. + 31, columns 32 (w / 4) .. + 31 of the buffer.
+// Warps 0-7 serve the rows; warp 8 issues TMA loads (one ring stage per step,
+// each step prefetched into L2 a few steps before its load); warp 9 owns the
+// tensor memory and issues every tcgen05.mma: the whole warp runs the issuing
+// loop converged and one elected lane issues.
 // Every wait is bounded; a wait that gives up raises the error word and the
 // abort flag, the roles leave their loops, in-flight copies and MMAs drain,
 // and the CTA frees its tensor memory.
@@ -264,11 +265,43 @@ __device__ __forceinline__ uint64_t kmajor_off(int kk, uint32_t chunk_bytes)
 // =============================================================================
 // dQ (and D) -- one CTA per (sequence, head, query tile), heaviest tiles first
 // =============================================================================
+// Geometry of the dQ kernel: 128-key steps with S and dP single-buffered in
+// TMEM -- S in columns [0, 128), dP in [128, 256) (dS packed into its first
+// half per thread), dQ in [256, 256 + D), Q and dO as bf16 A operands after it.
+// The MMA warp issues, per step j: S_{j+1} as soon as the rows have read S_j,
+// dQ += dS_j K_j once they have stored dS_j, then dP_{j+1}; so the tensor
+// pipe runs S_{j+1} while the rows finish dS_j, and only dQ_j waits for them.
+// The ring holds K_j and V_j (128 rows each) in three stages: two of their
+// own and, once the prologue has copied Q and dO into TMEM and formed D, the
+// region that held the resident Q and dO tiles.
+template <int D>
+struct CfgQ {
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kTileBytes = BT * D * 2;       // one 128-row bf16 tile
+    static constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K_j, V_j
+    static constexpr int kStages = 3;                         // stage 2 = the Q / dO region
+    static constexpr uint32_t kOffRes = 0;
+    static constexpr uint32_t kOffRing = 2 * kTileBytes;
+    static constexpr uint32_t kOffXch = kOffRing + 2 * kStageBytes;   // 128 D_i values
+    static constexpr uint32_t kOffBar = kOffXch + BT * 4;
+    // a_full, kv_full[3], kv_empty[3], s_full, dp_full, s_free, p_full, o_full,
+    // drain, a_tm, res_free
+    static constexpr int kBars = 1 + 2 * kStages + 8;
+    static constexpr uint32_t kSmemBytes = kOffBar + 8 * kBars + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static __device__ __forceinline__ uint32_t stage_off(int s)
+    {
+        return s == 2 ? kOffRes : kOffRing + uint32_t(s) * kStageBytes;
+    }
+};
+constexpr uint32_t kQColS = 0, kQColDP = 128;   // dQ kernel: S; dP, then dS packed
+constexpr int kQCols = 64;                      // columns of a step per row thread
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
-    using C = Cfg<D>;
+    using C = CfgQ<D>;
     // Q and dO as bf16 pairs in TMEM after the dQ accumulator (D / 2 columns
     // each): the A operands of S = Q K^T and dP = dO V^T
     constexpr uint32_t kColQA = kColAcc + D;
@@ -276,8 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Bars bar = carve<D>(smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + C::kBarBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *a_full = bars, *kv_full = bars + 1, *kv_empty = bars + 1 + C::kStages;
+    uint64_t *s_full = bars + 1 + 2 * C::kStages, *dp_full = s_full + 1, *s_free = s_full + 2,
+             *p_full = s_full + 3, *o_full = s_full + 4, *drain = s_full + 5, *a_tm = s_full + 6,
+             *res_free = s_full + 7;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int bh_count = p.B * p.H;
@@ -285,47 +322,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
     const int64_t row0 = int64_t(b) * p.N;          // first row of the sequence
-    // key sub-tiles this query tile sees (at least one)
-    const int n_kv = p.causal ? min(2 * qt + 2, p.n_sub) : p.n_sub;
+    // 128-key steps this query tile sees (at least one)
+    const int n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const uint32_t tmem = setup<D>(p, bar, 1u, abort_flag, tmem_slot);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(a_full, 1);
+        for (int st = 0; st < C::kStages; ++st) {
+            ptx::mbar_init(&kv_full[st], 1);
+            ptx::mbar_init(&kv_empty[st], 1);
+        }
+        ptx::mbar_init(s_full, 1);
+        ptx::mbar_init(dp_full, 1);
+        ptx::mbar_init(s_free, kRowWarps);
+        ptx::mbar_init(p_full, kRowWarps);
+        ptx::mbar_init(o_full, 1);
+        ptx::mbar_init(drain, 1);
+        ptx::mbar_init(a_tm, kRowWarps);
+        ptx::mbar_init(res_free, kRowWarps);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kWarpLoad && lane == 0) {
+        ptx::prefetch_tmap(&p.tm_a0);
+        ptx::prefetch_tmap(&p.tm_a1);
+        ptx::prefetch_tmap(&p.tm_s0);
+        ptx::prefetch_tmap(&p.tm_s1);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
     bool aborted = false;
-    uint8_t *tile_q = smem + C::kOffA0, *tile_do = smem + C::kOffA1;
-    uint8_t *ring = smem + C::kOffRing;
+    uint8_t *tile_q = smem + C::kOffRes, *tile_do = tile_q + C::kTileBytes;
 
     if (warp == kWarpLoad) {
         // ======================= TMA producer ==============================
-        // Ring stage of step j: K_j then V_j (64 keys each).
         if (lane == 0) {
             int last_phase[C::kStages];
-            for (int s = 0; s < C::kStages; ++s)
-                last_phase[s] = -1;
-            ptx::mbar_arrive_expect_tx(bar.a_full, 2 * C::kResBytes);
+            for (int st = 0; st < C::kStages; ++st)
+                last_phase[st] = -1;
+            ptx::mbar_arrive_expect_tx(a_full, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                ptx::tma_load_3d(tile_q + c * kResChunkBytes, &p.tm_a0, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_q + c * kResChunkBytes, &p.tm_a0, a_full, c * 64, h,
                                  int(row0 + int64_t(qt) * BT));
-                ptx::tma_load_3d(tile_do + c * kResChunkBytes, &p.tm_a1, bar.a_full, c * 64, h,
+                ptx::tma_load_3d(tile_do + c * kResChunkBytes, &p.tm_a1, a_full, c * 64, h,
                                  int(row0 + int64_t(qt) * BT));
             }
             int stage = 0;
             uint32_t phase = 0;
             for (int j = 0; j < n_kv; ++j) {
-                if (!ptx::mbar_wait(&bar.kv_empty[stage], phase ^ 1u, abort_flag, p.err_word))
+                if (!ptx::mbar_wait(&kv_empty[stage], phase ^ 1u, abort_flag, p.err_word))
                     break;
-                uint8_t *dst = ring + stage * C::kStageBytes;
-                const int row = int(row0 + int64_t(j) * BS);
-                ptx::mbar_arrive_expect_tx(&bar.kv_full[stage], C::kStageBytes);
+                // stage 2 is the Q / dO region: free once the rows are done with it
+                if (j == 2 && !ptx::mbar_wait(res_free, 0, abort_flag, p.err_word))
+                    break;
+                uint8_t *dst = smem + C::stage_off(stage);
+                const int row = int(row0 + int64_t(j) * BT);
+                ptx::mbar_arrive_expect_tx(&kv_full[stage], C::kStageBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    ptx::tma_load_3d(dst + c * kSubChunkBytes, &p.tm_s0, &bar.kv_full[stage],
-                                     c * 64, h, row);
-                    ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
-                                     &bar.kv_full[stage], c * 64, h, row);
+                    ptx::tma_load_3d(dst + c * kResChunkBytes, &p.tm_s0, &kv_full[stage], c * 64,
+                                     h, row);
+                    ptx::tma_load_3d(dst + C::kTileBytes + c * kResChunkBytes, &p.tm_s1,
+                                     &kv_full[stage], c * 64, h, row);
                 }
-                if (j + kL2Ahead < n_kv)
+                if (j + C::kStages < n_kv)
                     for (int c = 0; c < C::kChunks; ++c) {
-                        ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
-                        ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
+                        ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + C::kStages * BT);
+                        ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + C::kStages * BT);
                     }
                 last_phase[stage] = int(phase);
                 if (++stage == C::kStages) {
@@ -334,91 +402,101 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (*abort_flag) {
-                drain_wait(bar.a_full, 0);
-                for (int s = 0; s < C::kStages; ++s)
-                    if (last_phase[s] >= 0)
-                        drain_wait(&bar.kv_full[s], uint32_t(last_phase[s]));
+                drain_wait(a_full, 0);
+                for (int st = 0; st < C::kStages; ++st)
+                    if (last_phase[st] >= 0)
+                        drain_wait(&kv_full[st], uint32_t(last_phase[st]));
             }
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ======================= MMA issuer (whole warp) =====================
-        // Order: S_0, dP_0; then per step j: S_{j+1}, dP_{j+1} (other buffer),
-        // wait for dS_j, dQ += dS_j K_j.  The warp runs the loop converged and
-        // one elected lane issues the MMAs and commits.
-        constexpr uint32_t idesc_ss = ptx::idesc_bf16_f32(BT, BS, false);
-        constexpr uint32_t idesc_ts = ptx::idesc_bf16_f32(BT, D, true);
+        constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BT, false);   // N = 128 keys
+        constexpr uint32_t idesc_q = ptx::idesc_bf16_f32(BT, D, true);     // B MN-major
         constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
-        constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kSubChunkBytes, 1024);
-        const uint32_t ring_addr = ptx::smem_u32(ring);
-        int stage = 0;
-        uint32_t phase = 0;
-        int k_stage0 = 0, k_stage1 = 0;            // step's ring stage, per buffer
-        // S_j = Q K_j^T and dP_j = dO V_j^T into buffer j & 1
-        auto issue_s = [&](int j) -> bool {
-            if (!ptx::mbar_wait_warp(&bar.kv_full[stage], phase, abort_flag, p.err_word))
-                return false;
-            (j & 1 ? k_stage1 : k_stage0) = stage;
-            const uint32_t kaddr = ring_addr + stage * C::kStageBytes;
-            if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            ptx::tc_fence_after_sync();
+        constexpr uint64_t desc_mnmajor = ptx::smem_desc_base(kResChunkBytes, 1024);
+        // S = Q K^T into columns [0, 128) (A = Q from TMEM)
+        auto issue_s = [&](uint32_t kaddr) {
             const uint64_t dk = ptx::smem_desc(desc_kmajor, kaddr);
-            const uint64_t dv = ptx::smem_desc(desc_kmajor, kaddr + C::kSubBytes);
-            const uint32_t buf = tmem + uint32_t(j & 1) * kColBuf;
             if (ptx::elect_one()) {
-                // A = Q, dO from TMEM (K step kk: 8 columns of bf16 pairs)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ts(buf, tmem + kColQA + 8 * kk, dk + kmajor_off(kk, kSubChunkBytes),
-                                idesc_ss, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ts(buf + kColDP, tmem + kColQA + D / 2 + 8 * kk,
-                                dv + kmajor_off(kk, kSubChunkBytes), idesc_ss, kk > 0 ? 1u : 0u);
-                ptx::mma_commit(&bar.s_full[j & 1]);
+                    ptx::mma_ts(tmem + kQColS, tmem + kColQA + 8 * kk,
+                                dk + kmajor_off(kk, kResChunkBytes), idesc_s, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(s_full);
             }
             __syncwarp();
-            return true;
         };
+        // dP = dO V^T into columns [128, 256) (A = dO from TMEM)
+        auto issue_dp = [&](uint32_t vaddr) {
+            const uint64_t dv = ptx::smem_desc(desc_kmajor, vaddr);
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ts(tmem + kQColDP, tmem + kColQA + D / 2 + 8 * kk,
+                                dv + kmajor_off(kk, kResChunkBytes), idesc_s, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(dp_full);
+            }
+            __syncwarp();
+        };
+        const uint32_t smem_base = ptx::smem_u32(smem);
         do {
-            if (!ptx::mbar_wait_warp(bar.a_tm, 0, abort_flag, p.err_word) || !issue_s(0)) {
+            if (!ptx::mbar_wait_warp(a_tm, 0, abort_flag, p.err_word) ||
+                !ptx::mbar_wait_warp(&kv_full[0], 0, abort_flag, p.err_word)) {
                 aborted = true;
                 break;
             }
+            ptx::tc_fence_after_sync();
+            issue_s(smem_base + C::stage_off(0));
+            issue_dp(smem_base + C::stage_off(0) + C::kTileBytes);
+            int cur = 0;                               // ring stage of step j
+            int nxt = 1;
+            uint32_t nxt_phase = 0;                    // phase of step j + 1's stage
             for (int j = 0; j < n_kv; ++j) {
-                if (j + 1 < n_kv && !issue_s(j + 1)) {
-                    aborted = true;
-                    break;
+                const bool more = j + 1 < n_kv;
+                if (more) {
+                    // S_{j+1} overwrites S_j once every row has read it
+                    if (!ptx::mbar_wait_warp(s_free, uint32_t(j) & 1u, abort_flag, p.err_word) ||
+                        !ptx::mbar_wait_warp(&kv_full[nxt], nxt_phase, abort_flag, p.err_word)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    issue_s(smem_base + C::stage_off(nxt));
                 }
-                // dQ += dS_j K_j   (dS: bf16 packed in buffer j & 1)
-                if (!ptx::mbar_wait_warp(&bar.p_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag,
-                                         p.err_word)) {
+                // dQ += dS_j K_j   (dS: bf16 packed in the first half of each
+                // row thread's 64 dP columns; K_j an MN-major operand)
+                if (!ptx::mbar_wait_warp(p_full, uint32_t(j) & 1u, abort_flag, p.err_word)) {
                     aborted = true;
                     break;
                 }
                 ptx::tc_fence_after_sync();
-                const int ks = (j & 1) ? k_stage1 : k_stage0;
-                const uint64_t dkn = ptx::smem_desc(desc_mnmajor, ring_addr + ks * C::kStageBytes);
-                const uint32_t a_tm = tmem + uint32_t(j & 1) * kColBuf;
+                const uint64_t dkn = ptx::smem_desc(desc_mnmajor, smem_base + C::stage_off(cur));
                 if (ptx::elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BS / 16; ++kk)
-                        ptx::mma_ts(tmem + kColAcc, a_tm + packed_col(kk),
-                                    dkn + uint64_t((kk * 16 * 128) >> 4), idesc_ts,
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        ptx::mma_ts(tmem + kColAcc,
+                                    tmem + kQColDP + uint32_t(kQCols * (kk >> 2) + 8 * (kk & 3)),
+                                    dkn + uint64_t((kk * 16 * 128) >> 4), idesc_q,
                                     (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(&bar.kv_empty[ks]);
+                    ptx::mma_commit(&kv_empty[cur]);
                 }
                 __syncwarp();
+                // dP_{j+1} overwrites dS_j after the dQ product has read it
+                if (more)
+                    issue_dp(smem_base + C::stage_off(nxt) + C::kTileBytes);
+                cur = nxt;
+                if (++nxt == C::kStages) {
+                    nxt = 0;
+                    nxt_phase ^= 1u;
+                }
             }
         } while (false);
         if (ptx::elect_one()) {
             if (!aborted)
-                ptx::mma_commit(bar.o_full);
-            ptx::mma_commit(bar.drain);
-            drain_wait(bar.drain, 0);
+                ptx::mma_commit(o_full);
+            ptx::mma_commit(drain);
+            drain_wait(drain, 0);
         }
         __syncwarp();
     } else {
@@ -438,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row threads in shared memory.
         constexpr int kLanesPerRow = D / 8, kRowsPerInst = 32 / kLanesPerRow;
         constexpr int kRowsPerWarp = BT / kRowWarps;          // 16
-        float *xch = reinterpret_cast<float *>(smem + C::kOffStat);   // 128 sums
+        float *xch = reinterpret_cast<float *>(smem + C::kOffXch);   // 128 sums
         {
             const int sub = lane / kLanesPerRow, lr = lane % kLanesPerRow;
             uint4 ov[kRowsPerWarp / kRowsPerInst];
@@ -450,11 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        p.O + ((row0 + qi) * p.H + h) * D + lr * 8)
                                  : make_uint4(0, 0, 0, 0);
             }
-            const bool a_ok = row_wait(bar.a_full, 0, abort_flag, p.err_word);
+            const bool a_ok = row_wait(a_full, 0, abort_flag, p.err_word);
             if (a_ok) {
                 // this thread's half of row r of Q and of dO into TMEM, as the
-                // bf16 pairs of the S and dP products' A operands (shared-memory
-                // unit u of row r sits at unit u ^ (r % 8) of its 128 bytes)
+                // bf16 pairs of the S and dP products' A operands
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const uint8_t *tile = t == 0 ? tile_q : tile_do;
@@ -470,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w[4 * ul + 2] = v.z;
                         w[4 * ul + 3] = v.w;
                     }
-                    const uint32_t dst = tmem + lane_bits + kColQA + uint32_t(t * (D / 2) + g * (D / 4));
+                    const uint32_t dst =
+                        tmem + lane_bits + kColQA + uint32_t(t * (D / 2) + g * (D / 4));
                     if constexpr (D == 128)
                         ptx::tmem_st32(dst, w);
                     else
@@ -480,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0)
-                    ptx::mbar_arrive(bar.a_tm);
+                    ptx::mbar_arrive(a_tm);
             }
 #pragma unroll
             for (int k = 0; k < kRowsPerWarp / kRowsPerInst; ++k) {
@@ -508,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lr == 0)
                     xch[rr] = part;
             }
+            // this warp has finished with the Q / dO region (ring stage 2)
+            __syncwarp();
+            if (a_ok && lane == 0)
+                ptx::mbar_arrive(res_free);
         }
         const float lse_raw = row_ok ? p.lse[stat] : 0.f;
         asm volatile("bar.sync 1, %0;" ::"n"(BT * G) : "memory");   // the row threads
@@ -516,52 +598,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.D[stat] = Di;
         const float lse2 = lse_raw * kLog2e;
         const float sl = p.scale_log2;
-        const int col0 = g * kColsPerThread;
+        const int col0 = g * kQCols;
+        const uint32_t tS = tmem + lane_bits + kQColS + uint32_t(col0);
+        const uint32_t tDP = tmem + lane_bits + kQColDP + uint32_t(col0);
 
         for (int j = 0; j < n_kv; ++j) {
-            if (!row_wait(&bar.s_full[j & 1], uint32_t(j >> 1) & 1u, abort_flag,
-                                p.err_word)) {
+            const uint32_t par = uint32_t(j) & 1u;
+            if (!row_wait(s_full, par, abort_flag, p.err_word)) {
                 aborted = true;
                 break;
             }
             ptx::tc_fence_after_sync();
-            // last visible column of this key sub-tile for row i (causal
-            // diagonal, end of the sequence); rows past the end see nothing
-            int lim = BS - 1;
-            if (p.causal && i - j * BS < lim)
-                lim = i - j * BS;
-            if (p.N - 1 - j * BS < lim)
-                lim = p.N - 1 - j * BS;
+            // last visible column of this key tile for row i (causal diagonal,
+            // end of the sequence); rows past the end see nothing
+            int lim = BT - 1;
+            if (p.causal && i - j * BT < lim)
+                lim = i - j * BT;
+            if (p.N - 1 - j * BT < lim)
+                lim = p.N - 1 - j * BT;
             if (!row_ok)
                 lim = -1;
-            const uint32_t tS = tmem + lane_bits + uint32_t(j & 1) * kColBuf + col0;
-            uint32_t sv[32], dv[32], pk[16];
-            ptx::tmem_ld32(tS, sv);
-            ptx::tmem_ld32(tS + kColDP, dv);
-            ptx::tmem_wait_ld();
+            float pr[kQCols];
+            {
+                uint32_t sv0[32], sv1[32];
+                ptx::tmem_ld32(tS, sv0);
+                ptx::tmem_ld32(tS + 32, sv1);
+                ptx::tmem_wait_ld();
+                // S is read: the MMA warp may overwrite it with the next step's
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(s_free);
+                // masked entries get exponent -inf: exp2 gives 0, no branch
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                float ds[2];
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int c = col0 + 2 * e + k;
-                    const float x = __uint_as_float(sv[2 * e + k]);
-                    const float y = __uint_as_float(dv[2 * e + k]);
-                    // masked entries get exponent -inf: exp2 gives 0, no branch
-                    const float pv = ptx::ex2(c <= lim ? fmaf(x, sl, -lse2) : -INFINITY);
-                    ds[k] = pv * (y - Di);
+                for (int k = 0; k < 32; ++k) {
+                    const int c0 = col0 + k, c1 = col0 + 32 + k;
+                    pr[k] = ptx::ex2(c0 <= lim ? fmaf(__uint_as_float(sv0[k]), sl, -lse2)
+                                               : -INFINITY);
+                    pr[32 + k] = ptx::ex2(c1 <= lim ? fmaf(__uint_as_float(sv1[k]), sl, -lse2)
+                                                    : -INFINITY);
                 }
-                pk[e] = ptx::pack_bf16x2(ds[0], ds[1]);
             }
-            ptx::tmem_st16(tS, pk);                   // dS of this block, packed
+            if (!row_wait(dp_full, par, abort_flag, p.err_word)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            uint32_t pk[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t dv[32];
+                ptx::tmem_ld32(tDP + 32 * half, dv);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float d0 = pr[32 * half + 2 * e] * (__uint_as_float(dv[2 * e]) - Di);
+                    const float d1 =
+                        pr[32 * half + 2 * e + 1] * (__uint_as_float(dv[2 * e + 1]) - Di);
+                    pk[16 * half + e] = ptx::pack_bf16x2(d0, d1);
+                }
+            }
+            ptx::tmem_st32(tDP, pk);                  // dS of this row's 64 keys, packed
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                ptx::mbar_arrive(&bar.p_full[j & 1]);
+                ptx::mbar_arrive(p_full);
         }
         // the two groups store half of each row's dQ each
-        if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
+        if (!aborted && ptx::mbar_wait(o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
             store_row(tmem + lane_bits + kColAcc, p.scale, p.dQ + ((row0 + i) * p.H + h) * D,
                       row_ok, g * (D / 64), (g + 1) * (D / 64));
@@ -857,13 +962,13 @@ int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t st
 {
     static PerDeviceOnce once_dq, once_dkdv;
     if (!set_max_dynamic_smem(once_dq, reinterpret_cast<const void *>(attn_bwd_dq_kernel<D>),
-                              int(Cfg<D>::kSmemBytes)) ||
+                              int(CfgQ<D>::kSmemBytes)) ||
         !set_max_dynamic_smem(once_dkdv, reinterpret_cast<const void *>(attn_bwd_dkdv_kernel<D>),
                               int(Cfg<D>::kSmemBytes)))
         return FA_ERR_CUDA;
     const int64_t blocks = int64_t(p_dq.n_tiles) * p_dq.B * p_dq.H;
     attn_bwd_dq_kernel<D>
-        <<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dq);
+        <<<dim3(unsigned(blocks)), dim3(kThreads), CfgQ<D>::kSmemBytes, stream>>>(p_dq);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     attn_bwd_dkdv_kernel<D>
@@ -901,8 +1006,8 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
     BwdParams p_dq = p, p_dkdv = p;
     if (!make_tmap_bf16(&p_dq.tm_a0, a.Q, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p_dq.tm_a1, a.dO, total, a.H, a.d, BT) ||
-        !make_tmap_bf16(&p_dq.tm_s0, a.K, total, a.H, a.d, BS) ||
-        !make_tmap_bf16(&p_dq.tm_s1, a.V, total, a.H, a.d, BS) ||
+        !make_tmap_bf16(&p_dq.tm_s0, a.K, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p_dq.tm_s1, a.V, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p_dkdv.tm_a0, a.K, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p_dkdv.tm_a1, a.V, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p_dkdv.tm_s0, a.Q, total, a.H, a.d, BS) ||
