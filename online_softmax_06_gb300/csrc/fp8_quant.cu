@@ -413,7 +413,7 @@ struct VtParams {
 constexpr uint32_t kVtSmemBytes = kRows * 128 + 1024;
 
 // V' = codes of V / sv, transposed per head ([B, H, d, n_pad]; keys past N are
-// zero codes).  One CTA (8 warps) per (128-key tile, sequence * head): lane l
+// zero codes).  One CTA (8 warps) per (sequence * head, 128-key tile): lane l
 // takes keys 4l .. 4l + 3 and warp w head-dim columns 16w .. 16w + 15 (two
 // 16-byte pieces of a key row, one 32-byte sector).  For each of its columns
 // a lane writes the codes of its 4 keys as one 32-bit word into the staging
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(256) fp8_vt_kernel(const __grid_constant__ VtP
     extern __shared__ uint8_t smem_raw[];
     uint8_t *stage = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tile = blockIdx.x, bh = blockIdx.y;
+    const int bh = blockIdx.x, tile = blockIdx.y;
     const int b = bh / p.H, h = bh % p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = 16 * warp;
@@ -482,6 +482,10 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
     if (a.d != 128)
         return FA_ERR_UNSUPPORTED;
     const int n_tiles = (a.N + kRows - 1) / kRows;
+    // work items of the first kernel are counted in an int; the second
+    // kernel's grid takes the tiles of a head along y (at most 65535)
+    if (3 * int64_t(a.B) * a.H * n_tiles > 0x7fffffffLL || n_tiles > 65535)
+        return FA_ERR_TOO_LARGE;
     QkMmaParams q;
     if (!make_tmap_seq_4d(&q.tm_x[0], a.Q, false, a.B, a.N, a.H, a.d) ||
         !make_tmap_seq_4d(&q.tm_x[1], a.K, false, a.B, a.N, a.H, a.d) ||
@@ -526,7 +530,7 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
     if (!set_max_dynamic_smem(once_vt, reinterpret_cast<const void *>(fp8_vt_kernel),
                               int(kVtSmemBytes)))
         return FA_ERR_CUDA;
-    const dim3 grid_v(unsigned(n_tiles), unsigned(a.B * a.H));
+    const dim3 grid_v(unsigned(a.B * a.H), unsigned(n_tiles));
     fp8_vt_kernel<<<grid_v, 256, kVtSmemBytes, stream>>>(v);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -184,6 +184,45 @@ def test_fp8_outliers_pages_experiment(dev):
     assert rmse < 1.5e-2 and rmse < rmse_b
 
 
+def dequantised_from_workspace(ws, B, H, N, d):
+    """Q', K', V' as the kernels quantised them (codes times scales, float32),
+    read back from the workspace."""
+    L = layout(B, H, N, d)
+    T = L["T"]
+    e = B * N * H * d
+
+    def tile_scaled(off, soff):
+        codes = e4m3_decode(ws[off:off + e]).reshape(B, N, H, d)
+        sc = ws[soff:soff + B * H * T * 4].view(np.float32).reshape(B, H, T).astype(np.float64)
+        return codes * np.repeat(sc, 128, axis=2)[:, :, :N].transpose(0, 2, 1)[..., None]
+
+    Qd = tile_scaled(L["qf"], L["sq"])
+    Kd = tile_scaled(L["kf"], L["sk"])
+    vt = ws[L["vt"]:L["vt"] + B * H * d * 128 * T].reshape(B, H, d, 128 * T)
+    sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H).astype(np.float64)
+    Vd = e4m3_decode(np.ascontiguousarray(vt[..., :N])) * sv[:, :, None, None]
+    return (Qd.astype(np.float32), Kd.astype(np.float32),
+            np.ascontiguousarray(Vd.transpose(0, 3, 1, 2)).astype(np.float32))
+
+
+def test_fp8_many_heads(dev):
+    """More sequence-heads than a grid's y dimension holds (65535): the
+    quantisation and attention grids take them along x.  The attention is
+    checked on the codes the kernels produced (a few of 34 M codes may be
+    the neighbour of the float64 method's, which moves a one-key row's lse
+    by ~1e-2; the codes themselves are checked by the quantisation test)."""
+    B, H, N, d = 1, 66000, 2, 128
+    qkv, signs = make(B, H, N, d, seed=66)
+    O, lse, ws = run(qkv, signs, True, dev)
+    Qd, Kd, Vd = dequantised_from_workspace(ws, B, H, N, d)
+    Or, lr = oracle.attention_dense(Qd, Kd, Vd, 1 / math.sqrt(d), True)
+    rmse = float(np.sqrt(np.mean((O - Or) ** 2)))
+    V = qkv[2].float().numpy()
+    assert rmse <= FP8_O_RMSE and float(np.abs(O - Or).max()) <= 2.0 ** -4 * float(np.abs(V).max())
+    assert float(np.abs(lse - lr).max()) <= FP8_LSE_MAX
+    device_error_clear()
+
+
 def test_fp8_bad_arguments(dev):
     assert fa.fa_attention_fp8_workspace_bytes(1, 1, 128, 64) == -3
     q = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev)
