@@ -63,6 +63,8 @@ def normwise(g, ref):
     (2, 1, 640, 64, True),
     (1, 2, 192, 128, True),      # last tile exactly one 64-row sub-tile
     (1, 1, 65, 64, True),        # two sub-tiles, one tile
+    (1, 2, 1000, 128, True),     # up to 8 key steps of the dQ pass: its ring wraps, ragged end
+    (2, 1, 900, 64, False),      # the same at d = 64, non-causal, two sequences
 ])
 def test_bwd_matches_oracle(dev, B, H, N, d, causal):
     Q, K, V, dO = make_inputs(B, H, N, d, seed=N * 7 + d + B)
