@@ -46,6 +46,20 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int64_t split_stride_lse = int64_t(B) * H * N;
     const int64_t lse_off = (int64_t(b) * H + h) * N + i;
 
+    constexpr int kBatch = 16;
+    using Vec = typename std::conditional<kPerLane == 4, float4, float2>::type;
+    const int64_t split_stride_o = int64_t(B) * N * H * D;
+    const int64_t o_off = row * D + lane * kPerLane;   // row = (b * N + i) * H + h
+    // The first kBatch splits' O rows are loaded before the weights are known,
+    // so their loads overlap those of the logsumexps.  A split that saw no key
+    // of the row (lse_s = -inf) never wrote its O_s: its weight is 0 and its
+    // values, whatever they are, are selected away below, never multiplied.
+    Vec v0[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+        if (u < splits)
+            v0[u] = *reinterpret_cast<const Vec *>(O_accum + u * split_stride_o + o_off);
+
     // m = max_s lse_s; lse = m + ln sum_s exp(lse_s - m)   (log2 units inside).
     // Lane l keeps lse of split l (the first chunk of 32) in a register, so
     // with up to 32 splits every lse is read once.
@@ -67,19 +81,29 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const float total = (mx == -INFINITY) ? -INFINITY : mx + log2f(sum);   // log2 units
 
     // O = sum_s w_s O_s with w_s = exp(lse_s - lse).  Lane l holds w of split
-    // c0 + l of the current chunk of 32; the splits are taken sixteen at a time
-    // with their loads issued before the FMAs, so a warp keeps sixteen 128-bit
-    // loads per lane in flight.  A split with w = 0 (lse_s = -inf: it saw no
-    // key of the row, its O_s was never written) is not read.
-    constexpr int kBatch = 16;
-    using Vec = typename std::conditional<kPerLane == 4, float4, float2>::type;
+    // c0 + l of the current chunk of 32; past the first kBatch splits the
+    // splits are taken sixteen at a time with their loads issued before the
+    // FMAs, and a split with w = 0 is not read.
     float acc[kPerLane];
 #pragma unroll
     for (int e = 0; e < kPerLane; ++e)
         acc[e] = 0.f;
-    const int64_t split_stride_o = int64_t(B) * N * H * D;
-    const int64_t o_off = row * D + lane * kPerLane;   // row = (b * N + i) * H + h
     if (total != -INFINITY) {
+        // the early-loaded splits (a selected 0 for those with w = 0, whose
+        // values are never multiplied)
+        {
+            const float w_l = ptx::ex2(x0 - total);   // 0 past the last split
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const float w = __shfl_sync(0xffffffffu, w_l, u);
+                if (u < splits && w != 0.f) {
+                    const float *f = reinterpret_cast<const float *>(&v0[u]);
+#pragma unroll
+                    for (int e = 0; e < kPerLane; ++e)
+                        acc[e] = fmaf(w, f[e], acc[e]);
+                }
+            }
+        }
         for (int c0 = 0; c0 < splits; c0 += 32) {
             const int s_l = c0 + lane;
             const float x_l = c0 == 0 ? x0
@@ -88,7 +112,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                                              : -INFINITY);
             const float w_l = ptx::ex2(x_l - total);   // 0 past the last split
             const int n = splits - c0 < 32 ? splits - c0 : 32;
-            for (int u0 = 0; u0 < n; u0 += kBatch) {
+            for (int u0 = c0 == 0 ? kBatch : 0; u0 < n; u0 += kBatch) {
                 float w[kBatch];
                 Vec v[kBatch];
 #pragma unroll
