@@ -182,7 +182,8 @@ FA_API int fa_attention_bwd(const void *Q, const void *K, const void *V, const v
  *   boundary (T = ceil(N / 128)): e4m3 Q M / sq [B*N, H, d], e4m3 K M / sk
  *   [B*N, H, d], e4m3 V^T / sv [B, H, d, 128 T], fp32 sq and sk [B, H, T],
  *   fp32 per-tile amax of V [B, H, T], fp32 sv [B, H].
- *   d: 128 only.
+ *   d: 128 only.  Size limits: ceil(N / 128) <= 65535 and
+ *   3 * B * H * ceil(N / 128) < 2^31 (FA_ERR_TOO_LARGE otherwise).
  * Three kernels run on the library stream; no synchronisation.
  * Errors: FA_ERR_UNSUPPORTED (d != 128), FA_ERR_BAD_SIZE (also a workspace
  * that is too small), FA_ERR_NULL_POINTER, FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE,
