@@ -121,3 +121,26 @@ def test_stream_setting_is_per_thread(lib):
 def test_no_device_is_reported(lib):
     # valid-looking sizes with no GPU present: the library refuses before launching
     assert fa.fa_softmax_rows(ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 4) == -7
+
+
+def test_tensor_wrappers_refuse_host_tensors():
+    """No CPU fallback: the device-tensor wrappers reject host tensors before
+    anything runs (the host-buffer entry point is the one that takes them)."""
+    import torch
+    import online_softmax_06_gb300 as fa
+    x = torch.zeros((4, 8), dtype=torch.float32)
+    q = torch.zeros((1, 8, 1, 64), dtype=torch.bfloat16)
+    lse = torch.zeros((1, 1, 8), dtype=torch.float32)
+    signs = torch.ones(128, dtype=torch.float32)
+    q128 = torch.zeros((1, 8, 1, 128), dtype=torch.bfloat16)
+    calls = [
+        lambda: fa.softmax_rows(x),
+        lambda: fa.attention_fwd(q, q, q),
+        lambda: fa.attention_fwd(q.float(), q.float(), q.float()),
+        lambda: fa.attention_fwd_splitkv(q, q, q),
+        lambda: fa.attention_fwd_fp8(q128, q128, q128, signs),
+        lambda: fa.attention_bwd(q, q, q, q, q, lse),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError):
+            call()
