@@ -6,7 +6,9 @@ on the causal bf16 workload B=2, H=32, N=4096, d=128 (Q, K, V ~ N(0,1) rounded
 to bf16; 192 MiB of Q/K/V, larger than the 129 MB L2), through the C ABI.
 The row softmax (fp32, 4096 x N, the HBM-resident lengths) is timed in the
 same run with L2 flushed before every repetition and reported under
-"softmax"; split-KV attention on a decode-like shape (256 queries, 32768 keys)
+"softmax" (all five row lengths, each with its regime); the other attention
+configurations (fp32 single head, bf16 d=64 non-causal, bf16 varlen causal)
+under "configs"; split-KV attention on a decode-like shape (256 queries, 32768 keys)
 under "splitkv"; the attention backward on the headline workload under
 "bwd" and the FP8 forward under "fp8".  Prints one JSON line (rank 0).
 
@@ -52,8 +54,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(
         k for k, w in workloads.WORKLOADS.items() if w.dtype == "bf16"))
-    ap.add_argument("--softmax-n", default="4096,32768",
+    ap.add_argument("--softmax-n", default="32,128,1024,4096,32768",
                     help="comma-separated row lengths for the softmax leg ('' to skip)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the legs of the other attention configurations")
     ap.add_argument("--softmax-reps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-splitkv", action="store_true", help="skip the split-KV leg")
@@ -277,6 +281,54 @@ def time_attention(fa, w, dev, steps, warmup, dist, clocks):
     return ms, steps
 
 
+def time_config(fa, w, dev, reps, peaks, clocks):
+    """One more attention configuration, timed like the headline (CUDA events
+    over back-to-back launches on the library stream, after warm-up): the
+    d = 64 non-causal and the varlen causal workloads on the tensor-core
+    kernel, and the fp32 single-head workload on the CUDA-core kernel (a
+    correctness path: 16.8 MFLOP, one launch's latency)."""
+    import torch
+    if w.dtype == "f32":
+        Q, K, V = w.inputs()
+        q, k, v = (torch.from_numpy(t).to(dev) for t in (Q, K, V))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        fa.fa_set_stream(stream.cuda_stream)
+
+        def launch():
+            rc = fa.fa_attention_fwd_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale,
+                                         int(w.causal), None)
+            if rc != 0:
+                raise RuntimeError(fa.strerror(rc))
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(t0, time.time())
+        ms = e0.elapsed_time(e1) / reps
+        tf = w.flops() / (ms / 1e3) / 1e12
+        return {"ms": ms, "TFLOP_per_s": tf, "dtype": "f32", "bound": "latency",
+                "kernel": "attn_fwd_f32_kernel", "flops_per_launch": w.flops(),
+                "note": "fp32 CUDA-core path for fp32 accuracy; one small launch, so the "
+                        "time is launch and latency, not a roofline"}
+    ms, steps = time_attention(fa, w, dev, reps, 3, None, clocks)
+    ms /= steps
+    tf = w.flops() / (ms / 1e3) / 1e12
+    return {"ms": ms, "TFLOP_per_s": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "dtype": "bf16", "bound": "tensor", "kernel": f"attn_fwd_bf16_kernel<{w.d}>",
+            "flops_per_launch": w.flops(),
+            "l2": "inputs larger than L2 (Q/K/V %.0f MiB); %d back-to-back launches"
+                  % (3 * w.total * w.H * w.d * 2 / 2**20, reps)}
+
+
 def time_e2e(fa, w, dev, steps, warmup):
     """Same metric through the C ABI with host buffers: every step takes Q, K, V
     from pinned host memory and leaves O and lse in pinned host memory.  Dense
@@ -388,8 +440,17 @@ def time_softmax(fa, dev, Ns, reps, peaks, clocks):
         warm_ms = e0.elapsed_time(e1) / reps
         nbytes = 8.0 * rows * N
         gbs = nbytes / (ms / 1e3) / 1e9
+        if nbytes >= 2 * 129e6:
+            regime = "HBM-bound (input and output larger than the 129 MB L2)"
+        elif nbytes >= 16 * 2**20:
+            regime = ("input read cold from HBM, output (%.0f MiB) fits in L2 and is written "
+                      "back after the kernel: partly L2-bound" % (nbytes / 2 / 2**20))
+        else:
+            regime = ("latency-bound: %.1f MiB in and out, launch and one-wave latency "
+                      "dominate; the GB/s figure is not an HBM roofline fraction"
+                      % (nbytes / 2 / 2**20))
         out[str(N)] = {"rows": rows, "N": N, "ms": ms, "GB_per_s": gbs,
-                       "frac_of_hbm": gbs / peaks["hbm_gbs"],
+                       "frac_of_hbm": gbs / peaks["hbm_gbs"], "regime": regime,
                        "bytes_per_launch": nbytes,
                        "l2": "flushed before each rep (512 MiB written, then read back)",
                        "dirty_l2_GB_per_s": nbytes / (ms_dirty / 1e3) / 1e9,
@@ -603,6 +664,14 @@ def main():
         fp8 = None
         if not args.no_fp8 and rank == 0:
             fp8 = time_fp8(fa, w, dev, 50, peaks, clocks)
+        configs = None
+        if not args.no_configs and rank == 0:
+            configs = {}
+            for name, wc in workloads.WORKLOADS.items():
+                if name == w.name:
+                    continue
+                configs[name] = time_config(fa, wc, dev, 500 if wc.dtype == "f32" else 30,
+                                            peaks, clocks)
     finally:
         clk = clocks.stop()
     e2e = None
@@ -631,6 +700,7 @@ def main():
         "splitkv": splitkv,
         "bwd": bwd,
         "fp8": fp8,
+        "configs": configs,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -22,6 +22,11 @@
  *     reported by fa_get_device_error.
  *   - A negative return value means nothing was launched.
  *   - The library is thread-compatible: the stream setting is per host thread.
+ *   - Per-device state (the device error word's address, the static scratch
+ *     array's address, the helper streams of fa_attention_fwd_host) is looked
+ *     up once per device and kept for the life of the process.  A device reset
+ *     (cudaDeviceReset) or the destruction of the primary context invalidates
+ *     it: after either, make no further call into the library in that process.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -216,9 +221,12 @@ FA_API int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d);
  * copies of the others.  Every operation is ordered after the work already on
  * the library stream, and the library stream waits for the last copy: the
  * call is asynchronous like the others, and O and lse are complete once the
- * library stream has been synchronised.  The helper streams and events are
- * created once per device; concurrent calls from several threads must not
- * overlap.
+ * library stream has been synchronised.  Every argument is checked before
+ * anything is enqueued; if a CUDA call fails after copies were enqueued, the
+ * library stream is still made to wait for them before the error returns, so
+ * synchronising it before freeing Q, K, V suffices on every path.  The helper
+ * streams and events are created once per device; concurrent calls from
+ * several threads must not overlap.
  * Errors: FA_ERR_NULL_POINTER, FA_ERR_BAD_SIZE (also a workspace that is too
  * small), FA_ERR_UNSUPPORTED (d), FA_ERR_MISALIGNED (workspace), FA_ERR_TOO_LARGE,
  * FA_ERR_NO_DEVICE, FA_ERR_CUDA.
@@ -278,9 +286,9 @@ FA_API int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
  * different streams) race on it and may return wrong results.  Calls on one
  * stream run in order and are safe.
  *
- * Errors: as fa_attention_fwd_splitkv (except FA_ERR_NULL_POINTER for
- * scratch), FA_ERR_SCRATCH_LIMIT as above, FA_ERR_CUDA if the array's address
- * cannot be looked up.
+ * Errors: as fa_attention_fwd_splitkv, in the same order (except
+ * FA_ERR_NULL_POINTER for scratch), then FA_ERR_SCRATCH_LIMIT as above, and
+ * FA_ERR_CUDA if the array's address cannot be looked up.
  */
 FA_API int fa_attention_fwd_splitkv_noalloc(const void *Q, const void *K, const void *V, void *O,
                                             float *lse, int B, int H, int Nq, int Nk, int d,

@@ -27,6 +27,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libfa.so")
 
 FA_OK = 0
+FA_ERR_NULL_POINTER = -1
+FA_ERR_BAD_SIZE = -2
+FA_ERR_UNSUPPORTED = -3
+FA_ERR_MISALIGNED = -4
+FA_ERR_CUDA = -5
+FA_ERR_TOO_LARGE = -6
+FA_ERR_NO_DEVICE = -7
 FA_DEVERR_WAIT_TIMEOUT = 0x1
 FA_DEVERR_BAD_SEQLENS = 0x2
 FA_ERR_SCRATCH_LIMIT = -8

@@ -516,9 +516,32 @@ int fa_attention_fwd_host(const void *Q, const void *K, const void *V, void *O, 
     const size_t row = size_t(H) * d * 2, lse_row = size_t(H) * N * 4;
     const cudaStream_t s_main = fa::t_stream;
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // Every group's arguments are checked before anything is enqueued.
+    fa::AttnArgs args[fa::kHostGroups];
+    for (int g = 0, h0 = 0; g < n_groups; h0 += sizes[g], ++g) {
+        const size_t off = size_t(h0) * d * 2;
+        const int rc = fa::check_attention(dq + off, dk + off, dv + off, dout + off,
+                                           dl + size_t(h0) * N, B, sizes[g], N, d, causal,
+                                           nullptr, total, true, &args[g]);
+        if (rc != FA_OK)
+            return rc;
+        args[g].H_row = H;
+        args[g].scale = scale;
+        args[g].err_word = dev->err_word;
+    }
+    // On a failure after the first copy is enqueued, the library stream still
+    // waits for both helper streams, so the copies that read the caller's
+    // host buffers are ordered before anything the caller synchronises on.
+    auto join_and_fail = [&](int rc) {
+        if (cudaEventRecord(pp->done, pp->s_in) == cudaSuccess)
+            cudaStreamWaitEvent(s_main, pp->done, 0);
+        if (cudaEventRecord(pp->done, pp->s_out) == cudaSuccess)
+            cudaStreamWaitEvent(s_main, pp->done, 0);
+        return rc;
+    };
     if (!ok(cudaEventRecord(pp->start, s_main)) || !ok(cudaStreamWaitEvent(pp->s_in, pp->start, 0)) ||
         !ok(cudaStreamWaitEvent(pp->s_out, pp->start, 0)))
-        return FA_ERR_CUDA;
+        return join_and_fail(FA_ERR_CUDA);
     for (int g = 0, h0 = 0; g < n_groups; h0 += sizes[g], ++g) {
         const int hn = sizes[g];
         const size_t off = size_t(h0) * d * 2, width = size_t(hn) * d * 2;
@@ -530,18 +553,10 @@ int fa_attention_fwd_host(const void *Q, const void *K, const void *V, void *O, 
                                   cudaMemcpyHostToDevice, pp->s_in)) ||
             !ok(cudaEventRecord(pp->in[g], pp->s_in)) ||
             !ok(cudaStreamWaitEvent(s_main, pp->in[g], 0)))
-            return FA_ERR_CUDA;
-        fa::AttnArgs a;
-        int rc = fa::check_attention(dq + off, dk + off, dv + off, dout + off, dl + size_t(h0) * N,
-                                     B, hn, N, d, causal, nullptr, total, true, &a);
+            return join_and_fail(FA_ERR_CUDA);
+        const int rc = fa::launch_attention_bf16(args[g], s_main);
         if (rc != FA_OK)
-            return rc;
-        a.H_row = H;
-        a.scale = scale;
-        a.err_word = dev->err_word;
-        rc = fa::launch_attention_bf16(a, s_main);
-        if (rc != FA_OK)
-            return rc;
+            return join_and_fail(rc);
         if (!ok(cudaEventRecord(pp->comp[g], s_main)) ||
             !ok(cudaStreamWaitEvent(pp->s_out, pp->comp[g], 0)) ||
             !ok(cudaMemcpy2DAsync(ho + off, row, dout + off, row, width, size_t(total),
@@ -549,10 +564,10 @@ int fa_attention_fwd_host(const void *Q, const void *K, const void *V, void *O, 
             !ok(cudaMemcpy2DAsync(lse + size_t(h0) * N, lse_row, dl + size_t(h0) * N, lse_row,
                                   size_t(hn) * N * 4, size_t(B), cudaMemcpyDeviceToHost,
                                   pp->s_out)))
-            return FA_ERR_CUDA;
+            return join_and_fail(FA_ERR_CUDA);
     }
     if (!ok(cudaEventRecord(pp->done, pp->s_out)) || !ok(cudaStreamWaitEvent(s_main, pp->done, 0)))
-        return FA_ERR_CUDA;
+        return join_and_fail(FA_ERR_CUDA);
     return FA_OK;
 }
 

@@ -73,6 +73,26 @@ extern "C" int fa_attention_fwd_splitkv_noalloc(const void *Q, const void *K, co
     if (splits > n_kv)
         splits = n_kv;
 
+    // Malformed pointers and sizes the kernels cannot index are reported as
+    // fa_attention_fwd_splitkv reports them, before the scratch size is
+    // looked at: a call that is both malformed and too big for the array
+    // gets the same answer from both functions.
+    // (The checks run in fa_attention_fwd_splitkv's order.)
+    const int64_t total_q = int64_t(B) * Nq, total_k = int64_t(B) * Nk;
+    const int64_t index_limit = (int64_t(1) << 31) - 512;
+    if (total_k > index_limit || int64_t(Nk) > index_limit)
+        return FA_ERR_TOO_LARGE;
+    if (!Q || !K || !V || !O || !lse)
+        return FA_ERR_NULL_POINTER;
+    const auto aligned = [](const void *p, uintptr_t a) {
+        return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+    };
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        !aligned(lse, 4))
+        return FA_ERR_MISALIGNED;
+    if (total_q > index_limit || total_q * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+        return FA_ERR_TOO_LARGE;
+
     float *O_accum = nullptr, *lse_accum = nullptr;
     if (splits > 1) {
         // splits * (B * Nq * H) * (d + 1) floats must fit in the array; checked

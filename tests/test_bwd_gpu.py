@@ -10,7 +10,8 @@ use them and the gradients to bf16 at the end (unit roundoff u = 2^-9 each);
 D_i uses the bf16 O.  Each gradient element is a sum of terms rounded with
 relative error <= u, so its error is at most ~2u times the sum of the terms'
 magnitudes, which for these inputs stays within a few times the largest
-gradient magnitude: BWD_TOL = 2^-5 (8u).
+gradient magnitude: BWD_TOL = 2^-6 (8u).  Observed: 0.002-0.005 on the small
+shapes, <= 0.011 on the full-size rows.
 """
 import math
 
@@ -24,7 +25,7 @@ from gpu_common import device_error_clear, require_gpu
 
 pytestmark = pytest.mark.gpu
 
-BWD_TOL = 2.0 ** -5
+BWD_TOL = 2.0 ** -6
 
 
 @pytest.fixture(scope="module")

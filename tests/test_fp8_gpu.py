@@ -96,24 +96,33 @@ def test_fp8_quantisation_matches_reference(dev, B, H, N, causal):
     _, _, ws = run((Q, K, V), signs, causal, dev)
     L = layout(B, H, N, d)
     for name, X, off, soff in (("Q", Q, L["qf"], L["sq"]), ("K", K, L["kf"], L["sk"])):
+        # the reference's codes come from its own float64 rotation and scales
         Xr = fp8.rotate(X.float().numpy(), signs)
         _, ref_scales = fp8.blockwise_qk(Xr)
         got_scales = ws[soff:soff + B * H * L["T"] * 4].view(np.float32).reshape(B, H, L["T"])
-        assert np.allclose(got_scales, ref_scales, rtol=1e-5), name
+        assert np.allclose(got_scales, ref_scales, rtol=1e-5), name + " scales"
         codes = ws[off:off + B * N * H * d].reshape(B, N, H, d)
-        ref = fp8.e4m3_round(Xr / np.repeat(got_scales, 128, axis=2)[:, :, :N].transpose(0, 2, 1)[..., None])
-        assert_codes_match(codes, ref, name)
+        per_row = np.repeat(ref_scales, 128, axis=2)[:, :, :N].transpose(0, 2, 1)[..., None]
+        assert_codes_match(codes, fp8.e4m3_round(Xr / per_row), name)
     # V': one scale per (sequence, head), codes transposed to [B, H, d, n_pad],
-    # zero codes past N; the codes decided in float32 on both sides, so they
-    # are compared exactly
-    ref, ref_sv = fp8.per_head_v_fp32(V.float().numpy())
-    got_sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H)
-    assert np.array_equal(got_sv, ref_sv)
+    # zero codes past N
     n_pad = 128 * L["T"]
     codes = ws[L["vt"]:L["vt"] + B * H * d * n_pad].reshape(B, H, d, n_pad)
     assert not np.any(codes[..., N:]), "padding keys must hold zero codes"
-    got = e4m3_decode(np.ascontiguousarray(codes[..., :N]))
-    assert np.array_equal(got, ref.transpose(0, 2, 3, 1)), "V' codes"
+    got_codes = np.ascontiguousarray(codes[..., :N].transpose(0, 3, 1, 2))   # [B, N, H, d]
+    got_sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H)
+    # (1) against the float64 method (scale amax / 448 and the quotient in
+    # float64): only neighbouring codes where the quotient falls within
+    # float32 rounding of a half-way point
+    Vf = V.float().numpy()
+    _, sv64 = fp8.per_head_v(Vf)
+    assert np.allclose(got_sv, sv64, rtol=1e-7), "sv against the float64 method"
+    assert_codes_match(got_codes, fp8.e4m3_round(Vf / sv64[:, None, :, None]), "V (float64)")
+    # (2) against the same method with the decision taken in float32, as the
+    # kernel takes it: equal, code for code
+    ref, ref_sv = fp8.per_head_v_fp32(Vf)
+    assert np.array_equal(got_sv, ref_sv)
+    assert np.array_equal(e4m3_decode(got_codes), ref), "V' codes (float32 decision)"
 
 
 @pytest.mark.parametrize("B,H,N,causal", [(1, 2, 256, False), (2, 2, 512, True), (1, 3, 300, True),
@@ -135,37 +144,56 @@ def test_fp8_matches_reference(dev, B, H, N, causal):
     device_error_clear()
 
 
-def test_fp8_full_size_sampled(dev):
+def check_against_reference(O, lse, qkv, signs, causal, label):
+    """O and lse of every (token, head) row against the reference (the float64
+    rotation and blockwise quantisation, then the fp64 oracle on the
+    dequantised inputs).
+
+    O: RMSE <= FP8_O_RMSE and max <= 2^-4 max|V| (P rounded to e4m3).
+    lse: the kernel rotates in fp32 (tensor-core summation order), so at most
+    1e-3 of its Q', K' codes (observed ~1e-7) are the neighbour of the
+    reference's.  A score moves by at most scale * sum_k |dq'_k k'_k| +
+    |q'_k dk'_k| and lse, 1-Lipschitz in the largest score change, as much;
+    with every code one step off (a step is at most 2^-3 (1 + 2^-3) of the
+    value) that is bound_i = 2^-2 (1 + 2^-3) scale sum_k |q'_ik| max_j |k'_jk|.
+    So lse is held to FP8_LSE_MAX on all but 1e-4 of the rows and every row to
+    max(bound_i, FP8_LSE_MAX): a grid, tile or scale slip misplaces whole
+    tiles or heads and fails one of the three."""
+    Q, K, V = (t.float().numpy() for t in qkv)
+    B, N, H, d = Q.shape
+    scale = 1 / math.sqrt(d)
+    Qd, Kd, Vd = fp8.fp8_inputs(Q, K, V, signs)
+    Or, lr = oracle.attention_dense(Qd.astype(np.float32), Kd.astype(np.float32),
+                                    Vd.astype(np.float32), scale, causal)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(lse))
+    rmse = float(np.sqrt(np.mean((O - Or) ** 2)))
+    mx = float(np.abs(O - Or).max())
+    err_l = np.abs(lse - lr)                                            # [B, H, N]
+    kmax = np.abs(Kd).max(axis=1)                                       # [B, H, d]
+    bound = 2.0 ** -2 * (1 + 2.0 ** -3) * scale * np.einsum("bnhk,bhk->bhn", np.abs(Qd), kmax)
+    frac_off = float(np.mean(err_l > FP8_LSE_MAX))
+    print(f"{label}: all {O.size // d} rows; O rmse {rmse:.2e} max {mx:.2e}; lse max "
+          f"{err_l.max():.2e}, {frac_off:.2e} of rows above {FP8_LSE_MAX}")
+    assert rmse <= FP8_O_RMSE and mx <= 2.0 ** -4 * float(np.abs(V).max())
+    assert frac_off <= 1e-4
+    assert np.all(err_l <= np.maximum(bound, FP8_LSE_MAX))
+
+
+def test_fp8_full_size(dev):
     """The benchmark's FP8 launch (causal B=2 H=32 N=4096 d=128): every tile
-    scale of Q M and K M against the reference's, and O and lse on sampled
-    (token, head) rows against the reference attention on the dequantised
-    inputs (the reference row by row: the oracle's per-row attention)."""
-    import workloads
+    scale of Q M and K M against the reference's, and O and lse of every
+    (token, head) row against the reference attention on the dequantised
+    inputs."""
     B, H, N, d = 2, 32, 4096, 128
     qkv, signs = make(B, H, N, d, seed=4096)
     O, lse, ws = run(qkv, signs, True, dev)
-    assert np.all(np.isfinite(O)) and np.all(np.isfinite(lse))
-    Q, K, V = (t.float().numpy() for t in qkv)
+    device_error_clear()
     L = layout(B, H, N, d)
-    for name, X, soff in (("Q", Q, L["sq"]), ("K", K, L["sk"])):
-        _, ref_scales = fp8.blockwise_qk(fp8.rotate(X, signs))
+    for name, X, soff in (("Q", qkv[0], L["sq"]), ("K", qkv[1], L["sk"])):
+        _, ref_scales = fp8.blockwise_qk(fp8.rotate(X.float().numpy(), signs))
         got = ws[soff:soff + B * H * L["T"] * 4].view(np.float32).reshape(B, H, L["T"])
         assert np.allclose(got, ref_scales, rtol=1e-5), name
-    Qd, Kd, Vd = (x.reshape(B * N, H, d).astype(np.float32) for x in fp8.fp8_inputs(Q, K, V, signs))
-    must = list(range(0, 130)) + list(range(N - 130, N + 130)) + list(range(B * N - 130, B * N))
-    tok, head = workloads.sample_rows(B * N, H, 2000, seed=4097)
-    tok = np.concatenate([tok, np.asarray(must, np.int64)])
-    head = np.concatenate([head, np.asarray(must, np.int64) % H])
-    cu = np.arange(B + 1, dtype=np.int32) * N
-    Or, lr = oracle.attention_rows(Qd, Kd, Vd, cu, 1 / math.sqrt(d), True, tok, head)
-    Op = O.reshape(B * N, H, d)[tok, head]
-    lp = lse.transpose(1, 0, 2).reshape(H, B * N)[head, tok]
-    rmse = float(np.sqrt(np.mean((Op - Or) ** 2)))
-    mx = float(np.abs(Op - Or).max())
-    print(f"full size: rmse {rmse:.2e} max {mx:.2e} lse {np.abs(lp - lr).max():.2e}")
-    assert rmse <= FP8_O_RMSE and mx <= 2.0 ** -4 * float(np.abs(V).max())
-    assert float(np.abs(lp - lr).max()) <= FP8_LSE_MAX
-    device_error_clear()
+    check_against_reference(O, lse, qkv, signs, True, "full size")
 
 
 def test_fp8_outliers_pages_experiment(dev):
@@ -184,43 +212,17 @@ def test_fp8_outliers_pages_experiment(dev):
     assert rmse < 1.5e-2 and rmse < rmse_b
 
 
-def dequantised_from_workspace(ws, B, H, N, d):
-    """Q', K', V' as the kernels quantised them (codes times scales, float32),
-    read back from the workspace."""
-    L = layout(B, H, N, d)
-    T = L["T"]
-    e = B * N * H * d
-
-    def tile_scaled(off, soff):
-        codes = e4m3_decode(ws[off:off + e]).reshape(B, N, H, d)
-        sc = ws[soff:soff + B * H * T * 4].view(np.float32).reshape(B, H, T).astype(np.float64)
-        return codes * np.repeat(sc, 128, axis=2)[:, :, :N].transpose(0, 2, 1)[..., None]
-
-    Qd = tile_scaled(L["qf"], L["sq"])
-    Kd = tile_scaled(L["kf"], L["sk"])
-    vt = ws[L["vt"]:L["vt"] + B * H * d * 128 * T].reshape(B, H, d, 128 * T)
-    sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H).astype(np.float64)
-    Vd = e4m3_decode(np.ascontiguousarray(vt[..., :N])) * sv[:, :, None, None]
-    return (Qd.astype(np.float32), Kd.astype(np.float32),
-            np.ascontiguousarray(Vd.transpose(0, 3, 1, 2)).astype(np.float32))
-
-
 def test_fp8_many_heads(dev):
     """More sequence-heads than a grid's y dimension holds (65535): the
-    quantisation and attention grids take them along x.  The attention is
-    checked on the codes the kernels produced (a few of 34 M codes may be
-    the neighbour of the float64 method's, which moves a one-key row's lse
-    by ~1e-2; the codes themselves are checked by the quantisation test)."""
+    quantisation and attention grids take them along x.  Every row against
+    the reference; a one-key row's lse is its single score, which a
+    neighbouring Q' or K' code moves by up to ~1e-2 (the bound in
+    check_against_reference)."""
     B, H, N, d = 1, 66000, 2, 128
     qkv, signs = make(B, H, N, d, seed=66)
-    O, lse, ws = run(qkv, signs, True, dev)
-    Qd, Kd, Vd = dequantised_from_workspace(ws, B, H, N, d)
-    Or, lr = oracle.attention_dense(Qd, Kd, Vd, 1 / math.sqrt(d), True)
-    rmse = float(np.sqrt(np.mean((O - Or) ** 2)))
-    V = qkv[2].float().numpy()
-    assert rmse <= FP8_O_RMSE and float(np.abs(O - Or).max()) <= 2.0 ** -4 * float(np.abs(V).max())
-    assert float(np.abs(lse - lr).max()) <= FP8_LSE_MAX
+    O, lse, _ = run(qkv, signs, True, dev)
     device_error_clear()
+    check_against_reference(O, lse, qkv, signs, True, "many heads")
 
 
 def test_fp8_bad_arguments(dev):

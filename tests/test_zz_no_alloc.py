@@ -1,6 +1,10 @@
 """fa_attention_fwd_splitkv_noalloc (split-KV attention on the library's static
 scratch array) against fa_attention_fwd_splitkv with caller-owned scratch,
-through the C ABI.
+through the C ABI.  Both run the same kernels on the same inputs with the same
+split count, so their results must be equal bit for bit; each case is also
+checked against the fp64 oracle (bottom-right causal alignment), so a carve-up
+of the array that lands the partials in the wrong place fails even where it
+stays close to the caller-scratch result.
 
 The file name sorts last so that pytest collects it after every other test:
 the static array must give correct results both in a fresh process and after
@@ -12,8 +16,10 @@ import pytest
 import torch
 
 import online_softmax_06_gb300 as fa
+import oracle
 import workloads
-from gpu_common import ATTN_BF16_LSE_TOL, ATTN_BF16_O_TOL, device_error_clear, require_gpu
+from gpu_common import (ATTN_BF16_LSE_TOL, ATTN_BF16_O_TOL, device_error_clear, max_abs,
+                        require_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +47,15 @@ def call_noalloc(q, k, v, causal, splits):
     return rc, o, lse
 
 
-def close(a, b, tol):
-    return float((a.float() - b.float()).abs().max()) <= tol
+def assert_oracle(q, k, v, causal, o, lse):
+    """Every row of O and lse against the oracle on the same bf16 inputs."""
+    d = q.shape[3]
+    Or, lr = oracle.attention_qk(q.float().cpu().numpy(), k.float().cpu().numpy(),
+                                 v.float().cpu().numpy(), 1 / math.sqrt(d), causal)
+    err_o = max_abs(o.float().cpu().numpy(), Or)
+    err_l = max_abs(lse.cpu().numpy(), lr)
+    print(f"no-alloc {tuple(q.shape)} keys {k.shape[1]}: O err {err_o:.3e}, lse err {err_l:.3e}")
+    assert err_o <= ATTN_BF16_O_TOL and err_l <= ATTN_BF16_LSE_TOL
 
 
 def test_noalloc_two_calls_match_caller_scratch(dev):
@@ -65,8 +78,8 @@ def test_noalloc_two_calls_match_caller_scratch(dev):
     for ((q, k, v), causal, s), (o, lse) in zip(data, results):
         o_ref, lse_ref = fa.attention_fwd_splitkv(q, k, v, causal=causal, num_splits=s)
         torch.cuda.synchronize(dev)
-        assert close(o, o_ref, ATTN_BF16_O_TOL)
-        assert close(lse, lse_ref, ATTN_BF16_LSE_TOL)
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+        assert_oracle(q, k, v, causal, o, lse)
 
 
 def test_noalloc_scratch_limit(dev):
@@ -80,7 +93,7 @@ def test_noalloc_scratch_limit(dev):
     assert rc == 0, fa.strerror(rc)
     o_ref, lse_ref = fa.attention_fwd_splitkv(q, k, v, causal=False, num_splits=splits)
     torch.cuda.synchronize(dev)
-    assert close(o, o_ref, ATTN_BF16_O_TOL) and close(lse, lse_ref, ATTN_BF16_LSE_TOL)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
     q2 = torch.cat([q, q[:, :1]], dim=1).contiguous()
     o2 = torch.full_like(q2, 7.0)
@@ -111,3 +124,12 @@ def test_noalloc_argument_errors_match(dev):
         b = fa.fa_attention_fwd_splitkv(p, k.data_ptr(), k.data_ptr(), p, lse.data_ptr(),
                                         *args, None, None)
         assert a == b < 0
+    # a malformed call that would also exceed the scratch reports the
+    # malformation first, as fa_attention_fwd_splitkv does: a NULL Q, then a
+    # misaligned O, at 64 splits of 4096 queries (64 * 4096 * 65 * 4 bytes)
+    big = (1, 1, 4096, 8192, 64, 0.125, 0, 64)
+    kp = k.data_ptr()
+    for qp, op_, want in ((None, p, fa.FA_ERR_NULL_POINTER), (p, p + 2, fa.FA_ERR_MISALIGNED)):
+        a = fa.fa_attention_fwd_splitkv_noalloc(qp, kp, kp, op_, lse.data_ptr(), *big)
+        b = fa.fa_attention_fwd_splitkv(qp, kp, kp, op_, lse.data_ptr(), *big, p, lse.data_ptr())
+        assert a == b == want
