@@ -159,13 +159,31 @@ FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V,
  *   contents on entry are ignored).
  *   d: 64 or 128; bf16 pointers 16-byte aligned, lse and D_buf 4-byte aligned.
  * Two kernels run on the library stream (dQ and D, then dK and dV); no
- * synchronisation.  Packed (cu_seqlens) batches are not supported here.
+ * synchronisation.  Packed batches: fa_attention_bwd_varlen.
  * Errors: FA_ERR_NULL_POINTER, FA_ERR_BAD_SIZE, FA_ERR_UNSUPPORTED (d),
  * FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE, FA_ERR_NO_DEVICE, FA_ERR_CUDA.
  */
 FA_API int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O,
                             const void *dO, const float *lse, void *dQ, void *dK, void *dV,
                             float *D_buf, int B, int H, int N, int d, float scale, int causal);
+
+/*
+ * fa_attention_bwd for packed sequences ("第二十二课…" §三十五: a batch of
+ * variable-length sequences stored one after another, none attending to
+ * another): each sequence's gradients are those of its own attention.
+ *   Q, K, V, O, dO, dQ, dK, dV: bf16 [total, H, d]; lse and D_buf: fp32
+ *   [H, total] (the layout fa_attention_fwd writes lse in for packed
+ *   batches); cu_seqlens: DEVICE int32 [B + 1], non-decreasing, from 0 to
+ *   total; N: the longest sequence (an upper bound is fine); total: the
+ *   packed row count (= cu_seqlens[B]; nothing is read back, no
+ *   synchronisation).  A sequence longer than N is not computed and sets
+ *   FA_DEVERR_BAD_SEQLENS in the device error word.
+ * Errors: as fa_attention_bwd, and FA_ERR_NULL_POINTER for a NULL cu_seqlens.
+ */
+FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, const void *O,
+                                   const void *dO, const float *lse, void *dQ, void *dK,
+                                   void *dV, float *D_buf, int B, int H, int N, int64_t total,
+                                   int d, float scale, int causal, const int32_t *cu_seqlens);
 
 /*
  * FP8 attention forward ("少搬一趟…" §4.6: FP8 with blockwise quantisation and
@@ -311,6 +329,23 @@ FA_API int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, 
  * library does not take ownership.  Returns FA_OK.
  */
 FA_API int fa_set_stream(void *stream);
+
+/*
+ * Failure detection, for tests: arms a wait that cannot complete in the next
+ * bf16 attention forward (fa_attention_fwd / fa_attention_fwd_varlen) launched
+ * from this host thread.  In that launch the warp that issues the tensor-core
+ * instructions first waits, bounded by `ns` nanoseconds, on a barrier that
+ * nothing arrives at.  The wait runs out, sets FA_DEVERR_WAIT_TIMEOUT in the
+ * device error word and raises the CTA's abort flag, and every CTA winds down
+ * the way it does after any timed-out wait: the other roles leave their loops,
+ * copies already issued are waited for, tensor memory is freed, and O and lse
+ * are left unwritten.  The launch returns FA_OK; the error shows in
+ * fa_get_device_error.  One-shot: the setting is consumed by that launch.  The
+ * kernels' own waits keep their bound (2 s), so the device stays usable and the
+ * next call runs normally.  ns: 1 .. 10^9 arms, 0 disarms.
+ * Errors: FA_ERR_BAD_SIZE (ns < 0 or > 10^9).
+ */
+FA_API int fa_debug_expire_next_wait(int64_t ns);
 
 /* The stream currently selected for this host thread. */
 FA_API void *fa_get_stream(void);

@@ -9,11 +9,12 @@ compiled library is missing, importing the C functions fails loudly.
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
-``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_fwd_fp8``,
+``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_bwd_varlen``,
+``fa_attention_fwd_fp8``,
 ``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
 ``fa_attention_host_workspace_bytes``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
-``fa_version``.
+``fa_version``, ``fa_debug_expire_next_wait``.
 Tensor-level helpers: :func:`softmax_rows`, :func:`attention_fwd`,
 :func:`attention_fwd_splitkv`, :func:`attention_bwd`, :func:`attention_fwd_fp8`.
 """
@@ -81,6 +82,8 @@ def lib():
         L.fa_attention_host_workspace_bytes.restype = i64
         L.fa_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                        i32, f32, i32]
+        L.fa_attention_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                              i32, i64, i32, f32, i32, vp]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                        i32, f32, i32, i32]
         L.fa_set_stream.argtypes = [vp]
@@ -90,11 +93,14 @@ def lib():
         L.fa_strerror.argtypes = [i32]
         L.fa_strerror.restype = ctypes.c_char_p
         L.fa_version.argtypes = []
+        L.fa_debug_expire_next_wait.argtypes = [i64]
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
-                     "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd", "fa_attention_fwd_fp8",
+                     "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
+                     "fa_attention_bwd_varlen", "fa_attention_fwd_fp8",
                      "fa_attention_fwd_host",
-                     "fa_set_stream", "fa_get_device_error", "fa_version"):
+                     "fa_set_stream", "fa_get_device_error", "fa_version",
+                     "fa_debug_expire_next_wait"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -173,6 +179,12 @@ def fa_attention_bwd(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale, 
                                   causal)
 
 
+def fa_attention_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, total, d, scale,
+                            causal, cu_seqlens) -> int:
+    return lib().fa_attention_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, total,
+                                         d, scale, causal, cu_seqlens)
+
+
 def fa_set_stream(stream_ptr) -> int:
     return lib().fa_set_stream(stream_ptr)
 
@@ -187,6 +199,10 @@ def fa_get_device_error() -> int:
 
 def fa_version() -> int:
     return lib().fa_version()
+
+
+def fa_debug_expire_next_wait(ns: int) -> int:
+    return lib().fa_debug_expire_next_wait(ns)
 
 
 # ---- tensor-level helpers -------------------------------------------------------
@@ -385,11 +401,14 @@ def attention_fwd_host(q, k, v, causal: bool = False, scale: float | None = None
     return o, lse, workspace
 
 
-def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None):
-    """Attention backward through the C ABI (bf16, dense [B, N, H, d]).
+def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+                  cu_seqlens=None, max_seqlen: int | None = None):
+    """Attention backward through the C ABI (bf16).
 
+    Dense: q, k, v, o, do [B, N, H, d], lse [B, H, N].  Packed: [total, H, d]
+    with ``cu_seqlens`` (int32 CUDA [B+1]) and ``max_seqlen``, lse [H, total].
     ``o`` and ``lse`` are the forward's outputs for the same inputs.  The fp32
-    D scratch [B, H, N] is allocated here (torch).  Returns (dq, dk, dv).
+    D scratch (lse's shape) is allocated here (torch).  Returns (dq, dk, dv).
     """
     import torch
     for t in (q, k, v, o, do):
@@ -397,19 +416,33 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
             raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors")
         if t.shape != q.shape:
             raise ValueError("q, k, v, o, do must have one shape")
-    B, N, H, d = q.shape
-    if not (lse.is_cuda and lse.dtype == torch.float32 and lse.shape == (B, H, N)
+    if cu_seqlens is None:
+        B, N, H, d = q.shape
+        lse_shape = (B, H, N)
+    else:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        tot, H, d = q.shape
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen) if max_seqlen is not None else tot
+        lse_shape = (H, tot)
+    if not (lse.is_cuda and lse.dtype == torch.float32 and tuple(lse.shape) == lse_shape
             and lse.is_contiguous()):
-        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, H, N]")
+        raise ValueError(f"lse must be a contiguous float32 CUDA tensor {list(lse_shape)}")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     _use_current_stream(q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    d_buf = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = fa_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                          _ptr(dk), _ptr(dv), _ptr(d_buf), B, H, N, d, float(scale),
-                          int(bool(causal)))
-    _check(rc, "fa_attention_bwd")
+    d_buf = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(d_buf))
+    if cu_seqlens is None:
+        rc = fa_attention_bwd(*ptrs, B, H, N, d, float(scale), int(bool(causal)))
+        _check(rc, "fa_attention_bwd")
+    else:
+        rc = fa_attention_bwd_varlen(*ptrs, B, H, N, q.shape[0], d, float(scale),
+                                     int(bool(causal)), _ptr(cu_seqlens))
+        _check(rc, "fa_attention_bwd_varlen")
     return dq, dk, dv
 
 
@@ -417,9 +450,10 @@ __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
     "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
-    "attention_bwd", "fa_attention_bwd", "attention_fwd_fp8", "fa_attention_fwd_fp8",
+    "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "attention_fwd_fp8",
+    "fa_attention_fwd_fp8",
     "fa_attention_fp8_workspace_bytes",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",
-    "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS",
+    "FA_DEVERR_WAIT_TIMEOUT", "FA_DEVERR_BAD_SEQLENS", "fa_debug_expire_next_wait",
 ]

@@ -84,7 +84,7 @@ struct Cfg {
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffRing = 2 * kQBytes;
     static constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
-    static constexpr uint32_t kBarBytes = 8 * (2 + 2 * kStages + 2 + 2 + 2 + 1);
+    static constexpr uint32_t kBarBytes = 8 * (2 + 2 * kStages + 2 + 2 + 2 + 1 + 1);
     static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 16 + 1024;  // +1024 align slack
 };
 
@@ -110,10 +110,12 @@ struct Bf16Params {
     float *lse_accum;                // splits > 1: [splits, B, H, N] fp32 partial lse
     const int32_t *cu_seqlens;
     int *err_word;
+    uint32_t expire_wait_ns;         // failure-detection test only (0: off)
 };
 
 struct Barriers {
     uint64_t *q_full, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *drain;
+    uint64_t *never;                 // nothing arrives: the failure-detection test waits here
 };
 
 // Bounded wait used only while draining after an abort: ignores the abort flag.
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar.p_full = bar.s_full + 2;
     bar.o_full = bar.p_full + 2;
     bar.drain = bar.o_full + 2;
+    bar.never = bar.drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + (C::kBarBytes / 8));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&bar.o_full[t], 1);
         }
         ptx::mbar_init(bar.drain, 1);
+        ptx::mbar_init(bar.never, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -399,7 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
-            do {
+            // Failure-detection test: a wait on a barrier that nothing arrives
+            // at runs out after expire_wait_ns; it raises the error bit and the
+            // abort flag, and the CTA winds down as after any timed-out wait.
+            if (p.expire_wait_ns != 0u &&
+                !__all_sync(0xffffffffu, ptx::mbar_wait_limited(bar.never, 0, abort_flag,
+                                                                p.err_word, p.expire_wait_ns)))
+                aborted = true;
+
+            if (aborted) {
+                // nothing issued: go straight to the drain below
+            } else do {
                 uint64_t k_desc, unused;
                 if (!next_stage(k_desc, unused)) {
                     aborted = true;
@@ -495,7 +509,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (FP8)                             // dequantise Q' K'^T: x sq sk
             sl *= p.sq[(int64_t(b) * p.H + h) * p.n_tiles + qt];
         float m = -INFINITY;                           // reference max, log2 units
-        float l = 0.f;                                 // running sum
+        float l = 0.f;                                 // running sum (lse)
+        // The running sum that divides O: l plus, per tile, the bf16 rounding
+        // error of the tile's largest probability.  Under the conditional
+        // rescale that probability is 2^(tile max - m), up to 2^8, not 1, and
+        // its rounding (up to 2^-8 relative) enters P V; adding it here keeps
+        // O a weighted mean of V rows for a row dominated by one key.
+        float l_o = 0.f;
 
         for (int j = 0; j < n_t; ++j) {
             if (!ptx::mbar_wait(&bar.s_full[t], uint32_t(j) & 1u, abort_flag, p.err_word)) {
@@ -560,8 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float corr = grew ? ptx::ex2(m - m_use) : 1.f;   // 0 on the first tile
 
-            // P = exp2(s * sl - m) in bf16 over columns 64..127 of S_t; the
-            // exponent arguments are formed two at a time (packed fp32x2 FMA)
+            // P = exp2(s * sl - m) in bf16 into P_t's columns; the exponent
+            // arguments are formed two at a time (packed fp32x2 FMA).
+            const uint32_t tP = tS + kColPinS;
             const float2 sl2 = make_float2(slj, slj);
             const float2 nm2 = make_float2(-m_use, -m_use);
             // the row sum is accumulated two lanes at a time (packed fp32x2 add)
@@ -587,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                              make_float2(p2, p3)));
                     pk[q4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
                 }
-                ptx::tmem_st32(tS + kColPinS, pk);
+                ptx::tmem_st32(tP, pk);
             } else
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -602,9 +623,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rowsum2 = __fadd2_rn(rowsum2, make_float2(p0, p1));
                     pk[e] = ptx::pack_bf16x2(p0, p1);
                 }
-                ptx::tmem_st32(tS + kColPinS + half * 32, pk);
+                ptx::tmem_st32(tP + half * 32, pk);
             }
-            l = l * corr + (rowsum2.x + rowsum2.y);
+            const float tile_sum = rowsum2.x + rowsum2.y;
+            l = l * corr + tile_sum;
+            if constexpr (FP8) {
+                l_o = l;
+            } else {
+                // the tile maximum's probability exactly as the loop formed
+                // it (same fma and ex2), and its bf16 value
+                const float p_top = ptx::ex2(fmaf(mx, slj, -m_use));
+                const float p_top_bf16 = __uint_as_float(ptx::pack_bf16x2(p_top, 0.f) << 16);
+                l_o = l_o * corr + (tile_sum + (p_top_bf16 - p_top));
+            }
             m = m_new;
 
             // rescale this row of O~ when its reference moved (never on the
@@ -637,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after_sync();
                     const bool row_ok = i < L;
                     const bool empty = !(l > 0.f);
-                    const float inv = empty ? 0.f : 1.f / l;
+                    const float inv = empty ? 0.f : 1.f / l_o;
                     __nv_bfloat16 *orow = p.O + ((start + i) * p.H_row + h) * D;
                     float *arow = p.O_accum +
                                   (((int64_t(split) * p.B + b) * p.N + i) * p.H + h) * D;
@@ -696,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok = !aborted && ptx::mbar_wait(&bar.o_full[t], 0, abort_flag, p.err_word);
             if (ok) {
                 ptx::tc_fence_after_sync();
-                const float inv = (FP8 ? p.sv[int64_t(b) * p.H + h] : 1.f) / l;
+                const float inv = (FP8 ? p.sv[int64_t(b) * p.H + h] : 1.f) / l_o;
                 const bool row_ok = i < L;
                 __nv_bfloat16 *orow = p.O + ((start + i) * p.H_row + h) * D;
 #pragma unroll
@@ -770,9 +801,11 @@ int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 {
     auto kern = attn_fwd_bf16_kernel<D, SPLIT>;
     static PerDeviceOnce once;
-    if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern), int(Cfg<D>::kSmemBytes)))
+    constexpr uint32_t smem = Cfg<D>::kSmemBytes;
+    static_assert(smem <= 227 * 1024, "shared memory per CTA");
+    if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern), int(smem)))
         return FA_ERR_CUDA;
-    kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p);
+    kern<<<dim3(unsigned(blocks)), dim3(kThreads), smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -807,6 +840,7 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     p.causal = a.causal;
     p.cu_seqlens = a.cu_seqlens;
     p.err_word = a.err_word;
+    p.expire_wait_ns = a.expire_wait_ns;
     const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H * p.splits;
     if (blocks == 0)
         return FA_OK;
@@ -855,6 +889,7 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     p.causal = a.causal;
     p.cu_seqlens = nullptr;
     p.err_word = a.err_word;
+    p.expire_wait_ns = 0;
     const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H;
     if (blocks == 0)
         return FA_OK;

@@ -118,11 +118,40 @@ struct BwdParams {
     const float *lse;                       // [B, H, N], natural log
     float *D;                               // [B, H, N]
     __nv_bfloat16 *dQ, *dK, *dV;
-    int B, H, N, n_tiles, n_sub;
+    int B, H, N, n_tiles, n_sub;     // N: sequence length (dense) / longest sequence (packed)
     float scale, scale_log2;
     int causal;
     int *err_word;
+    const int32_t *cu_seqlens;       // packed batches: [B + 1] prefix sums (else nullptr)
+    int64_t total;                   // rows of the tensors
 };
+
+// Rows of sequence b: its first row, its length and the index of its first
+// row statistic (lse, D) for head h -- [B, H, N] dense, [H, total] packed.
+// A packed length that contradicts N or the tensors is flagged, not computed.
+struct SeqRows {
+    int64_t row0, stat0;
+    int L;
+};
+__device__ __forceinline__ bool seq_rows(const BwdParams &p, int b, int h, SeqRows &q)
+{
+    if (p.cu_seqlens == nullptr) {
+        q.row0 = int64_t(b) * p.N;
+        q.L = p.N;
+        q.stat0 = (int64_t(b) * p.H + h) * p.N;
+        return true;
+    }
+    const int64_t s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+    if (s0 < 0 || s1 < s0 || s1 > p.total || s1 - s0 > p.N) {
+        if (threadIdx.x == 0)
+            record_device_error(p.err_word, FA_DEVERR_BAD_SEQLENS);
+        return false;
+    }
+    q.row0 = s0;
+    q.L = int(s1 - s0);
+    q.stat0 = int64_t(h) * p.total + s0;
+    return true;
+}
 
 struct Bars {
     uint64_t *a_full, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *drain;
@@ -321,9 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt = p.n_tiles - 1 - int(blockIdx.x) / bh_count;
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
-    const int64_t row0 = int64_t(b) * p.N;          // first row of the sequence
+    SeqRows sq;
+    if (!seq_rows(p, b, h, sq) || qt * BT >= sq.L)
+        return;                                     // whole CTA: nothing to do
+    const int64_t row0 = sq.row0;                   // first row of the sequence
+    const int L = sq.L;
+    const int n_tiles = (L + BT - 1) / BT;
     // 128-key steps this query tile sees (at least one)
-    const int n_kv = p.causal ? min(qt + 1, p.n_tiles) : p.n_tiles;
+    const int n_kv = p.causal ? min(qt + 1, n_tiles) : n_tiles;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -504,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane;        // query row in the tile = TMEM lane
         const int g = warp >> 2;                     // column group
         const int i = qt * BT + r;
-        const bool row_ok = i < p.N;
+        const bool row_ok = i < L;
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
-        const int64_t stat = (int64_t(b) * p.H + h) * p.N + i;
+        const int64_t stat = sq.stat0 + i;
         // D_i = dO_i . O_i (fp32), computed by the row warps together: a warp
         // takes 16 rows, D / 8 lanes per row, each lane 8 elements: O from
         // global memory (whole rows per load instruction), dO from the
@@ -524,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kRowsPerWarp / kRowsPerInst; ++k) {
                 const int rr = warp * kRowsPerWarp + k * kRowsPerInst + sub;
                 const int qi = qt * BT + rr;
-                ov[k] = qi < p.N ? *reinterpret_cast<const uint4 *>(
+                ov[k] = qi < L ? *reinterpret_cast<const uint4 *>(
                                        p.O + ((row0 + qi) * p.H + h) * D + lr * 8)
                                  : make_uint4(0, 0, 0, 0);
             }
@@ -614,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int lim = BT - 1;
             if (p.causal && i - j * BT < lim)
                 lim = i - j * BT;
-            if (p.N - 1 - j * BT < lim)
-                lim = p.N - 1 - j * BT;
+            if (L - 1 - j * BT < lim)
+                lim = L - 1 - j * BT;
             if (!row_ok)
                 lim = -1;
             float pr[kQCols];
@@ -694,10 +728,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kt = int(blockIdx.x) / bh_count;       // causal: low key tiles see most
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
-    const int64_t row0 = int64_t(b) * p.N;
+    SeqRows sq;
+    if (!seq_rows(p, b, h, sq) || kt * BT >= sq.L)
+        return;                                      // whole CTA: nothing to do
+    const int64_t row0 = sq.row0;
+    const int L = sq.L;
+    const int n_sub = (L + BS - 1) / BS;
     // first query sub-tile that sees the keys; at least one sub-tile follows
     const int i0 = p.causal ? 2 * kt : 0;
-    const int n_q = p.n_sub - i0;
+    const int n_q = n_sub - i0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const uint32_t tmem = setup<D>(p, bar, 32u, abort_flag, tmem_slot);
@@ -724,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int stage = 0;
         uint32_t phase = 0;
-        const int64_t stat0 = (int64_t(b) * p.H + h) * p.N;
+        const int64_t stat0 = sq.stat0;
         for (int s = 0; s < n_q; ++s) {
             const int i = i0 + s;
             // the step's statistics: global loads in flight during the slot wait
@@ -732,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < BS / 32; ++u) {
                 const int q = i * BS + lane * (BS / 32) + u;
-                const bool v = q < p.N;
+                const bool v = q < L;
                 ls[u] = v ? p.lse[stat0 + q] : 0.f;
                 ds[u] = v ? p.D[stat0 + q] : 0.f;
             }
@@ -752,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
                                      &bar.kv_full[stage], c * 64, h, row);
                 }
-                if (i + kL2Ahead < p.n_sub)
+                if (i + kL2Ahead < n_sub)
                     for (int c = 0; c < C::kChunks; ++c) {
                         ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
                         ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
@@ -910,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // visible columns [lo, hi]: causal keeps queries >= the key; the
             // sequence ends at N
             const int lo = p.causal ? k - i * BS : 0;
-            int hi = p.N - 1 - i * BS;
+            int hi = L - 1 - i * BS;
             if (hi > BS - 1)
                 hi = BS - 1;
             const uint32_t tS = tmem + lane_bits + uint32_t(s & 1) * kColBuf + col0;
@@ -944,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!aborted && ptx::mbar_wait(bar.o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
-            const bool key_ok = k < p.N;
+            const bool key_ok = k < L;
             // group 0 writes dV, group 1 writes dK
             if (g == 0)
                 store_row(tmem + lane_bits + kColAcc, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
@@ -981,7 +1020,7 @@ int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t st
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
 {
     BwdParams p;
-    const int64_t total = int64_t(a.B) * a.N;
+    const int64_t total = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * a.N;
     p.O = static_cast<const __nv_bfloat16 *>(a.O);
     p.dO = static_cast<const __nv_bfloat16 *>(a.dO);
     p.lse = a.lse;
@@ -998,6 +1037,8 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
     p.err_word = a.err_word;
+    p.cu_seqlens = a.cu_seqlens;
+    p.total = total;
     const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
     if (blocks == 0)
         return FA_OK;

@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 thread_local cudaStream_t t_stream = nullptr;
+// fa_debug_expire_next_wait: armed for the next bf16 forward from this thread
+thread_local uint32_t t_expire_wait_ns = 0;
 
 struct DeviceInfo {
     std::once_flag once;
@@ -128,7 +130,11 @@ int attention_common(const void *Q, const void *K, const void *V, void *O, float
         return FA_OK;
     a.scale = scale;
     a.err_word = dev->err_word;
-    return bf16 ? launch_attention_bf16(a, t_stream) : launch_attention_f32(a, t_stream);
+    if (!bf16)
+        return launch_attention_f32(a, t_stream);
+    a.expire_wait_ns = t_expire_wait_ns;
+    t_expire_wait_ns = 0;
+    return launch_attention_bf16(a, t_stream);
 }
 
 // Workspace of the FP8 forward: e4m3 Q', K' ([B*N, H, d]), the transposed
@@ -348,31 +354,37 @@ int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V, void *
     return fa::launch_attention_bf16(a, fa::t_stream);
 }
 
-int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
-                     const float *lse, void *dQ, void *dK, void *dV, float *D_buf, int B, int H,
-                     int N, int d, float scale, int causal)
+}  // extern "C"
+
+namespace fa {
+namespace {
+// Shared by the dense and packed backward entry points.
+int attention_bwd_common(const void *Q, const void *K, const void *V, const void *O,
+                         const void *dO, const float *lse, void *dQ, void *dK, void *dV,
+                         float *D_buf, int B, int H, int N, int64_t total, int d, float scale,
+                         int causal, const int32_t *cu_seqlens)
 {
-    if (B < 0 || H < 0 || N < 0)
+    if (B < 0 || H < 0 || N < 0 || total < 0)
         return FA_ERR_BAD_SIZE;
     if (d != 64 && d != 128)
         return FA_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || N == 0)
+    if (B == 0 || H == 0 || N == 0 || total == 0)
         return FA_OK;
     if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !D_buf)
         return FA_ERR_NULL_POINTER;
     const void *bf[8] = {Q, K, V, O, dO, dQ, dK, dV};
     for (const void *ptr : bf)
-        if (!fa::aligned(ptr, 16))
+        if (!aligned(ptr, 16))
             return FA_ERR_MISALIGNED;
-    if (!fa::aligned(lse, 4) || !fa::aligned(D_buf, 4))
+    if (!aligned(lse, 4) || !aligned(D_buf, 4) || (cu_seqlens && !aligned(cu_seqlens, 4)))
         return FA_ERR_MISALIGNED;
-    const int64_t total = int64_t(B) * N;
-    if (total > (int64_t(1) << 31) - 512 || total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+    if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
+        total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
-    fa::DeviceInfo *dev = fa::current_device();
+    DeviceInfo *dev = current_device();
     if (dev == nullptr)
         return FA_ERR_NO_DEVICE;
-    fa::AttnBwdArgs a;
+    AttnBwdArgs a;
     a.Q = Q;
     a.K = K;
     a.V = V;
@@ -390,7 +402,34 @@ int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O,
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.err_word = dev->err_word;
-    return fa::launch_attention_bwd(a, fa::t_stream);
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    return launch_attention_bwd(a, t_stream);
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                     const float *lse, void *dQ, void *dK, void *dV, float *D_buf, int B, int H,
+                     int N, int d, float scale, int causal)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N,
+                                    int64_t(B) * N, d, scale, causal, nullptr);
+}
+
+int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, const void *O,
+                            const void *dO, const float *lse, void *dQ, void *dK, void *dV,
+                            float *D_buf, int B, int H, int N, int64_t total, int d, float scale,
+                            int causal, const int32_t *cu_seqlens)
+{
+    if (cu_seqlens == nullptr)
+        return FA_ERR_NULL_POINTER;
+    return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N, total, d,
+                                    scale, causal, cu_seqlens);
 }
 
 int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d)
@@ -577,6 +616,14 @@ int fa_attention_fwd_f32(const float *Q, const float *K, const float *V, float *
 {
     return fa::attention_common(Q, K, V, O, lse, B, H, N, 0, false, d, scale, causal, cu_seqlens,
                                 false);
+}
+
+int fa_debug_expire_next_wait(int64_t ns)
+{
+    if (ns < 0 || ns > 1000000000)
+        return FA_ERR_BAD_SIZE;
+    fa::t_expire_wait_ns = uint32_t(ns);
+    return FA_OK;
 }
 
 int fa_set_stream(void *stream)

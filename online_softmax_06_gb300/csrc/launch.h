@@ -54,6 +54,10 @@ struct AttnArgs {
     int splits = 1;
     float *O_accum = nullptr; // [splits, B, N, H, d]
     float *lse_accum = nullptr;  // [splits, B, H, N]
+    // failure-detection test (fa_debug_expire_next_wait): nonzero makes the
+    // bf16 kernel's MMA warp first wait this many ns on a barrier that nothing
+    // arrives at, so the wait runs out and every CTA takes its abort path
+    uint32_t expire_wait_ns = 0;
 };
 
 int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream);
@@ -97,16 +101,19 @@ struct AttnFp8Args {
 };
 int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream);
 
-// Backward of the bf16 attention (dense [B, N, H, d]); layouts as in fa.h.
+// Backward of the bf16 attention (dense [B, N, H, d] or packed [total, H, d]);
+// layouts as in fa.h.
 struct AttnBwdArgs {
     const void *Q, *K, *V, *O, *dO;
-    const float *lse;          // [B, H, N], natural log, from the forward
+    const float *lse;          // [B, H, N] (packed: [H, total]), natural log, from the forward
     void *dQ, *dK, *dV;
-    float *D;                  // [B, H, N] scratch: D_i = dO_i . O_i
-    int B, H, N, d;
+    float *D;                  // the same layout as lse, scratch: D_i = dO_i . O_i
+    int B, H, N, d;            // packed: N = longest sequence (an upper bound)
     float scale;
     int causal;
     int *err_word;
+    const int32_t *cu_seqlens = nullptr;  // packed: device [B + 1] prefix sums
+    int64_t total = 0;                    // packed: rows of the tensors
 };
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
 

@@ -107,6 +107,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort, err_word);
 }
 
+// A wait with an explicit wall-time bound (no inlined fast path), for waits
+// whose bound is not the pipeline's: gives up after limit_ns, or at once when
+// *abort is raised, with the same error reporting as mbar_wait_slow.
+static __device__ __noinline__ bool mbar_wait_limited(uint64_t *bar, uint32_t parity,
+                                                      volatile int *abort, int *err_word,
+                                                      uint64_t limit_ns)
+{
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0; it < kWaitMaxPolls; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer() - t0 > limit_ns)
+            break;
+    }
+    record_device_error(err_word, FA_DEVERR_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
 // mbar_wait by all 32 lanes of a warp; the lanes agree on the result (a wait
 // that gives up in one lane gives up in all), so the warp stays converged.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,

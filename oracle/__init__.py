@@ -263,6 +263,39 @@ def attention_bwd(Q, K, V, dO, scale, causal, lib=None):
     return out
 
 
+def attention_bwd_packed(Q, K, V, dO, cu_seqlens, scale, causal, lib=None):
+    """Gradients of sum(dO * O) for packed sequences ("第二十二课…" §三十五:
+    a packed batch is a row of sequences, none attending to another).
+
+    Q, K, V, dO: [total, H, d]; cu_seqlens: [B+1] prefix sums.  Each sequence's
+    gradients are those of its own attention, so the dense backward runs on
+    each sequence's rows.  Returns a dict of float64 arrays: dQ, dK, dV, O
+    [total, H, d] and lse, D [H, total] (the packed layout of the row
+    statistics).
+    """
+    Q, K, V, dO = _f32(Q), _f32(K), _f32(V), _f32(dO)
+    total, H, d = Q.shape
+    for t in (K, V, dO):
+        if t.shape != Q.shape:
+            raise ValueError("Q, K, V, dO must have one shape")
+    cu = _cu(cu_seqlens)
+    if int(cu[-1]) != total:
+        raise ValueError("cu_seqlens[-1] must equal the number of packed tokens")
+    out = {k: np.zeros((total, H, d)) for k in ("dQ", "dK", "dV", "O")}
+    out["lse"] = np.zeros((H, total))
+    out["D"] = np.zeros((H, total))
+    for b in range(cu.size - 1):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        g = attention_bwd(*(X[None, s0:s1] for X in (Q, K, V, dO)), scale, causal, lib=lib)
+        for k in ("dQ", "dK", "dV", "O"):
+            out[k][s0:s1] = g[k][0]
+        out["lse"][:, s0:s1] = g["lse"][0]
+        out["D"][:, s0:s1] = g["D"][0]
+    return out
+
+
 def attention_bwd_head(Q, K, V, dO, scale, causal, b, h, q_idx, k_idx, lib=None):
     """dQ of the query rows q_idx and dK, dV of the keys k_idx for one (b, h).
 

@@ -518,6 +518,55 @@ def pin_bwd_head_matches_full(lib):
             _close(dv, g["dV"][b, ki, h], 1e-12, "head dV")
 
 
+def pin_bwd_packed_matches_dense(lib):
+    """Packed gradients with equal lengths equal the dense batch's, and the
+    row statistics land in the packed [H, total] layout."""
+    rng = np.random.default_rng(35)
+    B, N, H, d = 3, 11, 2, 8
+    Q, K, V, dO = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(4))
+    cu = np.arange(B + 1, dtype=np.int32) * N
+    for causal in (False, True):
+        g = oracle.attention_bwd(Q, K, V, dO, 0.4, causal, lib=lib)
+        gp = oracle.attention_bwd_packed(*(X.reshape(B * N, H, d) for X in (Q, K, V, dO)), cu,
+                                         0.4, causal, lib=lib)
+        for key in ("dQ", "dK", "dV", "O"):
+            _close(gp[key], g[key].reshape(B * N, H, d), 0.0, f"packed {key}")
+        for key in ("lse", "D"):
+            _close(gp[key], g[key].transpose(1, 0, 2).reshape(H, B * N), 0.0, f"packed {key}")
+
+
+def pin_bwd_packed_finite_differences(lib):
+    """Central differences of the packed forward oracle's loss sum(dO * O)
+    against the packed backward, entry by entry, on sequences of lengths 3, 1,
+    0 and 4: a gradient that leaks across a sequence boundary, or a slice off
+    by a row, changes some entry."""
+    rng = np.random.default_rng(36)
+    lens = [3, 1, 0, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total, H, d = int(cu[-1]), 2, 3
+    Q, K, V, dO = (_dyadic(rng, (total, H, d)) for _ in range(4))
+    scale = 0.5
+    step = 2.0 ** -12
+    for causal in (False, True):
+        g = oracle.attention_bwd_packed(Q, K, V, dO, cu, scale, causal, lib=lib)
+
+        def loss(Qx, Kx, Vx):
+            O, _ = oracle.attention_packed(Qx, Kx, Vx, cu, scale, causal, lib=lib)
+            return float((O * dO.astype(np.float64)).sum())
+
+        for name, X, key in (("Q", Q, "dQ"), ("K", K, "dK"), ("V", V, "dV")):
+            for idx in np.ndindex(X.shape):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[idx] += step
+                Xm[idx] -= step
+                args_p, args_m = [Q, K, V], [Q, K, V]
+                pos = "QKV".index(name)
+                args_p[pos], args_m[pos] = Xp, Xm
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * step)
+                assert abs(fd - g[key][idx]) <= 1e-6 * max(1.0, abs(fd)), (
+                    f"packed d{name}{idx} causal={causal}: fd {fd} vs oracle {g[key][idx]}")
+
+
 # ---- FP8 (blockwise quantisation + incoherent processing) -------------------
 
 def _e4m3_table():

@@ -95,6 +95,14 @@ def test_host_validation_without_gpu(lib):
     assert nl(None, None, None, None, None, 0, 1, 8, 8, 64, 1.0, 0, 0) == 0
 
 
+def test_expire_wait_argument_range(lib):
+    """The failure-detection switch takes 0 (off) .. 10^9 ns and is checked on
+    the host (no device needed)."""
+    assert fa.fa_debug_expire_next_wait(-1) == fa.FA_ERR_BAD_SIZE
+    assert fa.fa_debug_expire_next_wait(10**9 + 1) == fa.FA_ERR_BAD_SIZE
+    assert fa.fa_debug_expire_next_wait(0) == 0
+
+
 def test_noalloc_scratch_size_matches_header():
     text = open(HEADER, encoding="utf-8").read()
     m = re.search(r"#define FA_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", text)

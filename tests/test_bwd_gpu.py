@@ -100,6 +100,69 @@ def test_bwd_full_size_sampled(dev):
     device_error_clear()
 
 
+def run_gpu_packed(Q, K, V, dO, cu, max_len, causal, dev):
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    cu_d = torch.from_numpy(np.asarray(cu, np.int32)).to(dev)
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu_d, max_seqlen=max_len)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal, cu_seqlens=cu_d,
+                                  max_seqlen=max_len)
+    torch.cuda.synchronize(dev)
+    return [t.float().cpu().numpy() for t in (dq, dk, dv)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lens", [[1, 129, 300, 64, 257, 0, 128, 700], [1000, 3]])
+def test_bwd_packed_matches_oracle(dev, lens, d, causal):
+    """Packed sequences (lengths not multiples of the tiles, an empty one, one
+    token, the dQ pass's ring wrapping): every gradient against the oracle's
+    per-sequence backward."""
+    import workloads
+    cu = workloads.cu_seqlens_of(lens)
+    total, H = int(cu[-1]), 3
+    rng = np.random.default_rng(sum(lens) + d + causal)
+    Q, K, V, dO = (torch.from_numpy(rng.standard_normal((total, H, d)).astype(np.float32))
+                   .to(torch.bfloat16) for _ in range(4))
+    dq, dk, dv = run_gpu_packed(Q, K, V, dO, cu, max(lens), causal, dev)
+    ref = oracle.attention_bwd_packed(*(t.float().numpy() for t in (Q, K, V, dO)), cu,
+                                      1 / math.sqrt(d), causal)
+    errs = {name: normwise(g, ref[name]) for name, g in (("dQ", dq), ("dK", dk), ("dV", dv))}
+    print(f"packed {lens} d{d} causal={causal}: normwise errors {errs}")
+    for name, e in errs.items():
+        assert e <= BWD_TOL, f"{name}: {e}"
+    device_error_clear()
+
+
+def test_bwd_packed_equal_lengths_is_the_dense_call(dev):
+    """Packed sequences of one length give the dense call's bits (the same
+    kernels on the same rows; only the statistics' layout differs)."""
+    B, H, N, d = 2, 2, 300, 128
+    Q, K, V, dO = make_inputs(B, H, N, d, seed=17)
+    dense = run_gpu(Q, K, V, dO, True, dev)
+    cu = np.arange(B + 1, dtype=np.int32) * N
+    packed = run_gpu_packed(*(t.reshape(B * N, H, d) for t in (Q, K, V, dO)), cu, N, True, dev)
+    for x, y in zip(dense, packed):
+        assert np.array_equal(x.reshape(B * N, H, d), y)
+
+
+def test_bwd_packed_length_over_n_is_flagged(dev):
+    """A sequence longer than N is flagged in the device error word and not
+    computed (no access past the tensors)."""
+    H, d = 1, 64
+    q = torch.zeros((300, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((H, 300), dtype=torch.float32, device=dev)
+    cu = torch.tensor([0, 300], dtype=torch.int32, device=dev)
+    fa.fa_set_stream(torch.cuda.current_stream(dev).cuda_stream)
+    p, l = q.data_ptr(), lse.data_ptr()
+    rc = fa.fa_attention_bwd_varlen(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1,
+                                    cu.data_ptr())
+    assert rc == 0
+    assert fa.fa_get_device_error() == fa.FA_DEVERR_BAD_SEQLENS
+    assert fa.fa_get_device_error() == 0
+    assert fa.fa_attention_bwd_varlen(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1,
+                                      None) == fa.FA_ERR_NULL_POINTER
+
+
 def test_bwd_deterministic(dev):
     """No atomics: two runs give identical bits."""
     Q, K, V, dO = make_inputs(2, 2, 512, 128, seed=9)
