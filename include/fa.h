@@ -146,6 +146,35 @@ FA_API int fa_attention_fwd_splitkv(const void *Q, const void *K, const void *V,
                                     int causal, int num_splits, float *O_accum, float *lse_accum);
 
 /*
+ * fa_attention_fwd_splitkv for packed sequences whose query and key counts
+ * differ per sequence ("第二十二课…" §三十五 packed / variable-length sequences;
+ * e.g. one decode step over caches of different lengths): sequence b owns
+ * query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
+ * cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 and attends to nothing else.
+ *   Q, O: bf16 [total_q, H, d];  K, V: bf16 [total_k, H, d];  lse: fp32
+ *   [H, total_q].  cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1], each
+ *   non-decreasing from 0 to total_q / total_k.  Nq, Nk: the longest query
+ *   and key counts (upper bounds are fine; they size the grid and the split
+ *   choice).  causal != 0: within each sequence bottom-right aligned, query i
+ *   sees keys j <= i + Lk - Lq; a sequence with Lk < Lq, or longer than Nq /
+ *   Nk, is not computed and sets FA_DEVERR_BAD_SEQLENS.
+ *   num_splits: as fa_attention_fwd_splitkv (0: the library chooses from B,
+ *   H, Nq, Nk).  O_accum: fp32 [num_splits, total_q, H, d], lse_accum: fp32
+ *   [num_splits, H, total_q] -- caller scratch as in fa_attention_fwd_splitkv
+ *   (unused when one split is in effect).  Nothing is read back; no
+ *   synchronisation.
+ * Errors: as fa_attention_fwd_splitkv, and FA_ERR_NULL_POINTER for a NULL
+ * prefix-sum array.
+ */
+FA_API int fa_attention_fwd_splitkv_varlen(const void *Q, const void *K, const void *V, void *O,
+                                           float *lse, int B, int H, int Nq, int Nk,
+                                           int64_t total_q, int64_t total_k, int d, float scale,
+                                           int causal, int num_splits,
+                                           const int32_t *cu_seqlens_q,
+                                           const int32_t *cu_seqlens_k, float *O_accum,
+                                           float *lse_accum);
+
+/*
  * Attention backward for the bf16 forward (dense batches): the gradients of
  * sum(dO * O) with respect to Q, K and V, with the probabilities recomputed
  * from the forward's row logsumexp ("少搬一趟…" §2.4: P_ij = exp(S_ij - L_i);

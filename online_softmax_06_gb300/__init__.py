@@ -8,7 +8,7 @@ compiled library is missing, importing the C functions fails loudly.
 
 Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
-``fa_attention_fwd_splitkv``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
+``fa_attention_fwd_splitkv``, ``fa_attention_fwd_splitkv_varlen``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
 ``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_bwd_varlen``,
 ``fa_attention_fwd_fp8``,
 ``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
@@ -82,6 +82,9 @@ def lib():
         L.fa_attention_host_workspace_bytes.restype = i64
         L.fa_attention_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                        i32, f32, i32]
+        L.fa_attention_fwd_splitkv_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                      i64, i64, i32, f32, i32, i32, vp, vp, vp,
+                                                      vp]
         L.fa_attention_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                               i32, i64, i32, f32, i32, vp]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -97,7 +100,8 @@ def lib():
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
                      "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
-                     "fa_attention_bwd_varlen", "fa_attention_fwd_fp8",
+                     "fa_attention_bwd_varlen", "fa_attention_fwd_splitkv_varlen",
+                     "fa_attention_fwd_fp8",
                      "fa_attention_fwd_host",
                      "fa_set_stream", "fa_get_device_error", "fa_version",
                      "fa_debug_expire_next_wait"):
@@ -142,6 +146,13 @@ def fa_attention_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, nu
                              o_accum, lse_accum) -> int:
     return lib().fa_attention_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal,
                                           num_splits, o_accum, lse_accum)
+
+
+def fa_attention_fwd_splitkv_varlen(q, k, v, o, lse, B, H, Nq, Nk, total_q, total_k, d, scale,
+                                    causal, num_splits, cu_q, cu_k, o_accum, lse_accum) -> int:
+    return lib().fa_attention_fwd_splitkv_varlen(q, k, v, o, lse, B, H, Nq, Nk, total_q,
+                                                 total_k, d, scale, causal, num_splits, cu_q,
+                                                 cu_k, o_accum, lse_accum)
 
 
 def fa_splitkv_num_splits(B, H, Nq, Nk, d) -> int:
@@ -327,6 +338,53 @@ def attention_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = N
     return out, lse
 
 
+def attention_fwd_splitkv_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                                 max_seqlen_k: int, causal: bool = False,
+                                 scale: float | None = None, num_splits: int = 0):
+    """Split-KV attention forward on packed sequences through the C ABI (bf16).
+
+    q: [total_q, H, d]; k, v: [total_k, H, d]; cu_seqlens_q / cu_seqlens_k:
+    int32 CUDA [B+1].  causal is bottom-right aligned within each sequence.
+    The fp32 split scratch is allocated here (torch).  Returns
+    (O [total_q, H, d], lse [H, total_q]).
+    """
+    import torch
+    for t in (q, k, v):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.bfloat16):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    for c in (cu_seqlens_q, cu_seqlens_k):
+        if c.dtype != torch.int32 or not c.is_cuda:
+            raise ValueError("cu_seqlens must be int32 CUDA tensors")
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    if k.shape != (total_k, H, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [total_k, H, d]")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have one length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _use_current_stream(q.device)
+    splits = num_splits if num_splits > 0 else fa_splitkv_num_splits(B, H, max_seqlen_q,
+                                                                     max_seqlen_k, d)
+    if splits < 0:
+        raise FaError(splits, "fa_splitkv_num_splits")
+    splits = min(splits, (max_seqlen_k + 127) // 128)
+    out = torch.empty_like(q)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    o_acc = l_acc = None
+    if splits > 1:
+        o_acc = torch.empty((splits, total_q, H, d), dtype=torch.float32, device=q.device)
+        l_acc = torch.empty((splits, H, total_q), dtype=torch.float32, device=q.device)
+    rc = fa_attention_fwd_splitkv_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                         int(max_seqlen_q), int(max_seqlen_k), total_q, total_k,
+                                         d, float(scale), int(bool(causal)), splits,
+                                         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(o_acc),
+                                         _ptr(l_acc))
+    _check(rc, "fa_attention_fwd_splitkv_varlen")
+    return out, lse
+
+
 def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None = None,
                       workspace=None):
     """FP8 attention forward through the C ABI (bf16 dense [B, N, H, d], d = 128).
@@ -448,7 +506,9 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
 
 __all__ = [
     "build", "lib", "strerror", "FaError", "softmax_rows", "attention_fwd",
-    "attention_fwd_splitkv", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
+    "attention_fwd_splitkv", "attention_fwd_splitkv_varlen", "fa_attention_fwd_splitkv",
+    "fa_attention_fwd_splitkv_varlen",
+    "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
     "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "attention_fwd_fp8",
     "fa_attention_fwd_fp8",

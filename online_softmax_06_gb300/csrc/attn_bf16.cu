@@ -109,6 +109,10 @@ struct Bf16Params {
     float *O_accum;                  // splits > 1: [splits, B, N, H, d] fp32 partial O
     float *lse_accum;                // splits > 1: [splits, B, H, N] fp32 partial lse
     const int32_t *cu_seqlens;
+    // split-KV on packed batches: key rows per sequence (cu_seqlens then
+    // holds the query rows); causal is bottom-right within each sequence
+    const int32_t *cu_seqlens_k;
+    int64_t total_k;                 // rows of K / V
     int *err_word;
     uint32_t expire_wait_ns;         // failure-detection test only (0: off)
 };
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      pairs first ------------------------------------------------------------
     const int bh_count = p.B * p.H;
     const int n_splits = SPLIT ? p.splits : 1;
-    const int kv_off = SPLIT ? p.kv_off : 0;
+    int kv_off = SPLIT ? p.kv_off : 0;
     const int split = SPLIT ? int(blockIdx.x % unsigned(n_splits)) : 0;
     const int rest = SPLIT ? int(blockIdx.x / unsigned(n_splits)) : int(blockIdx.x);
     const int pair = p.n_pairs - 1 - rest / bh_count;
@@ -176,6 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         start = start_k = s0;
         L = Lk = int(s1 - s0);
+        if (SPLIT && p.cu_seqlens_k != nullptr) {
+            const int64_t k0 = p.cu_seqlens_k[b], k1 = p.cu_seqlens_k[b + 1];
+            if (k0 < 0 || k1 < k0 || k1 > p.total_k || k1 - k0 > p.Nk ||
+                (p.causal && k1 - k0 < L)) {
+                if (threadIdx.x == 0 && pair == 0 && h == 0 && split == 0)
+                    record_device_error(p.err_word, FA_DEVERR_BAD_SEQLENS);
+                return;
+            }
+            start_k = k0;
+            Lk = int(k1 - k0);
+            kv_off = Lk - L;
+        }
     } else {
         start = int64_t(b) * p.N;
         L = p.N;
@@ -185,6 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt0 = 2 * pair;                  // Q0 = tile qt0, Q1 = tile qt0 + 1
     if (qt0 * BM >= L)
         return;                                // whole CTA: nothing to do
+    // Split-KV partial results: [splits, B, N, H, d] and [splits, B, H, N]
+    // dense; packed batches use [splits, total, H, d] and [splits, H, total]
+    const bool packed = p.cu_seqlens != nullptr;
+    auto lse_acc_index = [&](int i) -> int64_t {
+        return packed ? (int64_t(split) * p.H + h) * p.total + start + i
+                      : ((int64_t(split) * p.B + b) * p.H + h) * p.N + i;
+    };
     const bool has_q1 = (qt0 + 1) * BM < L;
     const int n_kv = (Lk + BN - 1) / BN;
     int n0, n1, n_max, j0 = 0;
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n_splits > 1 && threadIdx.x < 2 * BM) {
             const int i = qt0 * BM + int(threadIdx.x);
             if (i < L)
-                p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = -INFINITY;
+                p.lse_accum[lse_acc_index(i)] = -INFINITY;
         }
         return;
     }
@@ -670,8 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool empty = !(l > 0.f);
                     const float inv = empty ? 0.f : 1.f / l_o;
                     __nv_bfloat16 *orow = p.O + ((start + i) * p.H_row + h) * D;
+                    const int64_t acc_rows = packed ? p.total : int64_t(p.B) * p.N;
+                    const int64_t acc_row0 = packed ? start : int64_t(b) * p.N;
                     float *arow = p.O_accum +
-                                  (((int64_t(split) * p.B + b) * p.N + i) * p.H + h) * D;
+                                  ((int64_t(split) * acc_rows + acc_row0 + i) * p.H + h) * D;
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -707,14 +732,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (row_ok) {
                         const float lse = empty ? -INFINITY : (m + log2f(l)) * kLn2;
                         if (n_splits > 1)
-                            p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = lse;
+                            p.lse_accum[lse_acc_index(i)] = lse;
+                        else if (packed)
+                            p.lse[int64_t(h) * p.total + start + i] = lse;
                         else
                             p.lse[(int64_t(b) * p.H_row + h) * p.N + i] = lse;
                     }
                 }
             } else if (!aborted && n_splits > 1 && i < L) {
                 // this tile has no keys in this split
-                p.lse_accum[((int64_t(split) * p.B + b) * p.H + h) * p.N + i] = -INFINITY;
+                p.lse_accum[lse_acc_index(i)] = -INFINITY;
             }
         } else if (n_t > 0) {
             // A whole tile goes out through shared memory and one TMA store:
@@ -815,7 +842,8 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
 {
     Bf16Params p;
     const int Nk = a.Nk > 0 ? a.Nk : a.N;
-    const int64_t total_k = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
+    const int64_t total_k = a.cu_seqlens_k != nullptr ? a.total_k
+                            : a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * Nk;
     const int H_row = a.H_row > 0 ? a.H_row : a.H;
     if (!make_tmap_bf16(&p.tm_q, a.Q, a.total, a.H, a.d, 128, H_row) ||
         !make_tmap_bf16(&p.tm_k, a.K, total_k, a.H, a.d, 128, H_row) ||
@@ -839,6 +867,8 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
     p.cu_seqlens = a.cu_seqlens;
+    p.cu_seqlens_k = a.cu_seqlens_k;
+    p.total_k = total_k;
     p.err_word = a.err_word;
     p.expire_wait_ns = a.expire_wait_ns;
     const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H * p.splits;
@@ -846,7 +876,7 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
         return FA_OK;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
-    const bool split = p.splits > 1 || p.kv_off != 0 || Nk != a.N;
+    const bool split = p.splits > 1 || p.kv_off != 0 || Nk != a.N || a.cu_seqlens_k != nullptr;
     int rc;
     if (a.d == 64)
         rc = split ? launch_d<64, true>(p, blocks, stream) : launch_d<64, false>(p, blocks, stream);
@@ -888,6 +918,8 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
     p.cu_seqlens = nullptr;
+    p.cu_seqlens_k = nullptr;
+    p.total_k = total;
     p.err_word = a.err_word;
     p.expire_wait_ns = 0;
     const int64_t blocks = int64_t(p.n_pairs) * a.B * a.H;

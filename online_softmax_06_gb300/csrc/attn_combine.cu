@@ -153,7 +153,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 int launch_attention_combine(const AttnArgs &a, cudaStream_t stream)
 {
-    const int64_t rows = int64_t(a.B) * a.N * a.H;
+    // a packed batch's partials ([splits, total, H, d], [splits, H, total]) are
+    // the dense layout of one sequence of `total` rows
+    const bool packed = a.cu_seqlens != nullptr;
+    const int B = packed ? 1 : a.B;
+    const int64_t N64 = packed ? a.total : a.N;
+    if (N64 > 0x7fffffffLL)
+        return FA_ERR_TOO_LARGE;
+    const int N = int(N64);
+    const int64_t rows = int64_t(B) * N * a.H;
     if (rows == 0)
         return FA_OK;
     const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
@@ -162,10 +170,10 @@ int launch_attention_combine(const AttnArgs &a, cudaStream_t stream)
     auto *O = static_cast<__nv_bfloat16 *>(a.O);
     if (a.d == 64)
         attn_combine_kernel<64><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
-            a.O_accum, a.lse_accum, O, a.lse, a.B, a.H, a.N, a.splits);
+            a.O_accum, a.lse_accum, O, a.lse, B, a.H, N, a.splits);
     else
         attn_combine_kernel<128><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
-            a.O_accum, a.lse_accum, O, a.lse, a.B, a.H, a.N, a.splits);
+            a.O_accum, a.lse_accum, O, a.lse, B, a.H, N, a.splits);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -411,6 +411,59 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
 
 extern "C" {
 
+int fa_attention_fwd_splitkv_varlen(const void *Q, const void *K, const void *V, void *O,
+                                    float *lse, int B, int H, int Nq, int Nk, int64_t total_q,
+                                    int64_t total_k, int d, float scale, int causal,
+                                    int num_splits, const int32_t *cu_seqlens_q,
+                                    const int32_t *cu_seqlens_k, float *O_accum,
+                                    float *lse_accum)
+{
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || total_q < 0 || total_k < 0 || num_splits < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 64 && d != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)
+        return FA_ERR_NULL_POINTER;
+    if (B == 0 || H == 0 || Nq == 0 || total_q == 0)
+        return FA_OK;
+    if (Nk == 0 || total_k == 0)
+        return FA_ERR_BAD_SIZE;            // no key for any query
+    fa::DeviceInfo *dev = fa::current_device();
+    if (dev == nullptr)
+        return FA_ERR_NO_DEVICE;
+    if (total_k > (int64_t(1) << 31) - 512 || int64_t(Nk) > (int64_t(1) << 31) - 512)
+        return FA_ERR_TOO_LARGE;
+    if (!fa::aligned(cu_seqlens_k, 4))
+        return FA_ERR_MISALIGNED;
+    fa::AttnArgs a;
+    int rc = fa::check_attention(Q, K, V, O, lse, B, H, Nq, d, causal, cu_seqlens_q, total_q, true,
+                                 &a);
+    if (rc != FA_OK)
+        return rc;
+    int splits = num_splits == 0 ? fa::choose_num_splits(B, H, Nq, Nk) : num_splits;
+    const int n_kv = (Nk + 127) / 128;
+    if (splits > n_kv)
+        splits = n_kv;
+    if (splits > 1) {
+        if (O_accum == nullptr || lse_accum == nullptr)
+            return FA_ERR_NULL_POINTER;
+        if (!fa::aligned(O_accum, 16) || !fa::aligned(lse_accum, 4))
+            return FA_ERR_MISALIGNED;
+        if (int64_t(splits) * total_q * H * d > (int64_t(1) << 56))
+            return FA_ERR_TOO_LARGE;
+    }
+    a.scale = scale;
+    a.err_word = dev->err_word;
+    a.Nk = Nk;
+    a.kv_off = 0;                          // per sequence, from the two prefix sums
+    a.splits = splits;
+    a.O_accum = splits > 1 ? O_accum : nullptr;
+    a.lse_accum = splits > 1 ? lse_accum : nullptr;
+    a.cu_seqlens_k = cu_seqlens_k;
+    a.total_k = total_k;
+    return fa::launch_attention_bf16(a, fa::t_stream);
+}
+
 int fa_attention_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                      const float *lse, void *dQ, void *dK, void *dV, float *D_buf, int B, int H,
                      int N, int d, float scale, int causal)

@@ -52,8 +52,12 @@ struct AttnArgs {
     int Nk = 0;               // 0: same as N
     int kv_off = 0;
     int splits = 1;
-    float *O_accum = nullptr; // [splits, B, N, H, d]
-    float *lse_accum = nullptr;  // [splits, B, H, N]
+    float *O_accum = nullptr; // [splits, B, N, H, d] (packed: [splits, total, H, d])
+    float *lse_accum = nullptr;  // [splits, B, H, N] (packed: [splits, H, total])
+    // split-KV on packed batches: key rows per sequence; cu_seqlens holds the
+    // query rows, total the query row count
+    const int32_t *cu_seqlens_k = nullptr;
+    int64_t total_k = 0;
     // failure-detection test (fa_debug_expire_next_wait): nonzero makes the
     // bf16 kernel's MMA warp first wait this many ns on a barrier that nothing
     // arrives at, so the wait runs out and every CTA takes its abort path

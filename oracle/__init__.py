@@ -241,6 +241,36 @@ def attention_qk(Q, K, V, scale, causal, samples=None, lib=None):
     return O, lse
 
 
+def attention_qk_packed(Q, K, V, cu_seqlens_q, cu_seqlens_k, scale, causal, lib=None):
+    """Attention with separate query / key lengths on packed sequences.
+
+    Q: [total_q, H, d]; K, V: [total_k, H, d]; sequence b owns query rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] ..
+    cu_seqlens_k[b+1]-1, and attends to nothing else ("第二十二课…" §三十五).
+    causal is bottom-right aligned within each sequence (query i sees keys
+    j <= i + Lk - Lq).  Each sequence is attention_qk's dense case with B = 1.
+    Returns (O [total_q, H, d] f64, lse [H, total_q] f64).
+    """
+    Q, K, V = _f32(Q), _f32(K), _f32(V)
+    cq, ck = _cu(cu_seqlens_q), _cu(cu_seqlens_k)
+    if cq.size != ck.size:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have one length")
+    total_q, H, d = Q.shape
+    if int(cq[-1]) != total_q or int(ck[-1]) != K.shape[0] or V.shape != K.shape:
+        raise ValueError("prefix sums must end at the row counts of Q and K, V")
+    O = np.zeros((total_q, H, d))
+    lse = np.zeros((H, total_q))
+    for b in range(cq.size - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        Ob, lb = attention_qk(Q[None, q0:q1], K[None, k0:k1], V[None, k0:k1], scale, causal,
+                              lib=lib)
+        O[q0:q1] = Ob[0]
+        lse[:, q0:q1] = lb[0]
+    return O, lse
+
+
 def attention_bwd(Q, K, V, dO, scale, causal, lib=None):
     """Gradients of sum(dO * O) for dense Q, K, V, dO [B, N, H, d].
 

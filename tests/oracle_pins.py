@@ -413,6 +413,34 @@ def _dyadic(rng, shape, denom=64, span=2):
     return (rng.integers(-span * denom, span * denom, size=shape) / denom).astype(np.float32)
 
 
+def pin_attention_qk_packed_layout(lib):
+    """Packed sequences with separate query and key lengths: equal lengths give
+    the dense batch of attention_qk, and equal query and key prefix sums give
+    the packed square attention (the causal case then aligns top-left and
+    bottom-right alike)."""
+    rng = np.random.default_rng(27)
+    B, Nq, Nk, H, d = 3, 5, 12, 2, 8
+    Q = rng.standard_normal((B, Nq, H, d)).astype(np.float32)
+    K, V = (rng.standard_normal((B, Nk, H, d)).astype(np.float32) for _ in range(2))
+    cq = np.arange(B + 1, dtype=np.int32) * Nq
+    ck = np.arange(B + 1, dtype=np.int32) * Nk
+    for causal in (False, True):
+        O, lse = oracle.attention_qk(Q, K, V, 0.3, causal, lib=lib)
+        Op, lp = oracle.attention_qk_packed(Q.reshape(B * Nq, H, d), K.reshape(B * Nk, H, d),
+                                            V.reshape(B * Nk, H, d), cq, ck, 0.3, causal,
+                                            lib=lib)
+        _close(Op, O.reshape(B * Nq, H, d), 0.0, "qk packed O vs dense")
+        _close(lp, lse.transpose(1, 0, 2).reshape(H, B * Nq), 0.0, "qk packed lse vs dense")
+    lens = [4, 1, 9, 0, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    X = [rng.standard_normal((int(cu[-1]), H, d)).astype(np.float32) for _ in range(3)]
+    for causal in (False, True):
+        Op, lp = oracle.attention_qk_packed(*X, cu, cu, 0.4, causal, lib=lib)
+        Or, lr = oracle.attention_packed(*X, cu, 0.4, causal, lib=lib)
+        _close(Op, Or, 1e-15, "qk packed square O")
+        _close(lp, lr, 1e-14, "qk packed square lse")
+
+
 def pin_bwd_finite_differences(lib):
     """Central differences of the (pinned) forward oracle's loss sum(dO * O)
     against the backward oracle, entry by entry on a tiny problem."""

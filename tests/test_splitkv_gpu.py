@@ -99,3 +99,80 @@ def test_splitkv_bad_arguments(dev):
     assert fa.fa_attention_fwd_splitkv(p, k2.data_ptr(), k2.data_ptr(), p, lse.data_ptr(),
                                        1, 1, 256, 1024, 64, 0.125, 1, 4, None, None) == -1
     assert fa.fa_splitkv_num_splits(1, 1, 256, 1024, 96) == -3
+
+
+# ---------------------------------------------------------------------------
+# packed sequences with their own query and key counts (a decode step over
+# caches of different lengths)
+# ---------------------------------------------------------------------------
+
+def packed_inputs(lens_q, lens_k, H, d, seed):
+    rng = np.random.default_rng(seed)
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    mk = lambda n: torch.from_numpy(rng.standard_normal((n, H, d), dtype=np.float32)).to(
+        torch.bfloat16)
+    return mk(tq), mk(tk), mk(tk)
+
+
+def run_packed(Q, K, V, lens_q, lens_k, causal, splits, dev):
+    cq = torch.from_numpy(workloads.cu_seqlens_of(lens_q)).to(dev)
+    ck = torch.from_numpy(workloads.cu_seqlens_of(lens_k)).to(dev)
+    q, k, v = (t.to(dev) for t in (Q, K, V))
+    O, lse = fa.attention_fwd_splitkv_varlen(q, k, v, cq, ck, max(lens_q), max(lens_k),
+                                             causal=causal, num_splits=splits)
+    torch.cuda.synchronize(dev)
+    return O.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("splits", [0, 1, 3, 16])
+def test_splitkv_packed_matches_oracle(dev, d, causal, splits):
+    """Sequences of 1, 7, 0, 300 and 129 new queries against 1000, 7, 50, 3000
+    and 129 keys (a query-free sequence, a square one, one whose keys fit one
+    tile): every row against the oracle's per-sequence attention."""
+    lens_q, lens_k = [1, 7, 0, 300, 129], [1000, 7, 50, 3000, 129]
+    Q, K, V = packed_inputs(lens_q, lens_k, 3, d, seed=d + causal + splits)
+    O, lse = run_packed(Q, K, V, lens_q, lens_k, causal, splits, dev)
+    Or, lr = oracle.attention_qk_packed(Q.float().numpy(), K.float().numpy(), V.float().numpy(),
+                                        workloads.cu_seqlens_of(lens_q),
+                                        workloads.cu_seqlens_of(lens_k), 1 / math.sqrt(d), causal)
+    assert max_abs(O, Or) <= ATTN_BF16_O_TOL
+    assert max_abs(lse, lr) <= ATTN_BF16_LSE_TOL
+    device_error_clear()
+
+
+def test_splitkv_packed_equal_lengths_is_the_dense_call(dev):
+    """Packed sequences of one query and one key count give the dense split-KV
+    call's bits at the same split count."""
+    B, H, Nq, Nk, d = 3, 2, 200, 1500, 128
+    Q, K, V = inputs(B, H, Nq, Nk, d, seed=77)
+    Od, ld = run(Q, K, V, True, 4, dev)
+    Op, lp = run_packed(Q.reshape(B * Nq, H, d), K.reshape(B * Nk, H, d),
+                        V.reshape(B * Nk, H, d), [Nq] * B, [Nk] * B, True, 4, dev)
+    assert np.array_equal(Op, Od.reshape(B * Nq, H, d))
+    assert np.array_equal(lp, ld.transpose(1, 0, 2).reshape(H, B * Nq))
+
+
+def test_splitkv_packed_bad_lengths_are_flagged(dev):
+    """Causal with fewer keys than queries in one sequence, or a key count over
+    the stated maximum, sets the device error bit instead of computing."""
+    H, d = 1, 64
+    q = torch.zeros((10, H, d), dtype=torch.bfloat16, device=dev)
+    k = torch.zeros((20, H, d), dtype=torch.bfloat16, device=dev)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((H, 10), dtype=torch.float32, device=dev)
+    fa.fa_set_stream(torch.cuda.current_stream(dev).cuda_stream)
+    for lens_q, lens_k, Nk in (([6, 4], [2, 18], 18), ([10], [20], 16)):
+        cq = torch.from_numpy(workloads.cu_seqlens_of(lens_q)).to(dev)
+        ck = torch.from_numpy(workloads.cu_seqlens_of(lens_k)).to(dev)
+        rc = fa.fa_attention_fwd_splitkv_varlen(q.data_ptr(), k.data_ptr(), k.data_ptr(),
+                                                o.data_ptr(), lse.data_ptr(), len(lens_q), H,
+                                                max(lens_q), Nk, 10, 20, d, 0.125, 1, 1,
+                                                cq.data_ptr(), ck.data_ptr(), None, None)
+        assert rc == 0
+        assert fa.fa_get_device_error() == fa.FA_DEVERR_BAD_SEQLENS
+    assert fa.fa_attention_fwd_splitkv_varlen(q.data_ptr(), k.data_ptr(), k.data_ptr(),
+                                              o.data_ptr(), lse.data_ptr(), 1, H, 10, 20, 10, 20,
+                                              d, 0.125, 1, 1, None, None, None,
+                                              None) == fa.FA_ERR_NULL_POINTER
