@@ -670,7 +670,7 @@ def main():
             for name, wc in workloads.WORKLOADS.items():
                 if name == w.name:
                     continue
-                configs[name] = time_config(fa, wc, dev, 500 if wc.dtype == "f32" else 30,
+                configs[name] = time_config(fa, wc, dev, 50 if wc.dtype == "f32" else 30,
                                             peaks, clocks)
     finally:
         clk = clocks.stop()

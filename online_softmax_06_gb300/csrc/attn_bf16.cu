@@ -648,19 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tmem_st32(tP + half * 32, pk);
             }
-            const float tile_sum = rowsum2.x + rowsum2.y;
-            l = l * corr + tile_sum;
-            if constexpr (FP8) {
-                l_o = l;
-            } else {
-                // the tile maximum's probability exactly as the loop formed
-                // it (same fma and ex2), and its bf16 value
-                const float p_top = ptx::ex2(fmaf(mx, slj, -m_use));
-                const float p_top_bf16 = __uint_as_float(ptx::pack_bf16x2(p_top, 0.f) << 16);
-                l_o = l_o * corr + (tile_sum + (p_top_bf16 - p_top));
-            }
-            m = m_new;
-
             // rescale this row of O~ when its reference moved (never on the
             // first tile: the first P V overwrites O); the warp goes together,
             // lanes whose reference did not move multiply by exactly 1
@@ -679,6 +666,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
             ptx::mbar_arrive(&bar.p_full[t]);
+
+            // The row sums are needed only after the last tile: they are
+            // updated after P is handed over, off the path to the next MMA.
+            const float tile_sum = rowsum2.x + rowsum2.y;
+            l = l * corr + tile_sum;
+            if constexpr (FP8) {
+                l_o = l;
+            } else {
+                // the tile maximum's probability exactly as the loop formed
+                // it (same fma and ex2), and its bf16 value
+                const float p_top = ptx::ex2(fmaf(mx, slj, -m_use));
+                const float p_top_bf16 = __uint_as_float(ptx::pack_bf16x2(p_top, 0.f) << 16);
+                l_o = l_o * corr + (tile_sum + (p_top_bf16 - p_top));
+            }
+            m = m_new;
         }
 
         // ---- epilogue: O = O~ / l (bf16), lse = (m + log2 l) * ln 2 -----------

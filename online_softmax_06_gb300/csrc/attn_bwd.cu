@@ -133,9 +133,10 @@ struct SeqRows {
     int64_t row0, stat0;
     int L;
 };
+template <bool PACKED>
 __device__ __forceinline__ bool seq_rows(const BwdParams &p, int b, int h, SeqRows &q)
 {
-    if (p.cu_seqlens == nullptr) {
+    if constexpr (!PACKED) {
         q.row0 = int64_t(b) * p.N;
         q.L = p.N;
         q.stat0 = (int64_t(b) * p.H + h) * p.N;
@@ -326,7 +327,7 @@ struct CfgQ {
 constexpr uint32_t kQColS = 0, kQColDP = 128;   // dQ kernel: S; dP, then dS packed
 constexpr int kQCols = 64;                      // columns of a step per row thread
 
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
     SeqRows sq;
-    if (!seq_rows(p, b, h, sq) || qt * BT >= sq.L)
+    if (!seq_rows<PACKED>(p, b, h, sq) || qt * BT >= sq.L)
         return;                                     // whole CTA: nothing to do
     const int64_t row0 = sq.row0;                   // first row of the sequence
     const int L = sq.L;
@@ -712,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =============================================================================
 // dK, dV -- one CTA per (sequence, head, key tile), heaviest tiles first
 // =============================================================================
-template <int D>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p)
 {
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = int(blockIdx.x) % bh_count;
     const int b = bh / p.H, h = bh % p.H;
     SeqRows sq;
-    if (!seq_rows(p, b, h, sq) || kt * BT >= sq.L)
+    if (!seq_rows<PACKED>(p, b, h, sq) || kt * BT >= sq.L)
         return;                                      // whole CTA: nothing to do
     const int64_t row0 = sq.row0;
     const int L = sq.L;
@@ -996,22 +997,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     teardown<D>(tmem);
 }
 
-template <int D>
+template <int D, bool PACKED>
 int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t stream)
 {
+    auto kdq = attn_bwd_dq_kernel<D, PACKED>;
+    auto kdkdv = attn_bwd_dkdv_kernel<D, PACKED>;
     static PerDeviceOnce once_dq, once_dkdv;
-    if (!set_max_dynamic_smem(once_dq, reinterpret_cast<const void *>(attn_bwd_dq_kernel<D>),
+    if (!set_max_dynamic_smem(once_dq, reinterpret_cast<const void *>(kdq),
                               int(CfgQ<D>::kSmemBytes)) ||
-        !set_max_dynamic_smem(once_dkdv, reinterpret_cast<const void *>(attn_bwd_dkdv_kernel<D>),
+        !set_max_dynamic_smem(once_dkdv, reinterpret_cast<const void *>(kdkdv),
                               int(Cfg<D>::kSmemBytes)))
         return FA_ERR_CUDA;
     const int64_t blocks = int64_t(p_dq.n_tiles) * p_dq.B * p_dq.H;
-    attn_bwd_dq_kernel<D>
-        <<<dim3(unsigned(blocks)), dim3(kThreads), CfgQ<D>::kSmemBytes, stream>>>(p_dq);
+    kdq<<<dim3(unsigned(blocks)), dim3(kThreads), CfgQ<D>::kSmemBytes, stream>>>(p_dq);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    attn_bwd_dkdv_kernel<D>
-        <<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dkdv);
+    kdkdv<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dkdv);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -1054,8 +1055,13 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
         !make_tmap_bf16(&p_dkdv.tm_s0, a.Q, total, a.H, a.d, BS) ||
         !make_tmap_bf16(&p_dkdv.tm_s1, a.dO, total, a.H, a.d, BS))
         return FA_ERR_CUDA;
-    return a.d == 64 ? launch_bwd_d<64>(p_dq, p_dkdv, stream)
-                     : launch_bwd_d<128>(p_dq, p_dkdv, stream);
+    // packed batches get their own instantiation, so that the dense kernels
+    // keep the sequence length a kernel constant
+    if (a.cu_seqlens != nullptr)
+        return a.d == 64 ? launch_bwd_d<64, true>(p_dq, p_dkdv, stream)
+                         : launch_bwd_d<128, true>(p_dq, p_dkdv, stream);
+    return a.d == 64 ? launch_bwd_d<64, false>(p_dq, p_dkdv, stream)
+                     : launch_bwd_d<128, false>(p_dq, p_dkdv, stream);
 }
 
 }  // namespace fa
