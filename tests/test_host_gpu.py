@@ -34,7 +34,7 @@ def host_inputs(shape, seed, pinned):
 
 
 # head counts below, at and above the number of head groups (8), and not
-# multiples of it; ragged sequence lengths
+# multiples of it; ragged sequence lengths, long and many short sequences
 @pytest.mark.parametrize("B,N,H,d,causal", [
     (2, 300, 3, 128, True),
     (1, 513, 12, 64, False),
@@ -42,6 +42,13 @@ def host_inputs(shape, seed, pinned):
     (1, 1, 1, 64, True),
     (3, 129, 8, 64, True),
     (1, 1100, 32, 128, True),
+    (1, 4100, 2, 128, True),
+    (1, 4100, 2, 64, False),
+    (3, 2000, 4, 128, True),
+    (3, 2000, 4, 64, False),
+    (12, 1100, 2, 128, True),
+    (40, 200, 2, 64, True),
+    (100, 64, 1, 128, False),
 ])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_host_matches_device(dev, B, N, H, d, causal, pinned):
