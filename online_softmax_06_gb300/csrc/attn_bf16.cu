@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ Bf16Params p)
 {
     static_assert(!FP8 || (D == 128 && !SPLIT), "FP8: d = 128, no key splits");
+    // FP8: launched as a programmatic dependent of the V transpose; nothing
+    // the quantisation wrote is read before this wait returns
+    if constexpr (FP8)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -934,7 +938,19 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern),
                               int(Cfg<128, true>::kSmemBytes)))
         return FA_ERR_CUDA;
-    kern<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<128, true>::kSmemBytes, stream>>>(p);
+    // programmatic dependent launch of the quantisation's last kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<128, true>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess)
+        return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

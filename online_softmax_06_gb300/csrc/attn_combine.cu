@@ -34,6 +34,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     attn_combine_kernel(const float *O_accum, const float *lse_accum, __nv_bfloat16 *O,
                         float *lse, int B, int H, int N, int splits)
 {
+    // Launched as a programmatic dependent of the split kernel: everything
+    // above the partials' first read may overlap that kernel's end; the wait
+    // returns once the split kernel has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int kPerLane = D / 32;
     const int lane = threadIdx.x & 31;
     const int64_t row = int64_t(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -168,13 +172,24 @@ int launch_attention_combine(const AttnArgs &a, cudaStream_t stream)
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
     auto *O = static_cast<__nv_bfloat16 *>(a.O);
-    if (a.d == 64)
-        attn_combine_kernel<64><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
-            a.O_accum, a.lse_accum, O, a.lse, B, a.H, N, a.splits);
-    else
-        attn_combine_kernel<128><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, 0, stream>>>(
-            a.O_accum, a.lse_accum, O, a.lse, B, a.H, N, a.splits);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    // programmatic dependent launch: the combine's launch and start overlap
+    // the end of the split kernel before it on the stream
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kWarpsPerBlock * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e =
+        a.d == 64 ? cudaLaunchKernelEx(&cfg, attn_combine_kernel<64>, a.O_accum, a.lse_accum, O,
+                                       a.lse, B, a.H, N, a.splits)
+                  : cudaLaunchKernelEx(&cfg, attn_combine_kernel<128>, a.O_accum, a.lse_accum, O,
+                                       a.lse, B, a.H, N, a.splits);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace fa

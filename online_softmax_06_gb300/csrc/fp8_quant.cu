@@ -445,6 +445,10 @@ __global__ void __launch_bounds__(256) fp8_vt_kernel(const __grid_constant__ VtP
             raw[j][1] = make_uint4(0, 0, 0, 0);
         }
     }
+    // Launched as a programmatic dependent of the quantisation kernel: V (an
+    // input) is loaded above; the per-tile amax it wrote is read only after
+    // the wait, which returns once that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     float amax = 0.f;
     for (int t = lane; t < p.n_tiles; t += 32)
         amax = fmaxf(amax, p.vamax[int64_t(bh) * p.n_tiles + t]);
@@ -530,8 +534,20 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
     if (!set_max_dynamic_smem(once_vt, reinterpret_cast<const void *>(fp8_vt_kernel),
                               int(kVtSmemBytes)))
         return FA_ERR_CUDA;
-    const dim3 grid_v(unsigned(a.B * a.H), unsigned(n_tiles));
-    fp8_vt_kernel<<<grid_v, 256, kVtSmemBytes, stream>>>(v);
+    // programmatic dependent launch: its launch and its loads of V overlap
+    // the end of the quantisation kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.B * a.H), unsigned(n_tiles));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kVtSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fp8_vt_kernel, v) != cudaSuccess)
+        return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
