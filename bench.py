@@ -182,7 +182,9 @@ def packed_f32(w):
 
 def cpu_baseline(w, seconds: float):
     import oracle
+    oracle.load()                                            # built and loaded before timing
     Qp, Kp, Vp = packed_f32(w)
+    time_oracle(w, Qp, Kp, Vp, 64, seed=0)                   # warm-up (threads, caches)
     dt, _ = time_oracle(w, Qp, Kp, Vp, 64, seed=1)          # calibration
     per_row = max(dt / 64, 1e-6)
     n = int(min(max(seconds / per_row, 256), w.total * w.H))
@@ -197,8 +199,10 @@ def run_reference(args, rank: int):
     if rank != 0:
         return 0
     import oracle
+    oracle.load()                                            # built and loaded before timing
     w = workloads.WORKLOADS[args.workload]
     Qp, Kp, Vp = packed_f32(w)
+    time_oracle(w, Qp, Kp, Vp, 64, seed=0)                   # warm-up (threads, caches)
     dt, _ = time_oracle(w, Qp, Kp, Vp, 64, seed=1)
     per_row = max(dt / 64, 1e-6)
     # each step is a bounded sample sized so the whole run stays within minutes
