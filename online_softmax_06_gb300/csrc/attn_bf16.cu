@@ -244,11 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_max = n0 > n1 ? n0 : n1;
     if (SPLIT && n_max == 0) {
         // an empty split: its partial result for the pair's rows is empty
-        // (lse = -inf, weight 0 in the combine)
-        if (n_splits > 1 && threadIdx.x < 2 * BM) {
+        // (lse = -inf, weight 0 in the combine).  With one split this happens
+        // only for a packed sequence without keys: its rows see no key, so O
+        // is 0 and lse is -inf.
+        if (threadIdx.x < 2 * BM) {
             const int i = qt0 * BM + int(threadIdx.x);
-            if (i < L)
+            if (i < L && n_splits > 1) {
                 p.lse_accum[lse_acc_index(i)] = -INFINITY;
+            } else if (i < L) {
+                uint4 *orow = reinterpret_cast<uint4 *>(p.O + ((start + i) * p.H_row + h) * D);
+#pragma unroll
+                for (int q = 0; q < D / 8; ++q)
+                    orow[q] = make_uint4(0, 0, 0, 0);
+                if (packed)
+                    p.lse[int64_t(h) * p.total + start + i] = -INFINITY;
+                else
+                    p.lse[(int64_t(b) * p.H_row + h) * p.N + i] = -INFINITY;
+            }
         }
         return;
     }

@@ -176,3 +176,21 @@ def test_splitkv_packed_bad_lengths_are_flagged(dev):
                                               o.data_ptr(), lse.data_ptr(), 1, H, 10, 20, 10, 20,
                                               d, 0.125, 1, 1, None, None, None,
                                               None) == fa.FA_ERR_NULL_POINTER
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_splitkv_packed_sequence_without_keys(dev, splits):
+    """A non-causal packed sequence with queries but no keys: its rows see no
+    key, so O = 0 and lse = -inf (the oracle's reading); the other sequences
+    are unaffected."""
+    lens_q, lens_k, d = [3, 5, 130], [0, 300, 1000], 128
+    Q, K, V = packed_inputs(lens_q, lens_k, 2, d, seed=31 + splits)
+    O, lse = run_packed(Q, K, V, lens_q, lens_k, False, splits, dev)
+    Or, lr = oracle.attention_qk_packed(Q.float().numpy(), K.float().numpy(), V.float().numpy(),
+                                        workloads.cu_seqlens_of(lens_q),
+                                        workloads.cu_seqlens_of(lens_k), 1 / math.sqrt(d), False)
+    assert np.all(O[:3] == 0.0) and np.all(np.isneginf(lse[:, :3]))
+    assert np.array_equal(np.isneginf(lse), np.isneginf(lr))
+    assert max_abs(O, Or) <= ATTN_BF16_O_TOL
+    assert max_abs(lse[:, 3:], lr[:, 3:]) <= ATTN_BF16_LSE_TOL
+    device_error_clear()
