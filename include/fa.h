@@ -236,6 +236,7 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  *   fp32 per-tile amax of V [B, H, T], fp32 sv [B, H].
  *   d: 128 only.  Size limits: ceil(N / 128) <= 65535 and
  *   3 * B * H * ceil(N / 128) < 2^31 (FA_ERR_TOO_LARGE otherwise).
+ *   Packed batches: fa_attention_fwd_fp8_varlen.
  * Three kernels run on the library stream; no synchronisation.
  * Errors: FA_ERR_UNSUPPORTED (d != 128), FA_ERR_BAD_SIZE (also a workspace
  * that is too small), FA_ERR_NULL_POINTER, FA_ERR_MISALIGNED, FA_ERR_TOO_LARGE,
@@ -247,6 +248,33 @@ FA_API int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, voi
 
 /* Workspace bytes fa_attention_fwd_fp8 needs, or a negative FA_ERR_* code. */
 FA_API int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_attention_fwd_fp8 for packed sequences ("第二十二课…" §三十五: variable-length
+ * sequences stored one after another, none attending to another).  Each
+ * sequence is quantised on its own: Q and K tiles of 128 rows from the
+ * sequence's first token (a tile cut by the sequence's end takes its amax over
+ * the sequence's rows only), one V scale per (sequence, head).
+ *   Q, K, V, O: bf16 [total, H, d]; lse: fp32 [H, total]; cu_seqlens: DEVICE
+ *   int32 [B + 1], non-decreasing from 0 to total; N: the longest sequence (an
+ *   upper bound is fine; it sizes the tile grid and the workspace); total: the
+ *   packed row count (= cu_seqlens[B]; nothing is read back).
+ *   workspace: at least fa_attention_fp8_varlen_workspace_bytes(B, H, N, total,
+ *   d) bytes, laid out as for the dense call with [total, H, d] code arrays
+ *   and per-sequence padded V'^T [B, H, d, 128 ceil(N / 128)].
+ *   causal: key j of a sequence visible to its query i iff j <= i.
+ * A sequence longer than N is not computed and sets FA_DEVERR_BAD_SEQLENS.
+ * Errors: as fa_attention_fwd_fp8, and FA_ERR_NULL_POINTER for a NULL
+ * cu_seqlens.
+ */
+FA_API int fa_attention_fwd_fp8_varlen(const void *Q, const void *K, const void *V, void *O,
+                                       float *lse, int B, int H, int N, int64_t total, int d,
+                                       float scale, int causal, const int32_t *cu_seqlens,
+                                       const float *signs, void *workspace,
+                                       int64_t workspace_bytes);
+
+/* Workspace bytes fa_attention_fwd_fp8_varlen needs, or a negative FA_ERR_* code. */
+FA_API int64_t fa_attention_fp8_varlen_workspace_bytes(int B, int H, int N, int64_t total, int d);
 
 /*
  * bf16 attention forward on HOST buffers: the same result as fa_attention_fwd

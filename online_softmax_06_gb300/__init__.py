@@ -10,7 +10,7 @@ Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_attention_fwd_splitkv_varlen``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
 ``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_bwd_varlen``,
-``fa_attention_fwd_fp8``,
+``fa_attention_fwd_fp8``, ``fa_attention_fwd_fp8_varlen``,
 ``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
 ``fa_attention_host_workspace_bytes``,
 ``fa_set_stream``, ``fa_get_stream``, ``fa_get_device_error``, ``fa_strerror``,
@@ -85,6 +85,10 @@ def lib():
         L.fa_attention_fwd_splitkv_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                       i64, i64, i32, f32, i32, i32, vp, vp, vp,
                                                       vp]
+        L.fa_attention_fwd_fp8_varlen.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i64, i32, f32,
+                                                  i32, vp, vp, vp, i64]
+        L.fa_attention_fp8_varlen_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
+        L.fa_attention_fp8_varlen_workspace_bytes.restype = i64
         L.fa_attention_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
                                               i32, i64, i32, f32, i32, vp]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -101,7 +105,7 @@ def lib():
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
                      "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
                      "fa_attention_bwd_varlen", "fa_attention_fwd_splitkv_varlen",
-                     "fa_attention_fwd_fp8",
+                     "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
                      "fa_attention_fwd_host",
                      "fa_set_stream", "fa_get_device_error", "fa_version",
                      "fa_debug_expire_next_wait"):
@@ -173,6 +177,16 @@ def fa_attention_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, causal, signs, work
 
 def fa_attention_fp8_workspace_bytes(B, H, N, d) -> int:
     return lib().fa_attention_fp8_workspace_bytes(B, H, N, d)
+
+
+def fa_attention_fwd_fp8_varlen(q, k, v, o, lse, B, H, N, total, d, scale, causal, cu_seqlens,
+                                signs, workspace, workspace_bytes) -> int:
+    return lib().fa_attention_fwd_fp8_varlen(q, k, v, o, lse, B, H, N, total, d, scale, causal,
+                                             cu_seqlens, signs, workspace, workspace_bytes)
+
+
+def fa_attention_fp8_varlen_workspace_bytes(B, H, N, total, d) -> int:
+    return lib().fa_attention_fp8_varlen_workspace_bytes(B, H, N, total, d)
 
 
 def fa_attention_fwd_host(q, k, v, o, lse, B, H, N, d, scale, causal, workspace,
@@ -386,12 +400,15 @@ def attention_fwd_splitkv_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen
 
 
 def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None = None,
-                      workspace=None):
-    """FP8 attention forward through the C ABI (bf16 dense [B, N, H, d], d = 128).
+                      workspace=None, cu_seqlens=None, max_seqlen: int | None = None):
+    """FP8 attention forward through the C ABI (bf16 inputs, d = 128).
 
-    ``signs``: float32 CUDA tensor [d] of +-1.  The workspace (uint8, sized by
-    fa_attention_fp8_workspace_bytes) is allocated here unless given.
-    Returns (O [B, N, H, d] bf16, lse [B, H, N] fp32, workspace).
+    Dense: q, k, v [B, N, H, d] -> (O [B, N, H, d], lse [B, H, N]).  Packed:
+    [total, H, d] with ``cu_seqlens`` (int32 CUDA [B+1]) and ``max_seqlen`` ->
+    (O [total, H, d], lse [H, total]).  ``signs``: float32 CUDA tensor [d] of
+    +-1.  The workspace (uint8, sized by fa_attention_fp8_workspace_bytes or
+    its packed counterpart) is allocated here unless given.  Returns
+    (O, lse, workspace).
     """
     import torch
     for t in (q, k, v):
@@ -399,21 +416,38 @@ def attention_fwd_fp8(q, k, v, signs, causal: bool = False, scale: float | None 
             raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
         if t.shape != q.shape:
             raise ValueError("q, k, v must have one shape")
-    B, N, H, d = q.shape
+    if cu_seqlens is None:
+        B, N, H, d = q.shape
+        nbytes = fa_attention_fp8_workspace_bytes(B, H, N, d)
+        lse_shape = (B, H, N)
+    else:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        tot, H, d = q.shape
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen) if max_seqlen is not None else tot
+        nbytes = fa_attention_fp8_varlen_workspace_bytes(B, H, N, tot, d)
+        lse_shape = (H, tot)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    nbytes = fa_attention_fp8_workspace_bytes(B, H, N, d)
     if nbytes < 0:
         raise FaError(int(nbytes), "fa_attention_fp8_workspace_bytes")
     if workspace is None:
         workspace = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=q.device)
     _use_current_stream(q.device)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = fa_attention_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                              float(scale), int(bool(causal)), _ptr(signs), _ptr(workspace),
-                              workspace.numel())
-    _check(rc, "fa_attention_fwd_fp8")
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    if cu_seqlens is None:
+        rc = fa_attention_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                  float(scale), int(bool(causal)), _ptr(signs), _ptr(workspace),
+                                  workspace.numel())
+        _check(rc, "fa_attention_fwd_fp8")
+    else:
+        rc = fa_attention_fwd_fp8_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N,
+                                         q.shape[0], d, float(scale), int(bool(causal)),
+                                         _ptr(cu_seqlens), _ptr(signs), _ptr(workspace),
+                                         workspace.numel())
+        _check(rc, "fa_attention_fwd_fp8_varlen")
     return o, lse, workspace
 
 
@@ -511,7 +545,7 @@ __all__ = [
     "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
     "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "attention_fwd_fp8",
-    "fa_attention_fwd_fp8",
+    "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
     "fa_attention_fp8_workspace_bytes",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",
     "fa_set_stream", "fa_get_stream", "fa_get_device_error", "fa_version",

@@ -910,7 +910,7 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     if (a.d != 128)
         return FA_ERR_UNSUPPORTED;
     Bf16Params p{};
-    const int64_t total = int64_t(a.B) * a.N;
+    const int64_t total = a.cu_seqlens != nullptr ? a.total : int64_t(a.B) * a.N;
     if (!make_tmap_e4m3_rows(&p.tm_q, a.Qf, total, a.H, a.d) ||
         !make_tmap_e4m3_rows(&p.tm_k, a.Kf, total, a.H, a.d) ||
         !make_tmap_e4m3_vt(&p.tm_v, a.Vt, int64_t(a.B) * a.H * a.d, a.n_pad, a.d) ||
@@ -935,7 +935,7 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
     p.total = total;
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
-    p.cu_seqlens = nullptr;
+    p.cu_seqlens = a.cu_seqlens;
     p.cu_seqlens_k = nullptr;
     p.total_k = total;
     p.err_word = a.err_word;

@@ -144,13 +144,14 @@ struct Fp8Layout {
     int n_tiles, n_pad;
 };
 
-Fp8Layout fp8_layout(int B, int H, int N, int d)
+// total: the rows of Q, K, V (B * N dense; the packed row count otherwise)
+Fp8Layout fp8_layout(int B, int H, int N, int d, int64_t total)
 {
     auto up = [](int64_t x) { return (x + 255) & ~int64_t(255); };
     Fp8Layout L;
     L.n_tiles = (N + 127) / 128;
     L.n_pad = L.n_tiles * 128;
-    const int64_t elems = int64_t(B) * N * H * d;
+    const int64_t elems = total * H * d;
     const int64_t tiles = int64_t(B) * H * L.n_tiles;
     int64_t off = 0;
     L.qf = off;
@@ -485,42 +486,39 @@ int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, const v
                                     scale, causal, cu_seqlens);
 }
 
-int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d)
-{
-    if (B < 0 || H < 0 || N < 0)
-        return FA_ERR_BAD_SIZE;
-    if (d != 128)
-        return FA_ERR_UNSUPPORTED;
-    return fa::fp8_layout(B, H, N, d).bytes;
-}
+}  // extern "C"
 
-int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
-                         int H, int N, int d, float scale, int causal, const float *signs,
-                         void *workspace, int64_t workspace_bytes)
+namespace fa {
+namespace {
+// Shared by the dense and packed FP8 entry points.
+int attention_fp8_common(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                         int H, int N, int64_t total, int d, float scale, int causal,
+                         const int32_t *cu_seqlens, const float *signs, void *workspace,
+                         int64_t workspace_bytes)
 {
-    if (B < 0 || H < 0 || N < 0 || workspace_bytes < 0)
+    if (B < 0 || H < 0 || N < 0 || total < 0 || workspace_bytes < 0)
         return FA_ERR_BAD_SIZE;
     if (d != 128)
         return FA_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || N == 0)
+    if (B == 0 || H == 0 || N == 0 || total == 0)
         return FA_OK;
     if (!Q || !K || !V || !O || !lse || !signs || !workspace)
         return FA_ERR_NULL_POINTER;
-    if (!fa::aligned(Q, 16) || !fa::aligned(K, 16) || !fa::aligned(V, 16) ||
-        !fa::aligned(O, 16) || !fa::aligned(lse, 4) || !fa::aligned(signs, 4) ||
-        !fa::aligned(workspace, 256))
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+        !aligned(lse, 4) || !aligned(signs, 4) || !aligned(workspace, 256) ||
+        (cu_seqlens && !aligned(cu_seqlens, 4)))
         return FA_ERR_MISALIGNED;
-    const int64_t total = int64_t(B) * N;
-    if (total > (int64_t(1) << 31) - 512 || total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
+    if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
+        total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
-    const fa::Fp8Layout L = fa::fp8_layout(B, H, N, d);
+    const Fp8Layout L = fp8_layout(B, H, N, d, total);
     if (workspace_bytes < L.bytes)
         return FA_ERR_BAD_SIZE;
-    fa::DeviceInfo *dev = fa::current_device();
+    DeviceInfo *dev = current_device();
     if (dev == nullptr)
         return FA_ERR_NO_DEVICE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    fa::Fp8QuantArgs q;
+    Fp8QuantArgs q;
     q.Q = Q;
     q.K = K;
     q.V = V;
@@ -537,10 +535,12 @@ int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, f
     q.N = N;
     q.d = d;
     q.err_word = dev->err_word;
-    int rc = fa::launch_fp8_quantize(q, fa::t_stream);
+    q.cu_seqlens = cu_seqlens;
+    q.total = total;
+    int rc = launch_fp8_quantize(q, t_stream);
     if (rc != FA_OK)
         return rc;
-    fa::AttnFp8Args a;
+    AttnFp8Args a;
     a.Qf = q.Qf;
     a.Kf = q.Kf;
     a.Vt = q.Vt;
@@ -557,7 +557,52 @@ int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, f
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.err_word = dev->err_word;
-    return fa::launch_attention_fp8(a, fa::t_stream);
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    return launch_attention_fp8(a, t_stream);
+}
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int64_t fa_attention_fp8_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return fa::fp8_layout(B, H, N, d, int64_t(B) * N).bytes;
+}
+
+int64_t fa_attention_fp8_varlen_workspace_bytes(int B, int H, int N, int64_t total, int d)
+{
+    if (B < 0 || H < 0 || N < 0 || total < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return fa::fp8_layout(B, H, N, d, total).bytes;
+}
+
+int fa_attention_fwd_fp8(const void *Q, const void *K, const void *V, void *O, float *lse, int B,
+                         int H, int N, int d, float scale, int causal, const float *signs,
+                         void *workspace, int64_t workspace_bytes)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    return fa::attention_fp8_common(Q, K, V, O, lse, B, H, N, int64_t(B) * N, d, scale, causal,
+                                    nullptr, signs, workspace, workspace_bytes);
+}
+
+int fa_attention_fwd_fp8_varlen(const void *Q, const void *K, const void *V, void *O, float *lse,
+                                int B, int H, int N, int64_t total, int d, float scale,
+                                int causal, const int32_t *cu_seqlens, const float *signs,
+                                void *workspace, int64_t workspace_bytes)
+{
+    if (cu_seqlens == nullptr)
+        return FA_ERR_NULL_POINTER;
+    return fa::attention_fp8_common(Q, K, V, O, lse, B, H, N, total, d, scale, causal,
+                                    cu_seqlens, signs, workspace, workspace_bytes);
 }
 
 int64_t fa_attention_host_workspace_bytes(int B, int H, int N, int d)

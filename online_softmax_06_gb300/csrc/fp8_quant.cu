@@ -72,10 +72,15 @@ constexpr uint32_t kQkTmemCols = 256;                // two 128-column accumulat
 static_assert(kQkSmemBytes <= 227 * 1024, "shared memory");
 
 struct QkMmaParams {
-    CUtensorMap tm_x[3];              // Q, K, V: bf16 [B, N, H, 128], box {64, 1, 128, 1}
-    CUtensorMap tm_f[2];              // Q', K': e4m3 [B, N, H, 128], box {128, 1, 128, 1}
+    // dense: 4-D maps over [B, N, H, 128], boxes {64, 1, 128, 1} (bf16) and
+    // {128, 1, 128, 1} (e4m3); packed: 3-D maps over [total, H, 128], boxes
+    // {64, 1, 128} and {128, 1, 128}
+    CUtensorMap tm_x[3];              // Q, K, V (bf16)
+    CUtensorMap tm_f[2];              // Q', K' (e4m3)
     const float *signs;               // [128], +-1
     float *sq, *sk, *vamax;           // [B, H, n_tiles]
+    uint8_t *Qf, *Kf;                 // packed: the codes' rows, for ragged tiles
+    const int32_t *cu_seqlens;        // packed: [B + 1] prefix sums (else nullptr)
     int H, n_tiles, BH, n_items;
     int *err_word;
 };
@@ -108,7 +113,10 @@ __device__ __forceinline__ void drain(uint64_t *bar, uint32_t parity)
 struct Item {
     int which, b, h, tile;
     int64_t sidx;                     // (b * H + h) * n_tiles + tile
+    int64_t row0;                     // packed: the tile's first row of [total, H, d]
+    int valid;                        // rows of the tile inside the sequence (<= 0: none)
 };
+template <bool PACKED>
 __device__ __forceinline__ Item decode_item(const QkMmaParams &p, int j)
 {
     Item it;
@@ -119,9 +127,20 @@ __device__ __forceinline__ Item decode_item(const QkMmaParams &p, int j)
     it.b = bh / p.H;
     it.h = bh % p.H;
     it.sidx = int64_t(bh) * p.n_tiles + it.tile;
+    it.row0 = 0;
+    it.valid = kRows;                 // dense: the 4-D maps clip the sequence's end
+    if constexpr (PACKED) {
+        const int64_t s0 = p.cu_seqlens[it.b], s1 = p.cu_seqlens[it.b + 1];
+        it.row0 = s0 + int64_t(it.tile) * kRows;
+        const int64_t v = s1 - it.row0;
+        it.valid = v < kRows ? int(v) : kRows;
+    }
     return it;
 }
 
+// PACKED: sequences from cu_seqlens over [total, H, d] (3-D maps); the dense
+// instantiation keeps the 4-D maps and whole-tile stores.
+template <bool PACKED>
 __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_constant__ QkMmaParams p)
 {
     constexpr int D = 128;
@@ -176,15 +195,26 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
             int stage = 0;
             uint32_t phase = 0;
             for (int j = int(blockIdx.x); j < p.n_items; j += int(gridDim.x)) {
+                const Item it = decode_item<PACKED>(p, j);
+                if (it.valid <= 0)
+                    continue;                      // a tile past its sequence's end
                 if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err_word))
                     break;
-                const Item it = decode_item(p, j);
                 uint8_t *dst = ring + stage * kStageBytes;
                 ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-                ptx::tma_load_4d(dst, &p.tm_x[it.which], &full[stage], 0, it.h, it.tile * kRows,
-                                 it.b);
-                ptx::tma_load_4d(dst + kChunk, &p.tm_x[it.which], &full[stage], 64, it.h,
-                                 it.tile * kRows, it.b);
+                if constexpr (PACKED) {
+                    // rows past the sequence's end are the next one's: the
+                    // epilogue leaves them out of the amax and does not store them
+                    ptx::tma_load_3d(dst, &p.tm_x[it.which], &full[stage], 0, it.h,
+                                     int(it.row0));
+                    ptx::tma_load_3d(dst + kChunk, &p.tm_x[it.which], &full[stage], 64, it.h,
+                                     int(it.row0));
+                } else {
+                    ptx::tma_load_4d(dst, &p.tm_x[it.which], &full[stage], 0, it.h,
+                                     it.tile * kRows, it.b);
+                    ptx::tma_load_4d(dst + kChunk, &p.tm_x[it.which], &full[stage], 64, it.h,
+                                     it.tile * kRows, it.b);
+                }
                 last_phase[stage] = int(phase);
                 if (++stage == kQkStages) {
                     stage = 0;
@@ -207,7 +237,10 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
         int stage = 0, abuf = 0;
         uint32_t phase = 0, aphase = 0;
         for (int j = int(blockIdx.x); j < p.n_items; j += int(gridDim.x)) {
-            const int which = (j / p.n_tiles) / p.BH;
+            const Item itm = decode_item<PACKED>(p, j);
+            if (itm.valid <= 0)
+                continue;                          // skipped by every role alike
+            const int which = itm.which;
             const int st = stage;
             const uint32_t ph = phase;
             if (++stage == kQkStages) {
@@ -279,7 +312,10 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
         int stage = 0, abuf = 0, ob = 0, ib = 0;
         uint32_t phase = 0, aphase = 0;
         for (int j = int(blockIdx.x); j < p.n_items; j += int(gridDim.x)) {
-            const Item it = decode_item(p, j);
+            const Item it = decode_item<PACKED>(p, j);
+            if (it.valid <= 0)
+                continue;                          // skipped by every role alike
+            const bool row_in = !PACKED || r < it.valid;   // this thread's row is in the sequence
             const int st = stage;
             const uint32_t ph = phase;
             if (++stage == kQkStages) {
@@ -294,7 +330,7 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
                 // that a warp's loads fall in distinct banks
                 const bool ok = warp_wait(&full[st], ph, abort_flag, p.err_word);
                 uint32_t m = 0;                  // two |bf16| maxima, as bf16x2
-                if (ok) {
+                if (ok && row_in) {
                     const uint8_t *src = ring + st * kStageBytes;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
@@ -342,6 +378,8 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
                         amax = ptx::max3(amax, fabsf(__uint_as_float(v[e])),
                                          fabsf(__uint_as_float(v[e + 1])));
                 }
+                if (!row_in)
+                    amax = 0.f;                  // a row of the next sequence
             }
             amax = warp_max(amax) * inv_d;
             if (lane == 0)
@@ -355,8 +393,11 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
             if (et == 0)
                 (it.which == 0 ? p.sq : p.sk)[it.sidx] = scale;
             const float mul = inv_d * (1.f / scale);
-            // pass 2: the codes of row r into staging tile ob
+            // pass 2: the codes of row r into staging tile ob, or, for a
+            // packed tile cut by its sequence's end, straight to its row
+            const bool ragged = PACKED && it.valid < kRows;
             uint8_t *row = out + ob * kChunk + r * 128;
+            uint8_t *grow = (it.which == 0 ? p.Qf : p.Kf) + ((it.row0 + r) * p.H + it.h) * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -369,6 +410,14 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
                                             __uint_as_float(v[4 * k + 1]) * mul,
                                             __uint_as_float(v[4 * k + 2]) * mul,
                                             __uint_as_float(v[4 * k + 3]) * mul);
+                if (ragged) {
+                    if (row_in) {
+                        *reinterpret_cast<uint4 *>(grow + 32 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(grow + 32 * c + 16) =
+                            make_uint4(w[4], w[5], w[6], w[7]);
+                    }
+                    continue;
+                }
                 *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
@@ -380,9 +429,13 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
                 ptx::mbar_arrive(&acc_empty[abuf]);  // this warp's accumulator rows are read
             ptx::fence_proxy_async_smem();       // staged codes -> the TMA store
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-            if (et == 0) {
-                ptx::tma_store_4d(&p.tm_f[it.which], out + ob * kChunk, 0, it.h,
-                                  it.tile * kRows, it.b);
+            if (et == 0 && !ragged) {
+                if constexpr (PACKED)
+                    ptx::tma_store_3d(&p.tm_f[it.which], out + ob * kChunk, 0, it.h,
+                                      int(it.row0));
+                else
+                    ptx::tma_store_4d(&p.tm_f[it.which], out + ob * kChunk, 0, it.h,
+                                      it.tile * kRows, it.b);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
             ob ^= 1;
@@ -404,9 +457,10 @@ __global__ void __launch_bounds__(kQkThreads, 1) fp8_qk_mma_kernel(const __grid_
 
 struct VtParams {
     CUtensorMap tm_vt;                // Vt: e4m3 [B*H*d, n_pad], box {128 keys, 128 rows}
-    const __nv_bfloat16 *V;
+    const __nv_bfloat16 *V;           // dense [B, N, H, d]; packed [total, H, d]
     const float *vamax;               // [B, H, n_tiles]
     float *sv;                        // [B, H]
+    const int32_t *cu_seqlens;        // packed: [B + 1] prefix sums (else nullptr)
     int B, H, N, n_tiles;
 };
 
@@ -429,15 +483,26 @@ __global__ void __launch_bounds__(256) fp8_vt_kernel(const __grid_constant__ VtP
     const int b = bh / p.H, h = bh % p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = 16 * warp;
+    // the sequence's first row and length (packed: from the prefix sums);
+    // tiles past its end are never read by the attention kernel
+    int64_t row0 = int64_t(b) * p.N;
+    int L = p.N;
+    if (p.cu_seqlens != nullptr) {
+        row0 = p.cu_seqlens[b];
+        L = int(p.cu_seqlens[b + 1] - row0);
+    }
+    if (tile * kRows >= L)
+        return;
+    const int n_tiles = (L + kRows - 1) / kRows;
     // the tile's loads go out first, then the per-head amax (one tile amax per
     // lane, reduced across the warp), then the conversions
     uint4 raw[4][2];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int key = tile * kRows + 4 * lane + j;
-        if (key < p.N) {
+        if (key < L) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.V + ((int64_t(b) * p.N + key) * p.H + h) * D + c0);
+                p.V + ((row0 + key) * p.H + h) * D + c0);
             raw[j][0] = src[0];
             raw[j][1] = src[1];
         } else {
@@ -450,7 +515,7 @@ __global__ void __launch_bounds__(256) fp8_vt_kernel(const __grid_constant__ VtP
     // the wait, which returns once that kernel has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     float amax = 0.f;
-    for (int t = lane; t < p.n_tiles; t += 32)
+    for (int t = lane; t < n_tiles; t += 32)
         amax = fmaxf(amax, p.vamax[int64_t(bh) * p.n_tiles + t]);
     amax = warp_max(amax);
     const float scale = amax > 0.f ? amax / kE4M3Max : 1.f;
@@ -491,12 +556,23 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
     if (3 * int64_t(a.B) * a.H * n_tiles > 0x7fffffffLL || n_tiles > 65535)
         return FA_ERR_TOO_LARGE;
     QkMmaParams q;
-    if (!make_tmap_seq_4d(&q.tm_x[0], a.Q, false, a.B, a.N, a.H, a.d) ||
-        !make_tmap_seq_4d(&q.tm_x[1], a.K, false, a.B, a.N, a.H, a.d) ||
-        !make_tmap_seq_4d(&q.tm_x[2], a.V, false, a.B, a.N, a.H, a.d) ||
-        !make_tmap_seq_4d(&q.tm_f[0], a.Qf, true, a.B, a.N, a.H, a.d) ||
-        !make_tmap_seq_4d(&q.tm_f[1], a.Kf, true, a.B, a.N, a.H, a.d))
+    if (a.cu_seqlens != nullptr) {
+        if (!make_tmap_bf16(&q.tm_x[0], a.Q, a.total, a.H, a.d) ||
+            !make_tmap_bf16(&q.tm_x[1], a.K, a.total, a.H, a.d) ||
+            !make_tmap_bf16(&q.tm_x[2], a.V, a.total, a.H, a.d) ||
+            !make_tmap_e4m3_rows(&q.tm_f[0], a.Qf, a.total, a.H, a.d) ||
+            !make_tmap_e4m3_rows(&q.tm_f[1], a.Kf, a.total, a.H, a.d))
+            return FA_ERR_CUDA;
+    } else if (!make_tmap_seq_4d(&q.tm_x[0], a.Q, false, a.B, a.N, a.H, a.d) ||
+               !make_tmap_seq_4d(&q.tm_x[1], a.K, false, a.B, a.N, a.H, a.d) ||
+               !make_tmap_seq_4d(&q.tm_x[2], a.V, false, a.B, a.N, a.H, a.d) ||
+               !make_tmap_seq_4d(&q.tm_f[0], a.Qf, true, a.B, a.N, a.H, a.d) ||
+               !make_tmap_seq_4d(&q.tm_f[1], a.Kf, true, a.B, a.N, a.H, a.d)) {
         return FA_ERR_CUDA;
+    }
+    q.Qf = a.Qf;
+    q.Kf = a.Kf;
+    q.cu_seqlens = a.cu_seqlens;
     q.signs = a.signs;
     q.sq = a.sq;
     q.sk = a.sk;
@@ -511,12 +587,14 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         sms <= 0)
         return FA_ERR_CUDA;
-    static PerDeviceOnce once_qk;
-    if (!set_max_dynamic_smem(once_qk, reinterpret_cast<const void *>(fp8_qk_mma_kernel),
-                              int(kQkSmemBytes)))
+    static PerDeviceOnce once_qk, once_qk_packed;
+    const bool packed = a.cu_seqlens != nullptr;
+    auto kqk = packed ? fp8_qk_mma_kernel<true> : fp8_qk_mma_kernel<false>;
+    if (!set_max_dynamic_smem(packed ? once_qk_packed : once_qk,
+                              reinterpret_cast<const void *>(kqk), int(kQkSmemBytes)))
         return FA_ERR_CUDA;
     const int grid = q.n_items < sms ? q.n_items : sms;
-    fp8_qk_mma_kernel<<<grid, kQkThreads, kQkSmemBytes, stream>>>(q);
+    kqk<<<grid, kQkThreads, kQkSmemBytes, stream>>>(q);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     VtParams v;
@@ -526,6 +604,7 @@ int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream)
     v.V = static_cast<const __nv_bfloat16 *>(a.V);
     v.vamax = a.vamax;
     v.sv = a.sv;
+    v.cu_seqlens = a.cu_seqlens;
     v.B = a.B;
     v.H = a.H;
     v.N = a.N;

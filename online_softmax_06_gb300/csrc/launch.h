@@ -102,6 +102,8 @@ struct AttnFp8Args {
     float scale;
     int causal;
     int *err_word;
+    const int32_t *cu_seqlens = nullptr;  // packed: [B + 1] prefix sums; N = longest
+    int64_t total = 0;                    // packed: rows of Q, K, V, O
 };
 int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream);
 
@@ -131,6 +133,8 @@ struct Fp8QuantArgs {
     float *sv;                 // [B, H]
     int B, H, N, d;
     int *err_word;             // device error word (bounded waits)
+    const int32_t *cu_seqlens = nullptr;  // packed: [B + 1]; Q, K, V, Qf, Kf [total, H, d]
+    int64_t total = 0;
 };
 int launch_fp8_quantize(const Fp8QuantArgs &a, cudaStream_t stream);
 

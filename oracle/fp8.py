@@ -141,3 +141,27 @@ def fp8_attention(Q, K, V, signs, scale, causal, per_tensor_scales=False, rotate
     # 2^-4)
     return attention_dense(Qd.astype(np.float32), Kd.astype(np.float32),
                            Vd.astype(np.float32), scale, causal, lib=lib)
+
+
+def fp8_attention_packed(Q, K, V, cu_seqlens, signs, scale, causal, lib=None):
+    """The FP8 method on packed sequences: each sequence is quantised on its
+    own (Q and K tiles of 128 rows from the sequence's first token, one V scale
+    per (sequence, head)) and attends only to itself.
+
+    Q, K, V: [total, H, d]; cu_seqlens: [B+1].  Returns (O [total, H, d],
+    lse [H, total]) in float64."""
+    Q, K, V = (np.asarray(X) for X in (Q, K, V))
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    total, H, d = Q.shape
+    O = np.zeros((total, H, d))
+    lse = np.zeros((H, total))
+    for b in range(cu.size - 1):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        Ob, lb = fp8_attention(Q[None, s0:s1], K[None, s0:s1], V[None, s0:s1], signs, scale,
+                               causal, lib=lib)
+        O[s0:s1] = Ob[0]
+        lse[:, s0:s1] = lb[0]
+    return O, lse
+

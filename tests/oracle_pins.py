@@ -676,6 +676,24 @@ def pin_fp8_v_codes_fp32(lib):
     assert np.all(step <= spacing[diff] * (1 + 1e-12)), "only neighbouring codes may differ"
 
 
+def pin_fp8_packed_matches_dense(lib):
+    """The packed FP8 reference with equal lengths equals the dense batch's
+    (each sequence quantised on its own), and the row statistics land in the
+    packed [H, total] layout."""
+    from oracle import fp8
+    rng = np.random.default_rng(45)
+    B, N, H, d = 3, 150, 2, 128
+    Q, K, V = (rng.standard_normal((B, N, H, d)).astype(np.float32) for _ in range(3))
+    signs = rng.choice([-1.0, 1.0], size=d)
+    cu = np.arange(B + 1) * N
+    for causal in (False, True):
+        O, lse = fp8.fp8_attention(Q, K, V, signs, 0.09, causal, lib=lib)
+        Op, lp = fp8.fp8_attention_packed(*(X.reshape(B * N, H, d) for X in (Q, K, V)), cu,
+                                          signs, 0.09, causal, lib=lib)
+        _close(Op, O.reshape(B * N, H, d), 0.0, "fp8 packed O")
+        _close(lp, lse.transpose(1, 0, 2).reshape(H, B * N), 0.0, "fp8 packed lse")
+
+
 def pin_fp8_hadamard_vs_scipy(lib):
     """The Sylvester construction equals scipy's Hadamard matrix."""
     from scipy.linalg import hadamard

@@ -49,10 +49,10 @@ def run(qkv, signs, causal, dev):
     return o.float().cpu().numpy(), lse.cpu().numpy(), ws.cpu().numpy()
 
 
-def layout(B, H, N, d):
+def layout(B, H, N, d, total=None):
     up = lambda x: (x + 255) & ~255
     T = (N + 127) // 128
-    elems = B * N * H * d
+    elems = (B * N if total is None else total) * H * d
     qf = 0
     kf = up(qf + elems)
     vt = up(kf + elems)
@@ -225,6 +225,104 @@ def test_fp8_many_heads(dev):
     O, lse, _ = run(qkv, signs, True, dev)
     device_error_clear()
     check_against_reference(O, lse, qkv, signs, True, "many heads")
+
+
+# ---------------------------------------------------------------------------
+# packed sequences
+# ---------------------------------------------------------------------------
+
+def make_packed(lens, H, d, seed):
+    rng = np.random.default_rng(seed)
+    total = int(sum(lens))
+    xs = [rng.standard_normal((total, H, d)) for _ in range(3)]
+    qkv = [torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16) for x in xs]
+    signs = rng.choice([-1.0, 1.0], size=d).astype(np.float32)
+    return qkv, signs
+
+
+def run_packed(qkv, signs, lens, causal, dev):
+    import workloads
+    q, k, v = (t.to(dev) for t in qkv)
+    cu = torch.from_numpy(workloads.cu_seqlens_of(lens)).to(dev)
+    o, lse, ws = fa.attention_fwd_fp8(q, k, v, torch.from_numpy(signs).to(dev), causal=causal,
+                                      cu_seqlens=cu, max_seqlen=max(lens))
+    torch.cuda.synchronize(dev)
+    return o.float().cpu().numpy(), lse.cpu().numpy(), ws.cpu().numpy()
+
+
+PACKED_LENS = [1, 129, 300, 0, 256, 700]    # ragged tiles, an empty sequence, whole tiles
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_packed_quantisation_matches_reference(dev, causal):
+    """Each sequence is quantised on its own: its Q', K' tile scales and codes
+    (tiles from its first token, a ragged last tile taking its amax over the
+    sequence's rows only) and its V' codes and scale against the reference run
+    on that sequence alone; no tile writes into another sequence's rows."""
+    import workloads
+    H, d = 2, 128
+    qkv, signs = make_packed(PACKED_LENS, H, d, seed=61 + causal)
+    _, _, ws = run_packed(qkv, signs, PACKED_LENS, causal, dev)
+    cu = workloads.cu_seqlens_of(PACKED_LENS)
+    B, N, total = len(PACKED_LENS), max(PACKED_LENS), int(cu[-1])
+    L = layout(B, H, N, d, total)
+    T = L["T"]
+    for name, X, off, soff in (("Q", qkv[0], L["qf"], L["sq"]), ("K", qkv[1], L["kf"], L["sk"])):
+        got_scales = ws[soff:soff + B * H * T * 4].view(np.float32).reshape(B, H, T)
+        codes = ws[off:off + total * H * d].reshape(total, H, d)
+        for b in range(B):
+            s0, s1 = int(cu[b]), int(cu[b + 1])
+            if s1 == s0:
+                continue
+            Xr = fp8.rotate(X[s0:s1].float().numpy()[None], signs)
+            _, ref_scales = fp8.blockwise_qk(Xr)
+            nt = ref_scales.shape[2]
+            assert np.allclose(got_scales[b, :, :nt], ref_scales[0], rtol=1e-5), (name, b)
+            per_row = np.repeat(ref_scales, 128, axis=2)[:, :, :s1 - s0].transpose(0, 2, 1)[..., None]
+            assert_codes_match(codes[None, s0:s1], fp8.e4m3_round(Xr / per_row), f"{name} seq {b}")
+    n_pad = 128 * T
+    vt = ws[L["vt"]:L["vt"] + B * H * d * n_pad].reshape(B, H, d, n_pad)
+    got_sv = ws[L["sv"]:L["sv"] + B * H * 4].view(np.float32).reshape(B, H)
+    for b in range(B):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        ref, ref_sv = fp8.per_head_v_fp32(qkv[2][s0:s1].float().numpy()[None])
+        assert np.array_equal(got_sv[b], ref_sv[0]), b
+        got = e4m3_decode(np.ascontiguousarray(vt[b, :, :, :s1 - s0]))       # [H, d, L]
+        assert np.array_equal(got, ref[0].transpose(1, 2, 0)), f"V' codes seq {b}"
+        assert not np.any(vt[b, :, :, s1 - s0:128 * ((s1 - s0 + 127) // 128)]), "padding keys"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_packed_matches_reference(dev, causal):
+    """O and lse of every row of a packed batch against the reference run
+    sequence by sequence (the lse bound of check_against_reference, per
+    sequence)."""
+    import workloads
+    H, d = 2, 128
+    qkv, signs = make_packed(PACKED_LENS, H, d, seed=71 + causal)
+    O, lse, _ = run_packed(qkv, signs, PACKED_LENS, causal, dev)
+    device_error_clear()
+    cu = workloads.cu_seqlens_of(PACKED_LENS)
+    for b in range(len(PACKED_LENS)):
+        s0, s1 = int(cu[b]), int(cu[b + 1])
+        if s1 == s0:
+            continue
+        seq = [t[s0:s1][None] for t in qkv]
+        check_against_reference(O[None, s0:s1], lse[None, :, s0:s1], seq, signs, causal,
+                                f"packed seq {b} ({s1 - s0} tokens)")
+
+
+def test_fp8_packed_equal_lengths_is_the_dense_call(dev):
+    """Packed sequences of one length give the dense call's bits."""
+    B, H, N, d = 2, 3, 300, 128
+    (Q, K, V), signs = make(B, H, N, d, seed=81)
+    O_d, l_d, _ = run((Q, K, V), signs, True, dev)
+    O_p, l_p, _ = run_packed([t.reshape(B * N, H, d) for t in (Q, K, V)], signs, [N] * B, True,
+                             dev)
+    assert np.array_equal(O_p, O_d.reshape(B * N, H, d))
+    assert np.array_equal(l_p, l_d.transpose(1, 0, 2).reshape(H, B * N))
 
 
 def test_fp8_bad_arguments(dev):
