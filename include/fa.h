@@ -215,6 +215,38 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
                                    int d, float scale, int causal, const int32_t *cu_seqlens);
 
 /*
+ * fa_attention_bwd in one pass over the key tiles, with dQ summed by atomic
+ * adds ("少搬一趟…" §3.3: the backward is split along the K, V column blocks,
+ * one block per CTA, and the blocks' overlapping contributions to dQ are
+ * summed with atomic additions; §5.6).  Each CTA forms dK and dV of its 128
+ * keys and its share dS K of dQ for every 64 queries it sees; the shares are
+ * added in fp32 into `workspace` by TMA reduce-adds in L2, and a last kernel
+ * writes dQ = scale * sum in bf16.  S and dP are formed once (five products
+ * instead of fa_attention_bwd's seven).
+ *   Arguments, layouts and the result's definition: as fa_attention_bwd
+ *   (dense batches; D_buf receives D_i).  d: 128 only.
+ *   workspace: DEVICE fp32 scratch owned by the caller, 256-byte aligned, at
+ *   least fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) bytes
+ *   ([B * H * d, N rounded up to 64]); contents on entry are ignored (the
+ *   first kernel zeroes it).
+ * The order of the reduce-adds is not fixed, so dQ may differ from run to run
+ * in its last bits; dK and dV are reproducible.  fa_attention_bwd is the
+ * deterministic form ("少搬一趟…" §5.6 offers one for the same reason).
+ * Three kernels run on the library stream (D_i and zeroing, the pass, the dQ
+ * conversion); no synchronisation.
+ * Errors: as fa_attention_bwd; FA_ERR_UNSUPPORTED for d != 128;
+ * FA_ERR_BAD_SIZE also for a workspace that is too small.
+ */
+FA_API int fa_attention_bwd_atomic(const void *Q, const void *K, const void *V, const void *O,
+                                   const void *dO, const float *lse, void *dQ, void *dK,
+                                   void *dV, float *D_buf, int B, int H, int N, int d,
+                                   float scale, int causal, void *workspace,
+                                   int64_t workspace_bytes);
+
+/* Workspace bytes fa_attention_bwd_atomic needs, or a negative FA_ERR_* code. */
+FA_API int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * FP8 attention forward ("少搬一趟…" §4.6: FP8 with blockwise quantisation and
  * incoherent processing), for bf16 inputs on dense batches:
  *   1. Q and K rows are multiplied by M = diag(signs) H_d / sqrt(d) (H_d the

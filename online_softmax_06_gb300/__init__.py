@@ -10,6 +10,7 @@ Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_softmax_rows``, ``fa_attention_fwd``, ``fa_attention_fwd_varlen``,
 ``fa_attention_fwd_splitkv``, ``fa_attention_fwd_splitkv_varlen``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
 ``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_bwd_varlen``,
+``fa_attention_bwd_atomic``, ``fa_attention_bwd_atomic_workspace_bytes``,
 ``fa_attention_fwd_fp8``, ``fa_attention_fwd_fp8_varlen``,
 ``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
 ``fa_attention_host_workspace_bytes``,
@@ -93,6 +94,10 @@ def lib():
                                               i32, i64, i32, f32, i32, vp]
         L.fa_attention_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                                        i32, f32, i32, i32]
+        L.fa_attention_bwd_atomic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                              i32, i32, f32, i32, vp, i64]
+        L.fa_attention_bwd_atomic_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.fa_attention_bwd_atomic_workspace_bytes.restype = i64
         L.fa_set_stream.argtypes = [vp]
         L.fa_get_stream.argtypes = []
         L.fa_get_stream.restype = vp
@@ -104,7 +109,8 @@ def lib():
         for name in ("fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen",
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
                      "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
-                     "fa_attention_bwd_varlen", "fa_attention_fwd_splitkv_varlen",
+                     "fa_attention_bwd_varlen", "fa_attention_bwd_atomic",
+                     "fa_attention_fwd_splitkv_varlen",
                      "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
                      "fa_attention_fwd_host",
                      "fa_set_stream", "fa_get_device_error", "fa_version",
@@ -208,6 +214,16 @@ def fa_attention_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, tot
                             causal, cu_seqlens) -> int:
     return lib().fa_attention_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, total,
                                          d, scale, causal, cu_seqlens)
+
+
+def fa_attention_bwd_atomic(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, scale, causal,
+                            workspace, workspace_bytes) -> int:
+    return lib().fa_attention_bwd_atomic(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d,
+                                         scale, causal, workspace, workspace_bytes)
+
+
+def fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) -> int:
+    return lib().fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
 
 
 def fa_set_stream(stream_ptr) -> int:
@@ -494,13 +510,15 @@ def attention_fwd_host(q, k, v, causal: bool = False, scale: float | None = None
 
 
 def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
-                  cu_seqlens=None, max_seqlen: int | None = None):
+                  cu_seqlens=None, max_seqlen: int | None = None, deterministic: bool = True):
     """Attention backward through the C ABI (bf16).
 
     Dense: q, k, v, o, do [B, N, H, d], lse [B, H, N].  Packed: [total, H, d]
     with ``cu_seqlens`` (int32 CUDA [B+1]) and ``max_seqlen``, lse [H, total].
     ``o`` and ``lse`` are the forward's outputs for the same inputs.  The fp32
-    D scratch (lse's shape) is allocated here (torch).  Returns (dq, dk, dv).
+    D scratch (lse's shape) is allocated here (torch).  ``deterministic=False``
+    calls the one-pass form with atomic dQ sums (``fa_attention_bwd_atomic``:
+    dense, d = 128; its fp32 workspace is allocated here).  Returns (dq, dk, dv).
     """
     import torch
     for t in (q, k, v, o, do):
@@ -528,7 +546,16 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
     d_buf = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
             _ptr(d_buf))
-    if cu_seqlens is None:
+    if not deterministic:
+        if cu_seqlens is not None:
+            raise ValueError("the one-pass backward takes dense batches")
+        nbytes = fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
+        _check(int(min(nbytes, 0)), "fa_attention_bwd_atomic_workspace_bytes")
+        ws = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
+        rc = fa_attention_bwd_atomic(*ptrs, B, H, N, d, float(scale), int(bool(causal)), _ptr(ws),
+                                     nbytes)
+        _check(rc, "fa_attention_bwd_atomic")
+    elif cu_seqlens is None:
         rc = fa_attention_bwd(*ptrs, B, H, N, d, float(scale), int(bool(causal)))
         _check(rc, "fa_attention_bwd")
     else:
@@ -544,7 +571,8 @@ __all__ = [
     "fa_attention_fwd_splitkv_varlen",
     "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
-    "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "attention_fwd_fp8",
+    "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "fa_attention_bwd_atomic",
+    "fa_attention_bwd_atomic_workspace_bytes", "attention_fwd_fp8",
     "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
     "fa_attention_fp8_workspace_bytes",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",

@@ -997,6 +997,514 @@ __global__ void __launch_bounds__(kThreads, 1)
     teardown<D>(tmem);
 }
 
+// =============================================================================
+// One-pass backward (d = 128, dense): dK, dV and each key tile's share of dQ
+// =============================================================================
+// One CTA per (sequence, head, 128-key tile), as the dK/dV kernel, that also
+// forms dQ^T_s = K^T dS^T_s for each 64-query sub-step and adds it into an
+// fp32 accumulator [B*H*d, n_pad] in global memory with TMA reduce-adds: the
+// contributions of the key tiles are summed in L2 ("少搬一趟…" §3.3: the
+// column blocks' dQ shares summed with atomic adds; §5.6). The order of those
+// adds varies from run to run, so dQ's rounding may too; dK and dV do not.
+// TMEM: S^T in two buffers [0, 64), [64, 128) (P^T packed into them); dP^T
+// single-buffered in [128, 192); dQ^T in [192, 256) (lanes = head-dim index,
+// columns = queries); dV in [256, 384); dK in [384, 512).
+// Shared memory: K and V resident; a 3-stage ring of (Q_s, dO_s); dS^T in two
+// 16 KB buffers (row = key, 64 queries = 128 bytes, 128-byte swizzle), which
+// is both the K-major A operand of dK += dS^T Q_s and the MN-major B operand
+// of dQ^T = K^T dS^T; one 4 KB staging tile per row warp for its reduce-adds.
+struct CfgF {
+    static constexpr int D = 128;
+    static constexpr int kChunks = D / 64;
+    static constexpr uint32_t kResBytes = BT * D * 2;
+    static constexpr uint32_t kSubBytes = BS * D * 2;
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kStageBytes = 2 * kSubBytes;
+    static constexpr uint32_t kDsBytes = BT * BS * 2;
+    static constexpr uint32_t kStgBytes = 32 * 32 * 4;
+    static constexpr uint32_t kOffA0 = 0;
+    static constexpr uint32_t kOffA1 = kResBytes;
+    static constexpr uint32_t kOffRing = 2 * kResBytes;
+    static constexpr uint32_t kOffDs = kOffRing + kStages * kStageBytes;
+    static constexpr uint32_t kOffStg = kOffDs + 2 * kDsBytes;
+    static constexpr uint32_t kOffStat = kOffStg + kRowWarps * kStgBytes;
+    static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;
+    static constexpr uint32_t kOffBar = kOffStat + kStatBytes;
+    // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], dp_read, dq_full,
+    // dq_free, o_full, drain
+    static constexpr int kBars = 1 + 2 * kStages + 9;
+    static constexpr uint32_t kSmemBytes = kOffBar + 8 * kBars + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+constexpr uint32_t kFColDP = 128, kFColDQ = 192, kFColDV = 256, kFColDK = 384;
+
+template <bool PACKED>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_fused_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_acc)
+{
+    using C = CfgF;
+    constexpr int D = C::D;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *a_full = bars, *kv_full = bars + 1, *kv_empty = bars + 1 + C::kStages;
+    uint64_t *s_full = bars + 1 + 2 * C::kStages;          // [2]
+    uint64_t *p_full = s_full + 2;                          // [2]
+    uint64_t *dp_read = s_full + 4, *dq_full = s_full + 5, *dq_free = s_full + 6,
+             *o_full = s_full + 7, *drain = s_full + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int bh_count = p.B * p.H;
+    const int kt = int(blockIdx.x) / bh_count;       // causal: low key tiles see most
+    const int bh = int(blockIdx.x) % bh_count;
+    const int b = bh / p.H, h = bh % p.H;
+    SeqRows sq;
+    if (!seq_rows<PACKED>(p, b, h, sq) || kt * BT >= sq.L)
+        return;                                      // whole CTA: nothing to do
+    const int64_t row0 = sq.row0;
+    const int L = sq.L;
+    const int n_sub = (L + BS - 1) / BS;
+    const int i0 = p.causal ? 2 * kt : 0;            // first query sub-tile that sees the keys
+    const int n_q = n_sub - i0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(a_full, 1);
+        for (int st = 0; st < C::kStages; ++st) {
+            ptx::mbar_init(&kv_full[st], 32);        // the load warp's lanes stage statistics
+            ptx::mbar_init(&kv_empty[st], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&s_full[i], 1);
+            ptx::mbar_init(&p_full[i], kRowWarps);
+        }
+        ptx::mbar_init(dp_read, kRowWarps);
+        ptx::mbar_init(dq_full, 1);
+        ptx::mbar_init(dq_free, kRowWarps);
+        ptx::mbar_init(o_full, 1);
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kWarpLoad && lane == 0) {
+        ptx::prefetch_tmap(&p.tm_a0);
+        ptx::prefetch_tmap(&p.tm_a1);
+        ptx::prefetch_tmap(&p.tm_s0);
+        ptx::prefetch_tmap(&p.tm_s1);
+        ptx::prefetch_tmap(&tm_acc);
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    bool aborted = false;
+    uint8_t *tile_k = smem + C::kOffA0, *tile_v = smem + C::kOffA1;
+    uint8_t *ring = smem + C::kOffRing;
+    float *stats = reinterpret_cast<float *>(smem + C::kOffStat);   // slot x (lse2, D) x 64
+
+    if (warp == kWarpLoad) {
+        // ======================= TMA producer (whole warp) ===================
+        int last_phase[C::kStages];
+        for (int st = 0; st < C::kStages; ++st)
+            last_phase[st] = -1;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(a_full, 2 * C::kResBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                ptx::tma_load_3d(tile_k + c * kResChunkBytes, &p.tm_a0, a_full, c * 64, h,
+                                 int(row0 + int64_t(kt) * BT));
+                ptx::tma_load_3d(tile_v + c * kResChunkBytes, &p.tm_a1, a_full, c * 64, h,
+                                 int(row0 + int64_t(kt) * BT));
+            }
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        const int64_t stat0 = sq.stat0;
+        // the statistics of step s are loaded two steps ahead (their latency
+        // would otherwise hold back the stage's completion)
+        float ls[BS / 32], ds[BS / 32], ls_next[BS / 32], ds_next[BS / 32];
+        auto load_stats = [&](int s, float (&l)[BS / 32], float (&dd)[BS / 32]) {
+#pragma unroll
+            for (int u = 0; u < BS / 32; ++u) {
+                const int q = (i0 + s) * BS + lane * (BS / 32) + u;
+                const bool v = s < n_q && q < L;
+                l[u] = v ? p.lse[stat0 + q] : 0.f;
+                dd[u] = v ? p.D[stat0 + q] : 0.f;
+            }
+        };
+        load_stats(0, ls, ds);
+        load_stats(1, ls_next, ds_next);
+        for (int s = 0; s < n_q; ++s) {
+            const int i = i0 + s;
+            int ok = 1;
+            if (lane == 0)
+                ok = ptx::mbar_wait(&kv_empty[stage], phase ^ 1u, abort_flag, p.err_word) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0))
+                break;
+            if (lane == 0) {
+                uint8_t *dst = ring + stage * C::kStageBytes;
+                const int row = int(row0 + int64_t(i) * BS);
+                ptx::mbar_expect_tx(&kv_full[stage], C::kStageBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    ptx::tma_load_3d(dst + c * kSubChunkBytes, &p.tm_s0, &kv_full[stage], c * 64,
+                                     h, row);
+                    ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
+                                     &kv_full[stage], c * 64, h, row);
+                }
+                if (i + kL2Ahead < n_sub)
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
+                        ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
+                    }
+                last_phase[stage] = int(phase);
+            }
+            float *slot = stats + stage * (2 * BS);
+#pragma unroll
+            for (int u = 0; u < BS / 32; ++u) {
+                slot[lane * (BS / 32) + u] = ls[u] * kLog2e;
+                slot[BS + lane * (BS / 32) + u] = ds[u];
+                ls[u] = ls_next[u];
+                ds[u] = ds_next[u];
+            }
+            ptx::mbar_arrive(&kv_full[stage]);       // all 32 lanes, after their writes
+            load_stats(s + 2, ls_next, ds_next);
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (lane == 0 && *abort_flag) {
+            drain_wait(a_full, 0);
+            for (int st = 0; st < C::kStages; ++st)
+                if (last_phase[st] >= 0)
+                    drain_wait(&kv_full[st], uint32_t(last_phase[st]));
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ======================= MMA issuer (whole warp) =====================
+        // Pipe order per step s: S^T_{s+1}, dP^T_{s+1} (once the rows have
+        // read dP^T_s), dV += P^T_s dO_s, dK += dS^T_s Q_s, dQ^T_s = K^T dS^T_s
+        // (once the rows have read dQ^T_{s-1}).  One elected lane issues.
+        constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BS, false);
+        constexpr uint32_t idesc_acc = ptx::idesc_bf16_f32(BT, D, true);          // B MN-major
+        constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32_mn(D, BS, true, true);  // both MN-major
+        constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
+        constexpr uint64_t desc_mn_sub = ptx::smem_desc_base(kSubChunkBytes, 1024);
+        constexpr uint64_t desc_mn_res = ptx::smem_desc_base(kResChunkBytes, 1024);
+        constexpr uint64_t desc_mn_ds = ptx::smem_desc_base(C::kDsBytes, 1024);
+        const uint64_t dk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_k));
+        const uint64_t dvk = ptx::smem_desc(desc_kmajor, ptx::smem_u32(tile_v));
+        const uint64_t dkt = ptx::smem_desc(desc_mn_res, ptx::smem_u32(tile_k));   // K^T
+        const uint32_t ring_addr = ptx::smem_u32(ring);
+        const uint32_t ds_addr = ptx::smem_u32(smem + C::kOffDs);
+        auto stage_addr = [&](int s) { return ring_addr + (s % C::kStages) * C::kStageBytes; };
+        // S^T_s = K Q_s^T into buffer s & 1 (waits for the step's ring stage)
+        auto issue_s = [&](int s) -> bool {
+            if (!ptx::mbar_wait_warp(&kv_full[s % C::kStages], uint32_t(s / C::kStages) & 1u,
+                                     abort_flag, p.err_word))
+                return false;
+            ptx::tc_fence_after_sync();
+            const uint64_t dq = ptx::smem_desc(desc_kmajor, stage_addr(s));
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + uint32_t(s & 1) * BS, dk + kmajor_off(kk, kResChunkBytes),
+                                dq + kmajor_off(kk, kSubChunkBytes), idesc_s, kk > 0 ? 1u : 0u);
+            }
+            __syncwarp();
+            return true;
+        };
+        // dP^T_s = V dO_s^T into the dP^T columns; completes s_full[s & 1]
+        auto issue_dp = [&](int s) {
+            const uint64_t ddo = ptx::smem_desc(desc_kmajor, stage_addr(s) + C::kSubBytes);
+            if (ptx::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + kFColDP, dvk + kmajor_off(kk, kResChunkBytes),
+                                ddo + kmajor_off(kk, kSubChunkBytes), idesc_s, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(&s_full[s & 1]);
+            }
+            __syncwarp();
+        };
+        do {
+            if (!ptx::mbar_wait_warp(a_full, 0, abort_flag, p.err_word) || !issue_s(0)) {
+                aborted = true;
+                break;
+            }
+            issue_dp(0);
+            for (int s = 0; s < n_q; ++s) {
+                if (s + 1 < n_q) {
+                    if (!issue_s(s + 1) ||
+                        !ptx::mbar_wait_warp(dp_read, uint32_t(s) & 1u, abort_flag, p.err_word)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    issue_dp(s + 1);
+                }
+                if (!ptx::mbar_wait_warp(&p_full[s & 1], uint32_t(s >> 1) & 1u, abort_flag,
+                                         p.err_word)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t qaddr = stage_addr(s);
+                const uint64_t dq_mn = ptx::smem_desc(desc_mn_sub, qaddr);
+                const uint64_t ddo_mn = ptx::smem_desc(desc_mn_sub, qaddr + C::kSubBytes);
+                const uint32_t dsb = ds_addr + uint32_t(s & 1) * C::kDsBytes;
+                const uint64_t ds_k = ptx::smem_desc(desc_kmajor, dsb);    // dS^T as A
+                const uint64_t ds_mn = ptx::smem_desc(desc_mn_ds, dsb);    // dS^T as B
+                const uint32_t a_tm = tmem + uint32_t(s & 1) * BS;
+                if (ptx::elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ts(tmem + kFColDV, a_tm + packed_col(kk),
+                                    ddo_mn + uint64_t((kk * 16 * 128) >> 4), idesc_acc,
+                                    (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ss(tmem + kFColDK, ds_k + uint64_t((kk * 32) >> 4),
+                                    dq_mn + uint64_t((kk * 16 * 128) >> 4), idesc_acc,
+                                    (s > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(&kv_empty[s % C::kStages]);
+                }
+                __syncwarp();
+                if (s > 0 &&
+                    !ptx::mbar_wait_warp(dq_free, uint32_t(s - 1) & 1u, abort_flag, p.err_word)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                if (ptx::elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)
+                        ptx::mma_ss(tmem + kFColDQ, dkt + uint64_t((kk * 16 * 128) >> 4),
+                                    ds_mn + uint64_t((kk * 16 * 128) >> 4), idesc_dq,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(dq_full);
+                }
+                __syncwarp();
+            }
+        } while (false);
+        if (ptx::elect_one()) {
+            if (!aborted)
+                ptx::mma_commit(o_full);
+            ptx::mma_commit(drain);
+            drain_wait(drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ======================= key rows ==================================
+        const int r = (warp & 3) * 32 + lane;        // key row = TMEM lane (= head-dim
+                                                     // index of dQ^T)
+        const int g = warp >> 2;                     // column group
+        const int k = kt * BT + r;
+        const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
+        const float sl = p.scale_log2;
+        const int col0 = g * kColsPerThread;
+        uint8_t *stg = smem + C::kOffStg + warp * C::kStgBytes;
+        // dQ^T of step t: load this thread's 32 queries of head-dim row r,
+        // free the columns, stage them (128-byte swizzle) and add them into
+        // the accumulator with one reduce per warp
+        auto drain_dq = [&](int t) -> bool {
+            if (!row_wait(dq_full, uint32_t(t) & 1u, abort_flag, p.err_word))
+                return false;
+            ptx::tc_fence_after_sync();
+            uint32_t v[32];
+            ptx::tmem_ld32(tmem + lane_bits + kFColDQ + col0, v);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(dq_free);
+                ptx::bulk_wait_read_all();           // the previous reduce has read stg
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_reduce_add_2d(&tm_acc, stg, (i0 + t) * BS + col0,
+                                       bh * D + (warp & 3) * 32);
+                ptx::bulk_commit();
+            }
+            return true;
+        };
+        for (int s = 0; s < n_q; ++s) {
+            const int i = i0 + s;
+            const int st = s % C::kStages;
+            if (!row_wait(&kv_full[st], uint32_t(s / C::kStages) & 1u, abort_flag, p.err_word)) {
+                aborted = true;
+                break;
+            }
+            float lv[32], dd[32];
+            {
+                const float *lse2s = stats + st * (2 * BS) + col0;
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + 4 * e4);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(lse2s + BS + 4 * e4);
+                    lv[4 * e4] = l4.x;
+                    lv[4 * e4 + 1] = l4.y;
+                    lv[4 * e4 + 2] = l4.z;
+                    lv[4 * e4 + 3] = l4.w;
+                    dd[4 * e4] = d4.x;
+                    dd[4 * e4 + 1] = d4.y;
+                    dd[4 * e4 + 2] = d4.z;
+                    dd[4 * e4 + 3] = d4.w;
+                }
+            }
+            if (!row_wait(&s_full[s & 1], uint32_t(s >> 1) & 1u, abort_flag, p.err_word)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            // visible columns [lo, hi]: causal keeps queries >= the key, the
+            // sequence ends at L; a key row past the end (the next sequence's
+            // K row in a dense batch) sees none, so it adds nothing to dQ
+            const int lo = k >= L ? BS : (p.causal ? k - i * BS : 0);
+            int hi = L - 1 - i * BS;
+            if (hi > BS - 1)
+                hi = BS - 1;
+            const uint32_t tS = tmem + lane_bits + uint32_t(s & 1) * BS + col0;
+            uint32_t sv[32], dv[32], pk[16], dk[16];
+            ptx::tmem_ld32(tS, sv);
+            ptx::tmem_ld32(tmem + lane_bits + kFColDP + col0, dv);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(dp_read);            // dP^T_{s+1} may overwrite the columns
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2) {
+                float pv[2], ds[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = 2 * e2 + u;
+                    const int c = col0 + e;
+                    const float x = __uint_as_float(sv[e]);
+                    const float y = __uint_as_float(dv[e]);
+                    pv[u] = ptx::ex2((c >= lo && c <= hi) ? fmaf(x, sl, -lv[e]) : -INFINITY);
+                    ds[u] = pv[u] * (y - dd[e]);
+                }
+                pk[e2] = ptx::pack_bf16x2(pv[0], pv[1]);
+                dk[e2] = ptx::pack_bf16x2(ds[0], ds[1]);
+            }
+            ptx::tmem_st16(tS, pk);                   // P^T of this block, packed
+            // dS^T row r, queries [col0, col0 + 32): 16-byte units 4g .. 4g + 3
+            uint8_t *dsrow = smem + C::kOffDs + (s & 1) * C::kDsBytes + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(dsrow + (((4 * g + j) ^ (r & 7)) << 4)) =
+                    make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();            // dS^T -> the tensor cores
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(&p_full[s & 1]);
+            if (s > 0 && !drain_dq(s - 1)) {
+                aborted = true;
+                break;
+            }
+        }
+        if (!aborted && n_q > 0 && !drain_dq(n_q - 1))
+            aborted = true;
+        if (lane == 0)
+            ptx::bulk_wait_all();                     // reduces done before the CTA ends
+        __syncwarp();
+        if (!aborted && ptx::mbar_wait(o_full, 0, abort_flag, p.err_word)) {
+            ptx::tc_fence_after_sync();
+            const bool key_ok = k < L;
+            if (g == 0)
+                store_row(tmem + lane_bits + kFColDV, 1.f, p.dV + ((row0 + k) * p.H + h) * D,
+                          key_ok, 0, D / 32);
+            else
+                store_row(tmem + lane_bits + kFColDK, p.scale,
+                          p.dK + ((row0 + k) * p.H + h) * D, key_ok, 0, D / 32);
+        }
+    }
+    teardown<D>(tmem);
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Before the one-pass kernel: D_i = dO_i . O_i for every (token, head) row of a
+// dense [B, N, H, 128] batch (one warp per row), stored [B, H, N]; and the dQ
+// accumulator set to zero.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
+                                                       const __nv_bfloat16 *dO, float *Dv,
+                                                       float4 *acc, int64_t acc_vec, int64_t rows,
+                                                       int H, int N)
+{
+    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = tid; i < acc_vec; i += nthreads)
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int lane = threadIdx.x & 31;
+    for (int64_t row = tid >> 5; row < rows; row += nthreads >> 5) {
+        const uint2 o = reinterpret_cast<const uint2 *>(O + row * 128)[lane];
+        const uint2 g = reinterpret_cast<const uint2 *>(dO + row * 128)[lane];
+        const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o);
+        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
+        float sum = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float2 a = __bfloat1622float2(o2[u]), c = __bfloat1622float2(g2[u]);
+            sum = fmaf(a.x, c.x, sum);
+            sum = fmaf(a.y, c.y, sum);
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+            const int64_t token = row / H;
+            const int hh = int(row % H);
+            const int64_t bb = token / N, q = token % N;
+            Dv[(bb * H + hh) * N + q] = sum;
+        }
+    }
+}
+
+// After it: dQ[b, q, h, :] = bf16(scale * acc[(b H + h) 128 + d, q]), one CTA
+// per (sequence, head, 64 queries), transposed through shared memory.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *acc, __nv_bfloat16 *dQ,
+                                                             int H, int N, int64_t n_pad,
+                                                             float scale)
+{
+    constexpr int D = 128, QB = 64;
+    __shared__ float tile[D][QB + 1];
+    const int q_blocks = int(n_pad / QB);
+    const int bh = int(blockIdx.x) / q_blocks;
+    const int q0 = (int(blockIdx.x) % q_blocks) * QB;
+    const float *src = acc + int64_t(bh) * D * n_pad + q0;
+    for (int idx = threadIdx.x; idx < D * QB; idx += blockDim.x) {
+        const int dd = idx / QB, q = idx % QB;
+        tile[dd][q] = src[int64_t(dd) * n_pad + q];
+    }
+    __syncthreads();
+    const int b = bh / H, h = bh % H;
+    for (int idx = threadIdx.x; idx < QB * (D / 2); idx += blockDim.x) {
+        const int q = idx / (D / 2), dp = idx % (D / 2);
+        if (q0 + q >= N)
+            break;                                   // idx grows with q
+        const uint32_t w = ptx::pack_bf16x2(scale * tile[2 * dp][q], scale * tile[2 * dp + 1][q]);
+        reinterpret_cast<uint32_t *>(dQ + ((int64_t(b) * N + q0 + q) * H + h) * D)[dp] = w;
+    }
+}
+
 template <int D, bool PACKED>
 int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t stream)
 {
@@ -1062,6 +1570,67 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
                          : launch_bwd_d<128, true>(p_dq, p_dkdv, stream);
     return a.d == 64 ? launch_bwd_d<64, false>(p_dq, p_dkdv, stream)
                      : launch_bwd_d<128, false>(p_dq, p_dkdv, stream);
+}
+
+int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
+{
+    if (a.d != 128 || a.cu_seqlens != nullptr || a.dq_acc == nullptr)
+        return FA_ERR_UNSUPPORTED;
+    BwdParams p;
+    const int64_t total = int64_t(a.B) * a.N;
+    const int64_t n_pad = bwd_atomic_n_pad(a.N);
+    p.O = static_cast<const __nv_bfloat16 *>(a.O);
+    p.dO = static_cast<const __nv_bfloat16 *>(a.dO);
+    p.lse = a.lse;
+    p.D = a.D;
+    p.dQ = static_cast<__nv_bfloat16 *>(a.dQ);
+    p.dK = static_cast<__nv_bfloat16 *>(a.dK);
+    p.dV = static_cast<__nv_bfloat16 *>(a.dV);
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.n_tiles = (a.N + BT - 1) / BT;
+    p.n_sub = (a.N + BS - 1) / BS;
+    p.scale = a.scale;
+    p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
+    p.causal = a.causal;
+    p.err_word = a.err_word;
+    p.cu_seqlens = nullptr;
+    p.total = total;
+    const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
+    if (blocks == 0)
+        return FA_OK;
+    const int64_t acc_rows = int64_t(a.B) * a.H * 128;
+    const int64_t conv_blocks = int64_t(a.B) * a.H * (n_pad / 64);
+    if (blocks > 0x7fffffffLL || conv_blocks > 0x7fffffffLL || acc_rows > 0x7fffffffLL)
+        return FA_ERR_TOO_LARGE;
+    CUtensorMap tm_acc;
+    if (!make_tmap_bf16(&p.tm_a0, a.K, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p.tm_a1, a.V, total, a.H, a.d, BT) ||
+        !make_tmap_bf16(&p.tm_s0, a.Q, total, a.H, a.d, BS) ||
+        !make_tmap_bf16(&p.tm_s1, a.dO, total, a.H, a.d, BS) ||
+        !make_tmap_f32_acc(&tm_acc, a.dq_acc, acc_rows, n_pad))
+        return FA_ERR_CUDA;
+    static PerDeviceOnce once_fused;
+    auto kf = attn_bwd_fused_kernel<false>;
+    if (!set_max_dynamic_smem(once_fused, reinterpret_cast<const void *>(kf),
+                              int(CfgF::kSmemBytes)))
+        return FA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    bwd_prep_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+        p.O, p.dO, a.D, reinterpret_cast<float4 *>(a.dq_acc), acc_rows * n_pad / 4,
+        total * a.H, a.H, a.N);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    kf<<<dim3(unsigned(blocks)), dim3(kThreads), CfgF::kSmemBytes, stream>>>(p, tm_acc);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    bwd_dq_convert_kernel<<<dim3(unsigned(conv_blocks)), dim3(256), 0, stream>>>(
+        a.dq_acc, p.dQ, a.H, a.N, n_pad, a.scale);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace fa

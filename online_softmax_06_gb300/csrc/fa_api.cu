@@ -363,25 +363,32 @@ namespace {
 int attention_bwd_common(const void *Q, const void *K, const void *V, const void *O,
                          const void *dO, const float *lse, void *dQ, void *dK, void *dV,
                          float *D_buf, int B, int H, int N, int64_t total, int d, float scale,
-                         int causal, const int32_t *cu_seqlens)
+                         int causal, const int32_t *cu_seqlens, bool one_pass = false,
+                         void *workspace = nullptr, int64_t workspace_bytes = 0)
 {
-    if (B < 0 || H < 0 || N < 0 || total < 0)
+    if (B < 0 || H < 0 || N < 0 || total < 0 || workspace_bytes < 0)
         return FA_ERR_BAD_SIZE;
     if (d != 64 && d != 128)
         return FA_ERR_UNSUPPORTED;
+    if (one_pass && d != 128)
+        return FA_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || N == 0 || total == 0)
         return FA_OK;
-    if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !D_buf)
+    if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !D_buf ||
+        (one_pass && !workspace))
         return FA_ERR_NULL_POINTER;
     const void *bf[8] = {Q, K, V, O, dO, dQ, dK, dV};
     for (const void *ptr : bf)
         if (!aligned(ptr, 16))
             return FA_ERR_MISALIGNED;
-    if (!aligned(lse, 4) || !aligned(D_buf, 4) || (cu_seqlens && !aligned(cu_seqlens, 4)))
+    if (!aligned(lse, 4) || !aligned(D_buf, 4) || (cu_seqlens && !aligned(cu_seqlens, 4)) ||
+        (one_pass && !aligned(workspace, 256)))
         return FA_ERR_MISALIGNED;
     if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
         total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
+    if (one_pass && workspace_bytes < int64_t(B) * H * d * bwd_atomic_n_pad(N) * 4)
+        return FA_ERR_BAD_SIZE;
     DeviceInfo *dev = current_device();
     if (dev == nullptr)
         return FA_ERR_NO_DEVICE;
@@ -405,6 +412,10 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
     a.err_word = dev->err_word;
     a.cu_seqlens = cu_seqlens;
     a.total = total;
+    if (one_pass) {
+        a.dq_acc = static_cast<float *>(workspace);
+        return launch_attention_bwd_atomic(a, t_stream);
+    }
     return launch_attention_bwd(a, t_stream);
 }
 }  // namespace
@@ -484,6 +495,25 @@ int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, const v
         return FA_ERR_NULL_POINTER;
     return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N, total, d,
                                     scale, causal, cu_seqlens);
+}
+
+int fa_attention_bwd_atomic(const void *Q, const void *K, const void *V, const void *O,
+                            const void *dO, const float *lse, void *dQ, void *dK, void *dV,
+                            float *D_buf, int B, int H, int N, int d, float scale, int causal,
+                            void *workspace, int64_t workspace_bytes)
+{
+    return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N,
+                                    int64_t(B) * N, d, scale, causal, nullptr, true, workspace,
+                                    workspace_bytes);
+}
+
+int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d)
+{
+    if (B < 0 || H < 0 || N < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return int64_t(B) * H * d * fa::bwd_atomic_n_pad(N) * 4;
 }
 
 }  // extern "C"

@@ -252,6 +252,28 @@ __device__ __forceinline__ void bulk_commit_and_wait_read()
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// TMA tiled reduce-add shared -> global (the element type and the add come
+// from the tensor map: fp32 adds performed at L2), bulk group.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *tmap, const void *smem_src,
+                                                  int x, int y)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], "
+        "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+        "r"(smem_u32(smem_src)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the committed bulk groups have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the committed bulk groups have completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory
@@ -460,6 +482,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The same with either operand MN-major (bit 15 for A, 16 for B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(uint32_t M, uint32_t N, bool a_mn_major,
+                                                         bool b_mn_major)
+{
+    return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A and B e4m3

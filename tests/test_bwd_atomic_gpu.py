@@ -1,0 +1,166 @@
+"""The one-pass backward (fa_attention_bwd_atomic: dQ summed over the key
+tiles by fp32 reduce-adds) on the GPU, through the C ABI, against the fp64
+oracle's gradients of sum(dO * O).
+
+Same tolerance as the two-pass backward (tests/test_bwd_gpu.py, BWD_TOL =
+2^-6 normwise per gradient tensor): P and dS are rounded to bf16 as there; the
+dQ shares are summed in fp32 in another order, which changes nothing at that
+scale.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import online_softmax_06_gb300 as fa
+import oracle
+from gpu_common import device_error_clear, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+BWD_TOL = 2.0 ** -6
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return require_gpu()
+
+
+def make_inputs(B, H, N, d, seed):
+    rng = np.random.default_rng(seed)
+    return [torch.from_numpy(rng.standard_normal((B, N, H, d)).astype(np.float32))
+            .to(torch.bfloat16) for _ in range(4)]   # Q, K, V, dO (bf16, CPU)
+
+
+def run_gpu(Q, K, V, dO, causal, dev, deterministic=False):
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    o, lse = fa.attention_fwd(q, k, v, causal=causal)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal,
+                                  deterministic=deterministic)
+    torch.cuda.synchronize(dev)
+    return [t.float().cpu().numpy() for t in (dq, dk, dv)]
+
+
+def normwise(g, ref, floor=1e-30):
+    return float(np.abs(g - ref).max() / max(np.abs(ref).max(), floor))
+
+
+# An all-zero reference (one token: P = 1, so dS = dP - D is exactly 0) is
+# compared against this floor: the kernel's dS is then the rounding
+# difference of two fp32 dot products of d terms (~1e-7 here).
+ZERO_FLOOR = 1e-3
+
+
+@pytest.mark.parametrize("B,H,N,causal", [
+    (1, 2, 128, False),
+    (2, 2, 256, True),
+    (1, 3, 300, True),       # ragged last key tile and query sub-tile
+    (2, 2, 200, False),      # ragged: a tile's last key rows are the next sequence's
+    (3, 1, 170, True),       # the same, causal, three sequences
+    (1, 1, 1, True),         # one token
+    (1, 2, 385, False),
+    (1, 2, 192, True),       # last key tile of one 64-row sub-tile
+    (1, 1, 65, True),        # two sub-tiles, one tile
+    (1, 2, 1000, True),      # 16 sub-steps: the 3-stage ring and both dS buffers wrap
+    (2, 1, 900, False),
+])
+def test_bwd_atomic_matches_oracle(dev, B, H, N, causal):
+    d = 128
+    Q, K, V, dO = make_inputs(B, H, N, d, seed=N * 11 + B)
+    dq, dk, dv = run_gpu(Q, K, V, dO, causal, dev)
+    ref = oracle.attention_bwd(*(t.float().numpy() for t in (Q, K, V, dO)), 1 / math.sqrt(d),
+                               causal)
+    errs = {name: normwise(g, ref[name], ZERO_FLOOR)
+            for name, g in (("dQ", dq), ("dK", dk), ("dV", dv))}
+    print(f"one-pass B{B} H{H} N{N} causal={causal}: normwise errors {errs}")
+    for name, e in errs.items():
+        assert e <= BWD_TOL, f"{name}: {e}"
+    device_error_clear()
+
+
+def test_bwd_atomic_full_size_sampled(dev):
+    """The benchmark's backward workload (causal B=2 H=32 N=4096 d=128):
+    gradients of sampled query rows and keys of three heads against the
+    oracle."""
+    B, H, N, d = 2, 32, 4096, 128
+    Q, K, V, dO = make_inputs(B, H, N, d, seed=4243)
+    dq, dk, dv = run_gpu(Q, K, V, dO, True, dev)
+    Qf, Kf, Vf, dOf = (t.float().numpy() for t in (Q, K, V, dO))
+    rng = np.random.default_rng(8)
+    for (b, h) in [(0, 0), (0, 17), (1, 31)]:
+        qi = np.unique(np.concatenate([[0, 1, 63, 64, 127, 128, N - 1], rng.integers(0, N, 20)]))
+        ki = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.integers(0, N, 20)]))
+        rq, rk, rv = oracle.attention_bwd_head(Qf, Kf, Vf, dOf, 1 / math.sqrt(d), True, b, h,
+                                               qi, ki)
+        for name, g, ref in (("dQ", dq[b, qi, h], rq), ("dK", dk[b, ki, h], rk),
+                             ("dV", dv[b, ki, h], rv)):
+            e = normwise(g, ref)
+            print(f"one-pass full size (b={b}, h={h}) {name}: normwise error {e}")
+            assert e <= BWD_TOL, f"{name}: {e}"
+    device_error_clear()
+
+
+def test_bwd_atomic_dk_dv_reproducible(dev):
+    """dK and dV involve no atomic sums: two runs give the same bits; dQ's
+    sums may be added in another order, so it is compared within a few fp32
+    roundings of its bf16 result."""
+    Q, K, V, dO = make_inputs(2, 2, 640, 128, seed=19)
+    a = run_gpu(Q, K, V, dO, True, dev)
+    b = run_gpu(Q, K, V, dO, True, dev)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert normwise(a[0], b[0]) <= 2.0 ** -8
+
+
+def test_bwd_atomic_ignores_workspace_contents(dev):
+    """The workspace's contents on entry do not matter (the first kernel
+    zeroes the accumulator): NaN-filled scratch gives the same gradients as
+    the two-pass call within the tolerance."""
+    B, H, N, d = 1, 2, 300, 128
+    Q, K, V, dO = make_inputs(B, H, N, d, seed=23)
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    nbytes = fa.fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
+    assert nbytes == B * H * d * 320 * 4             # N rounded up to 64
+    ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    d_buf = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fa.fa_set_stream(torch.cuda.current_stream(dev).cuda_stream)
+    rc = fa.fa_attention_bwd_atomic(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                    dv.data_ptr(), d_buf.data_ptr(), B, H, N, d,
+                                    1 / math.sqrt(d), 1, ws.data_ptr(), nbytes)
+    assert rc == 0
+    torch.cuda.synchronize(dev)
+    ref = fa.attention_bwd(q, k, v, o, do, lse, causal=True)
+    for g, r in zip((dq, dk, dv), ref):
+        g, r = g.float().cpu().numpy(), r.float().cpu().numpy()
+        assert np.isfinite(g).all()
+        assert normwise(g, r) <= 2.0 ** -7
+    device_error_clear()
+
+
+def test_bwd_atomic_bad_arguments(dev):
+    q = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
+    ws = torch.zeros((128 * 128 + 64,), dtype=torch.float32, device=dev)
+    p, l, w = q.data_ptr(), lse.data_ptr(), ws.data_ptr()
+    need = fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 128)
+    assert need == 128 * 128 * 4
+    assert fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 64) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_attention_bwd_atomic_workspace_bytes(-1, 1, 128, 128) == fa.FA_ERR_BAD_SIZE
+    call = fa.fa_attention_bwd_atomic
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 64, 0.1, 0, w, need) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 128, 0.1, 0, None, need) == \
+        fa.FA_ERR_NULL_POINTER
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 128, 0.1, 0, w, need - 4) == \
+        fa.FA_ERR_BAD_SIZE
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 128, 0.1, 0, w + 16, need) == \
+        fa.FA_ERR_MISALIGNED
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 0, 128, 0.1, 0, None, 0) == 0
+    q3 = q.reshape(128, 1, 128)
+    with pytest.raises(ValueError, match="dense"):
+        fa.attention_bwd(q3, q3, q3, q3, q3, lse.reshape(1, 128), causal=False,
+                         cu_seqlens=torch.tensor([0, 128], dtype=torch.int32, device=dev),
+                         max_seqlen=128, deterministic=False)
