@@ -225,10 +225,11 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  * instead of fa_attention_bwd's seven).
  *   Arguments, layouts and the result's definition: as fa_attention_bwd
  *   (dense batches; D_buf receives D_i).  d: 128 only.
- *   workspace: DEVICE fp32 scratch owned by the caller, 256-byte aligned, at
- *   least fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) bytes
- *   ([B * H * d, N rounded up to 64]); contents on entry are ignored (the
- *   first kernel zeroes it).
+ *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
+ *   fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) bytes: the fp32 dQ
+ *   accumulator [B * H, n_pad, d], then fp32 (lse log2 e, D) pairs [B * H,
+ *   n_pad], n_pad = N rounded up to 64; contents on entry are ignored (the
+ *   first kernel writes all of it).
  * The order of the reduce-adds is not fixed, so dQ may differ from run to run
  * in its last bits; dK and dV are reproducible.  fa_attention_bwd is the
  * deterministic form ("少搬一趟…" §5.6 offers one for the same reason).

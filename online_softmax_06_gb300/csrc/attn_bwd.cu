@@ -124,6 +124,9 @@ struct BwdParams {
     int *err_word;
     const int32_t *cu_seqlens;       // packed batches: [B + 1] prefix sums (else nullptr)
     int64_t total;                   // rows of the tensors
+    float *dq_acc;                   // one-pass kernel: fp32 [B * H, n_pad, d]
+    const float2 *stat2;             // one-pass kernel: [B * H, n_pad] of (lse log2 e, D)
+    int64_t n_pad;                   // N rounded up to 64
 };
 
 // Rows of sequence b: its first row, its length and the index of its first
@@ -1002,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =============================================================================
 // One CTA per (sequence, head, 128-key tile), as the dK/dV kernel, that also
 // forms dQ^T_s = K^T dS^T_s for each 64-query sub-step and adds it into an
-// fp32 accumulator [B*H*d, n_pad] in global memory with TMA reduce-adds: the
+// fp32 accumulator [B*H, n_pad, d] in global memory with atomic adds: the
 // contributions of the key tiles are summed in L2 ("少搬一趟…" §3.3: the
 // column blocks' dQ shares summed with atomic adds; §5.6). The order of those
 // adds varies from run to run, so dQ's rounding may too; dK and dV do not.
@@ -1012,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Shared memory: K and V resident; a 3-stage ring of (Q_s, dO_s); dS^T in two
 // 16 KB buffers (row = key, 64 queries = 128 bytes, 128-byte swizzle), which
 // is both the K-major A operand of dK += dS^T Q_s and the MN-major B operand
-// of dQ^T = K^T dS^T; one 4 KB staging tile per row warp for its reduce-adds.
+// of dQ^T = K^T dS^T.
 struct CfgF {
     static constexpr int D = 128;
     static constexpr int kChunks = D / 64;
@@ -1021,14 +1024,12 @@ struct CfgF {
     static constexpr int kStages = 3;
     static constexpr uint32_t kStageBytes = 2 * kSubBytes;
     static constexpr uint32_t kDsBytes = BT * BS * 2;
-    static constexpr uint32_t kStgBytes = 32 * 32 * 4;
     static constexpr uint32_t kOffA0 = 0;
     static constexpr uint32_t kOffA1 = kResBytes;
     static constexpr uint32_t kOffRing = 2 * kResBytes;
     static constexpr uint32_t kOffDs = kOffRing + kStages * kStageBytes;
-    static constexpr uint32_t kOffStg = kOffDs + 2 * kDsBytes;
-    static constexpr uint32_t kOffStat = kOffStg + kRowWarps * kStgBytes;
-    static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;
+    static constexpr uint32_t kOffStat = kOffDs + 2 * kDsBytes;
+    static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;   // (lse log2 e, D) pairs
     static constexpr uint32_t kOffBar = kOffStat + kStatBytes;
     // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], dp_read, dq_full,
     // dq_free, o_full, drain
@@ -1040,7 +1041,7 @@ constexpr uint32_t kFColDP = 128, kFColDQ = 192, kFColDV = 256, kFColDK = 384;
 
 template <bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_fused_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_acc)
+    attn_bwd_fused_kernel(const __grid_constant__ BwdParams p)
 {
     using C = CfgF;
     constexpr int D = C::D;
@@ -1073,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(a_full, 1);
         for (int st = 0; st < C::kStages; ++st) {
-            ptx::mbar_init(&kv_full[st], 32);        // the load warp's lanes stage statistics
+            ptx::mbar_init(&kv_full[st], 1);
             ptx::mbar_init(&kv_empty[st], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1097,7 +1098,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&p.tm_a1);
         ptx::prefetch_tmap(&p.tm_s0);
         ptx::prefetch_tmap(&p.tm_s1);
-        ptx::prefetch_tmap(&tm_acc);
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -1109,10 +1109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *stats = reinterpret_cast<float *>(smem + C::kOffStat);   // slot x (lse2, D) x 64
 
     if (warp == kWarpLoad) {
-        // ======================= TMA producer (whole warp) ===================
-        int last_phase[C::kStages];
-        for (int st = 0; st < C::kStages; ++st)
-            last_phase[st] = -1;
+        // ======================= TMA producer ==============================
+        // Ring stage of step s: Q_s, dO_s and the sub-tile's 64 (lse log2 e,
+        // D) pairs, all on the stage's barrier; one lane issues everything.
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(a_full, 2 * C::kResBytes);
             for (int c = 0; c < C::kChunks; ++c) {
@@ -1121,68 +1120,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(tile_v + c * kResChunkBytes, &p.tm_a1, a_full, c * 64, h,
                                  int(row0 + int64_t(kt) * BT));
             }
-        }
-        int stage = 0;
-        uint32_t phase = 0;
-        const int64_t stat0 = sq.stat0;
-        // the statistics of step s are loaded two steps ahead (their latency
-        // would otherwise hold back the stage's completion)
-        float ls[BS / 32], ds[BS / 32], ls_next[BS / 32], ds_next[BS / 32];
-        auto load_stats = [&](int s, float (&l)[BS / 32], float (&dd)[BS / 32]) {
-#pragma unroll
-            for (int u = 0; u < BS / 32; ++u) {
-                const int q = (i0 + s) * BS + lane * (BS / 32) + u;
-                const bool v = s < n_q && q < L;
-                l[u] = v ? p.lse[stat0 + q] : 0.f;
-                dd[u] = v ? p.D[stat0 + q] : 0.f;
-            }
-        };
-        load_stats(0, ls, ds);
-        load_stats(1, ls_next, ds_next);
-        for (int s = 0; s < n_q; ++s) {
-            const int i = i0 + s;
-            int ok = 1;
-            if (lane == 0)
-                ok = ptx::mbar_wait(&kv_empty[stage], phase ^ 1u, abort_flag, p.err_word) ? 1 : 0;
-            if (!__shfl_sync(0xffffffffu, ok, 0))
-                break;
-            if (lane == 0) {
+            const float2 *stat_src = p.stat2 + int64_t(bh) * p.n_pad;
+            int issued = 0;
+            for (int s = 0; s < n_q; ++s) {
+                const int stage = s % C::kStages;
+                const uint32_t phase = uint32_t(s / C::kStages) & 1u;
+                if (!ptx::mbar_wait(&kv_empty[stage], phase ^ 1u, abort_flag, p.err_word))
+                    break;
+                const int i = i0 + s;
                 uint8_t *dst = ring + stage * C::kStageBytes;
                 const int row = int(row0 + int64_t(i) * BS);
-                ptx::mbar_expect_tx(&kv_full[stage], C::kStageBytes);
+                ptx::mbar_arrive_expect_tx(&kv_full[stage], C::kStageBytes + 2 * BS * 4);
                 for (int c = 0; c < C::kChunks; ++c) {
                     ptx::tma_load_3d(dst + c * kSubChunkBytes, &p.tm_s0, &kv_full[stage], c * 64,
                                      h, row);
                     ptx::tma_load_3d(dst + C::kSubBytes + c * kSubChunkBytes, &p.tm_s1,
                                      &kv_full[stage], c * 64, h, row);
                 }
+                ptx::bulk_load(stats + stage * (2 * BS), stat_src + int64_t(i) * BS, 2 * BS * 4,
+                               &kv_full[stage]);
                 if (i + kL2Ahead < n_sub)
                     for (int c = 0; c < C::kChunks; ++c) {
                         ptx::tma_prefetch_3d(&p.tm_s0, c * 64, h, row + kL2Ahead * BS);
                         ptx::tma_prefetch_3d(&p.tm_s1, c * 64, h, row + kL2Ahead * BS);
                     }
-                last_phase[stage] = int(phase);
+                issued = s + 1;
             }
-            float *slot = stats + stage * (2 * BS);
-#pragma unroll
-            for (int u = 0; u < BS / 32; ++u) {
-                slot[lane * (BS / 32) + u] = ls[u] * kLog2e;
-                slot[BS + lane * (BS / 32) + u] = ds[u];
-                ls[u] = ls_next[u];
-                ds[u] = ds_next[u];
+            if (*abort_flag) {
+                // wait (bounded) for the copies in flight before the CTA ends:
+                // the last step issued into each stage
+                drain_wait(a_full, 0);
+                for (int s = issued - C::kStages > 0 ? issued - C::kStages : 0; s < issued; ++s)
+                    drain_wait(&kv_full[s % C::kStages], uint32_t(s / C::kStages) & 1u);
             }
-            ptx::mbar_arrive(&kv_full[stage]);       // all 32 lanes, after their writes
-            load_stats(s + 2, ls_next, ds_next);
-            if (++stage == C::kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        if (lane == 0 && *abort_flag) {
-            drain_wait(a_full, 0);
-            for (int st = 0; st < C::kStages; ++st)
-                if (last_phase[st] >= 0)
-                    drain_wait(&kv_full[st], uint32_t(last_phase[st]));
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -1307,10 +1277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_bits = uint32_t((warp & 3) * 32) << 16;
         const float sl = p.scale_log2;
         const int col0 = g * kColsPerThread;
-        uint8_t *stg = smem + C::kOffStg + warp * C::kStgBytes;
         // dQ^T of step t: load this thread's 32 queries of head-dim row r,
-        // free the columns, stage them (128-byte swizzle) and add them into
-        // the accumulator with one reduce per warp
+        // free the columns, and add them into the accumulator (a warp's 32
+        // lanes hold one query's 32 consecutive head-dim entries: one 128-byte
+        // row per atomic instruction)
         auto drain_dq = [&](int t) -> bool {
             if (!row_wait(dq_full, uint32_t(t) & 1u, abort_flag, p.err_word))
                 return false;
@@ -1320,22 +1290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
             ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0)
                 ptx::mbar_arrive(dq_free);
-                ptx::bulk_wait_read_all();           // the previous reduce has read stg
-            }
-            __syncwarp();
+            float *dst = p.dq_acc + (int64_t(bh) * p.n_pad + (i0 + t) * BS + col0) * D + r;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4 *>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                    make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                ptx::tma_reduce_add_2d(&tm_acc, stg, (i0 + t) * BS + col0,
-                                       bh * D + (warp & 3) * 32);
-                ptx::bulk_commit();
-            }
+            for (int c = 0; c < 32; ++c)
+                ptx::red_add_f32(dst + c * D, __uint_as_float(v[c]));
             return true;
         };
         for (int s = 0; s < n_q; ++s) {
@@ -1347,19 +1307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float lv[32], dd[32];
             {
-                const float *lse2s = stats + st * (2 * BS) + col0;
+                // (lse log2 e, D) pairs of the step's queries col0 .. col0 + 31
+                const float4 *st4 =
+                    reinterpret_cast<const float4 *>(stats + st * (2 * BS) + 2 * col0);
 #pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(lse2s + 4 * e4);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(lse2s + BS + 4 * e4);
-                    lv[4 * e4] = l4.x;
-                    lv[4 * e4 + 1] = l4.y;
-                    lv[4 * e4 + 2] = l4.z;
-                    lv[4 * e4 + 3] = l4.w;
-                    dd[4 * e4] = d4.x;
-                    dd[4 * e4 + 1] = d4.y;
-                    dd[4 * e4 + 2] = d4.z;
-                    dd[4 * e4 + 3] = d4.w;
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    const float4 v4 = st4[e2];
+                    lv[2 * e2] = v4.x;
+                    dd[2 * e2] = v4.y;
+                    lv[2 * e2 + 1] = v4.z;
+                    dd[2 * e2 + 1] = v4.w;
                 }
             }
             if (!row_wait(&s_full[s & 1], uint32_t(s >> 1) & 1u, abort_flag, p.err_word)) {
@@ -1418,9 +1375,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!aborted && n_q > 0 && !drain_dq(n_q - 1))
             aborted = true;
-        if (lane == 0)
-            ptx::bulk_wait_all();                     // reduces done before the CTA ends
-        __syncwarp();
         if (!aborted && ptx::mbar_wait(o_full, 0, abort_flag, p.err_word)) {
             ptx::tc_fence_after_sync();
             const bool key_ok = k < L;
@@ -1444,64 +1398,102 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // Before the one-pass kernel: D_i = dO_i . O_i for every (token, head) row of a
-// dense [B, N, H, 128] batch (one warp per row), stored [B, H, N]; and the dQ
-// accumulator set to zero.
+// dense [B, N, H, 128] batch, stored [B, H, N] and, with lse_i log2 e, as pairs
+// [B * H, n_pad] (zero pairs past N); and the dQ accumulator set to zero.
+// Half a warp takes a row (16 bytes a lane); a warp keeps 8 rows' loads in
+// flight.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
-                                                       const __nv_bfloat16 *dO, float *Dv,
-                                                       float4 *acc, int64_t acc_vec, int64_t rows,
-                                                       int H, int N)
+                                                       const __nv_bfloat16 *dO, const float *lse,
+                                                       float *Dv, float2 *stat2, float4 *acc,
+                                                       int64_t acc_vec, int64_t rows, int H,
+                                                       int N, int64_t n_pad)
 {
+    constexpr int kRowsPerWarp = 8;
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = tid; i < acc_vec; i += nthreads)
         acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int lane = threadIdx.x & 31;
-    for (int64_t row = tid >> 5; row < rows; row += nthreads >> 5) {
-        const uint2 o = reinterpret_cast<const uint2 *>(O + row * 128)[lane];
-        const uint2 g = reinterpret_cast<const uint2 *>(dO + row * 128)[lane];
-        const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o);
-        const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g);
-        float sum = 0.f;
+    const int64_t bh_count = rows / N / H * H;
+    const int64_t pads = bh_count * (n_pad - N);
+    for (int64_t i = tid; i < pads; i += nthreads) {
+        const int64_t bh = i / (n_pad - N), q = N + i % (n_pad - N);
+        stat2[bh * n_pad + q] = make_float2(0.f, 0.f);
+    }
+    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
+         base += (nthreads >> 5) * kRowsPerWarp) {
+        uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const float2 a = __bfloat1622float2(o2[u]), c = __bfloat1622float2(g2[u]);
-            sum = fmaf(a.x, c.x, sum);
-            sum = fmaf(a.y, c.y, sum);
+        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+            const int64_t row = base + 2 * u + half;
+            o[u] = make_uint4(0, 0, 0, 0);
+            g[u] = o[u];
+            if (row < rows) {
+                o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
+                g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+            }
         }
-        sum = warp_sum(sum);
-        if (lane == 0) {
-            const int64_t token = row / H;
-            const int hh = int(row % H);
-            const int64_t bb = token / N, q = token % N;
-            Dv[(bb * H + hh) * N + q] = sum;
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o[u]);
+            const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g[u]);
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = __bfloat1622float2(o2[e]), c = __bfloat1622float2(g2[e]);
+                sum = fmaf(a.x, c.x, sum);
+                sum = fmaf(a.y, c.y, sum);
+            }
+#pragma unroll
+            for (int m = 8; m > 0; m >>= 1)
+                sum += __shfl_xor_sync(0xffffffffu, sum, m);
+            const int64_t row = base + 2 * u + half;
+            if (l16 == 0 && row < rows) {
+                const int64_t token = row / H;
+                const int64_t bh = token / N * H + row % H, q = token % N;
+                Dv[bh * N + q] = sum;
+                stat2[bh * n_pad + q] = make_float2(lse[bh * N + q] * kLog2e, sum);
+            }
         }
     }
 }
 
-// After it: dQ[b, q, h, :] = bf16(scale * acc[(b H + h) 128 + d, q]), one CTA
-// per (sequence, head, 64 queries), transposed through shared memory.
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float *acc, __nv_bfloat16 *dQ,
-                                                             int H, int N, int64_t n_pad,
-                                                             float scale)
+// After it: dQ[b, q, h, :] = bf16(scale * acc[b H + h, q, :]), 8 elements per
+// thread and iteration (two 16-byte loads, one 16-byte store), four iterations'
+// loads in flight.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *acc, uint4 *dQ,
+                                                             int64_t bh_count, int H, int N,
+                                                             int64_t n_pad, float scale)
 {
-    constexpr int D = 128, QB = 64;
-    __shared__ float tile[D][QB + 1];
-    const int q_blocks = int(n_pad / QB);
-    const int bh = int(blockIdx.x) / q_blocks;
-    const int q0 = (int(blockIdx.x) % q_blocks) * QB;
-    const float *src = acc + int64_t(bh) * D * n_pad + q0;
-    for (int idx = threadIdx.x; idx < D * QB; idx += blockDim.x) {
-        const int dd = idx / QB, q = idx % QB;
-        tile[dd][q] = src[int64_t(dd) * n_pad + q];
-    }
-    __syncthreads();
-    const int b = bh / H, h = bh % H;
-    for (int idx = threadIdx.x; idx < QB * (D / 2); idx += blockDim.x) {
-        const int q = idx / (D / 2), dp = idx % (D / 2);
-        if (q0 + q >= N)
-            break;                                   // idx grows with q
-        const uint32_t w = ptx::pack_bf16x2(scale * tile[2 * dp][q], scale * tile[2 * dp + 1][q]);
-        reinterpret_cast<uint32_t *>(dQ + ((int64_t(b) * N + q0 + q) * H + h) * D)[dp] = w;
+    constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    const int64_t n = bh_count * N * kVec;            // (b h, q < N, 8-element group)
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
+         i0 += stride * kUnroll) {
+        float4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t row = i / kVec, bh = row / N, q = row % N;
+                const float4 *src = acc + (bh * n_pad + q) * (D / 4) + 2 * (i % kVec);
+                a[u] = src[0];
+                b[u] = src[1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t row = i / kVec, bh = row / N, q = row % N;
+                uint4 w;
+                w.x = ptx::pack_bf16x2(scale * a[u].x, scale * a[u].y);
+                w.y = ptx::pack_bf16x2(scale * a[u].z, scale * a[u].w);
+                w.z = ptx::pack_bf16x2(scale * b[u].x, scale * b[u].y);
+                w.w = ptx::pack_bf16x2(scale * b[u].z, scale * b[u].w);
+                dQ[(((bh / H) * N + q) * H + bh % H) * kVec + i % kVec] = w;
+            }
+        }
     }
 }
 
@@ -1597,19 +1589,20 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     p.err_word = a.err_word;
     p.cu_seqlens = nullptr;
     p.total = total;
+    p.dq_acc = a.dq_acc;
+    p.n_pad = n_pad;
+    // workspace: the accumulator, then the (lse log2 e, D) pairs
+    p.stat2 = reinterpret_cast<const float2 *>(a.dq_acc + int64_t(a.B) * a.H * n_pad * 128);
     const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
     if (blocks == 0)
         return FA_OK;
     const int64_t acc_rows = int64_t(a.B) * a.H * 128;
-    const int64_t conv_blocks = int64_t(a.B) * a.H * (n_pad / 64);
-    if (blocks > 0x7fffffffLL || conv_blocks > 0x7fffffffLL || acc_rows > 0x7fffffffLL)
+    if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
-    CUtensorMap tm_acc;
     if (!make_tmap_bf16(&p.tm_a0, a.K, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p.tm_a1, a.V, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p.tm_s0, a.Q, total, a.H, a.d, BS) ||
-        !make_tmap_bf16(&p.tm_s1, a.dO, total, a.H, a.d, BS) ||
-        !make_tmap_f32_acc(&tm_acc, a.dq_acc, acc_rows, n_pad))
+        !make_tmap_bf16(&p.tm_s1, a.dO, total, a.H, a.d, BS))
         return FA_ERR_CUDA;
     static PerDeviceOnce once_fused;
     auto kf = attn_bwd_fused_kernel<false>;
@@ -1621,15 +1614,16 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
     bwd_prep_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-        p.O, p.dO, a.D, reinterpret_cast<float4 *>(a.dq_acc), acc_rows * n_pad / 4,
-        total * a.H, a.H, a.N);
+        p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2), reinterpret_cast<float4 *>(a.dq_acc),
+        acc_rows * n_pad / 4, total * a.H, a.H, a.N, n_pad);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    kf<<<dim3(unsigned(blocks)), dim3(kThreads), CfgF::kSmemBytes, stream>>>(p, tm_acc);
+    kf<<<dim3(unsigned(blocks)), dim3(kThreads), CfgF::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    bwd_dq_convert_kernel<<<dim3(unsigned(conv_blocks)), dim3(256), 0, stream>>>(
-        a.dq_acc, p.dQ, a.H, a.N, n_pad, a.scale);
+    bwd_dq_convert_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+        reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ),
+        int64_t(a.B) * a.H, a.H, a.N, n_pad, a.scale);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

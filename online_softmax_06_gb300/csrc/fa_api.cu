@@ -387,7 +387,7 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
     if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
         total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
-    if (one_pass && workspace_bytes < int64_t(B) * H * d * bwd_atomic_n_pad(N) * 4)
+    if (one_pass && workspace_bytes < bwd_atomic_workspace_bytes(B, H, N))
         return FA_ERR_BAD_SIZE;
     DeviceInfo *dev = current_device();
     if (dev == nullptr)
@@ -513,7 +513,7 @@ int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d)
         return FA_ERR_BAD_SIZE;
     if (d != 128)
         return FA_ERR_UNSUPPORTED;
-    return int64_t(B) * H * d * fa::bwd_atomic_n_pad(N) * 4;
+    return fa::bwd_atomic_workspace_bytes(B, H, N);
 }
 
 }  // extern "C"

@@ -91,9 +91,6 @@ bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t 
 // 128-byte row segment (64 bf16 or 128 e4m3) x 1 head x 128 rows x 1 sequence,
 // 128-byte swizzle.  Rows past N of a sequence read as zero and are not stored.
 bool make_tmap_seq_4d(CUtensorMap *tm, const void *base, bool e4m3, int B, int N, int H, int d);
-// 2-D TMA map over an fp32 accumulator [rows, n_pad] (n_pad a multiple of
-// 64): box 32 x 32 (128-byte rows), 128-byte swizzle; used for reduce-adds.
-bool make_tmap_f32_acc(CUtensorMap *tm, float *base, int64_t rows, int64_t n_pad);
 
 // FP8 attention forward on the quantised tensors (dense; d = 128).
 struct AttnFp8Args {
@@ -123,13 +120,19 @@ struct AttnBwdArgs {
     int *err_word;
     const int32_t *cu_seqlens = nullptr;  // packed: device [B + 1] prefix sums
     int64_t total = 0;                    // packed: rows of the tensors
-    float *dq_acc = nullptr;              // one-pass form: fp32 [B * H * d, n_pad] scratch
+    float *dq_acc = nullptr;              // one-pass form: the workspace (see below)
 };
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
 // One-pass backward (dense, d = 128): dQ summed over the key tiles by fp32
 // reduce-adds into a.dq_acc (n_pad = N rounded up to 64), then converted.
 int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream);
 inline int64_t bwd_atomic_n_pad(int N) { return (int64_t(N) + 63) / 64 * 64; }
+// Workspace of the one-pass form (d = 128): the fp32 dQ accumulator [B H,
+// n_pad, 128], then (lse log2 e, D) pairs [B H, n_pad].
+inline int64_t bwd_atomic_workspace_bytes(int B, int H, int N)
+{
+    return int64_t(B) * H * bwd_atomic_n_pad(N) * (128 + 2) * 4;
+}
 
 // Quantisation pass of the FP8 forward (dense [B, N, H, d] bf16 inputs).
 struct Fp8QuantArgs {

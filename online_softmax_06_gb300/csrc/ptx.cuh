@@ -163,6 +163,18 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *t
         : "memory");
 }
 
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a
+// multiple of 16), completing on the barrier's transaction count.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *tmap,
                                             uint64_t *bar, int x, int y)
 {
@@ -252,27 +264,10 @@ __device__ __forceinline__ void bulk_commit_and_wait_read()
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// TMA tiled reduce-add shared -> global (the element type and the add come
-// from the tensor map: fp32 adds performed at L2), bulk group.
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *tmap, const void *smem_src,
-                                                  int x, int y)
+// Atomic fp32 add in global memory, no return value (performed at L2).
+__device__ __forceinline__ void red_add_f32(float *addr, float v)
 {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], "
-        "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
-        "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until the committed bulk groups have read their shared-memory sources.
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Waits until the committed bulk groups have completed (writes performed).
-__device__ __forceinline__ void bulk_wait_all()
-{
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

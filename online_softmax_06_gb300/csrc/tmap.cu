@@ -101,19 +101,4 @@ bool make_tmap_e4m3_vt(CUtensorMap *tm, const void *base, int64_t rows, int64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_tmap_f32_acc(CUtensorMap *tm, float *base, int64_t rows, int64_t n_pad)
-{
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr)
-        return false;
-    const cuuint64_t dims[2] = {cuuint64_t(n_pad), cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(n_pad) * 4};
-    const cuuint32_t box[2] = {32, 32};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace fa

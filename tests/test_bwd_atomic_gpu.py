@@ -121,7 +121,7 @@ def test_bwd_atomic_ignores_workspace_contents(dev):
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     o, lse = fa.attention_fwd(q, k, v, causal=True)
     nbytes = fa.fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
-    assert nbytes == B * H * d * 320 * 4             # N rounded up to 64
+    assert nbytes == B * H * 320 * (d + 2) * 4       # N rounded up to 64
     ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     d_buf = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -143,10 +143,10 @@ def test_bwd_atomic_ignores_workspace_contents(dev):
 def test_bwd_atomic_bad_arguments(dev):
     q = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16, device=dev)
     lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
-    ws = torch.zeros((128 * 128 + 64,), dtype=torch.float32, device=dev)
+    ws = torch.zeros((128 * 130 + 64,), dtype=torch.float32, device=dev)
     p, l, w = q.data_ptr(), lse.data_ptr(), ws.data_ptr()
     need = fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 128)
-    assert need == 128 * 128 * 4
+    assert need == 128 * 130 * 4
     assert fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 64) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_attention_bwd_atomic_workspace_bytes(-1, 1, 128, 128) == fa.FA_ERR_BAD_SIZE
     call = fa.fa_attention_bwd_atomic
