@@ -527,11 +527,14 @@ def time_splitkv(fa, dev, reps, peaks, clocks):
 
 
 def time_bwd(fa, w, dev, reps, peaks, clocks):
-    """Attention backward (dQ/D kernel + dK/dV kernel) on the headline
-    workload.  O and lse come from one forward call outside the timed region;
+    """Attention backward on the headline workload, both forms: the one-pass
+    call (fa_attention_bwd_atomic: D and zeroing, one pass over the key tiles
+    with dQ summed by fp32 atomic adds, the dQ conversion) and the
+    deterministic two-pass call (fa_attention_bwd: dQ/D kernel, dK/dV
+    kernel).  O and lse come from one forward call outside the timed region;
     dO ~ N(0, 1) in bf16.  Algorithmic work = 2.5 x the forward's (the five
-    products dS-recompute, dP, dV, dK, dQ of 2 N^2 d each against the
-    forward's two; the kernels run seven, recomputing S and dP for dQ)."""
+    products S, dP, dV, dK, dQ of 2 N^2 d each against the forward's two);
+    the two-pass form runs seven, recomputing S and dP for dQ."""
     import torch
     if w.varlen:
         return None
@@ -545,34 +548,54 @@ def time_bwd(fa, w, dev, reps, peaks, clocks):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dbuf = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     args = [t.data_ptr() for t in (q, k, v, o, do, lse, dq, dk, dv, dbuf)]
+    ws_bytes = fa.fa_attention_bwd_atomic_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty((max(ws_bytes, 4) // 4,), dtype=torch.float32, device=dev)
 
-    def launch():
+    def two_pass():
         rc = fa.fa_attention_bwd(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal))
         if rc != 0:
             raise RuntimeError(fa.strerror(rc))
 
-    for _ in range(3):
-        launch()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.time()
-    e0.record(stream)
-    for _ in range(reps):
-        launch()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark(t0, time.time())
-    dev_err = fa.fa_get_device_error()
-    if dev_err != 0:
-        raise RuntimeError(f"device error word {dev_err:#x}")
-    ms = e0.elapsed_time(e1) / reps
+    def one_pass():
+        rc = fa.fa_attention_bwd_atomic(*args, w.B, w.H, w.N, w.d, w.scale, int(w.causal),
+                                        ws.data_ptr(), ws_bytes)
+        if rc != 0:
+            raise RuntimeError(fa.strerror(rc))
+
+    def timed(launch):
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(stream)
+        for _ in range(reps):
+            launch()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        clocks.mark(t0, time.time())
+        dev_err = fa.fa_get_device_error()
+        if dev_err != 0:
+            raise RuntimeError(f"device error word {dev_err:#x}")
+        return e0.elapsed_time(e1) / reps
+
     flops = 2.5 * w.flops()
-    tf = flops / (ms / 1e3) / 1e12
-    return {"workload": w.name, "ms": ms, "TFLOP_per_s": tf,
-            "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "bound": "tensor",
-            "algorithmic_flops_per_call": flops, "executed_flops_per_call": 3.5 * w.flops(),
-            "launches_per_call": 2,
-            "l2": "inputs larger than L2 (Q/K/V/O/dO 320 MiB); %d back-to-back calls" % reps}
+    out = {"workload": w.name, "bound": "tensor", "algorithmic_flops_per_call": flops,
+           "l2": "inputs larger than L2 (Q/K/V/O/dO 320 MiB); %d back-to-back calls" % reps}
+    ms2 = timed(two_pass)
+    det = {"api": "fa_attention_bwd", "ms": ms2, "TFLOP_per_s": flops / (ms2 / 1e3) / 1e12,
+           "executed_flops_per_call": 3.5 * w.flops(), "launches_per_call": 2}
+    det["frac_of_bf16_peak"] = det["TFLOP_per_s"] / peaks["bf16_tflops"]
+    if w.d == 128:
+        ms1 = timed(one_pass)
+        tf = flops / (ms1 / 1e3) / 1e12
+        out.update({"api": "fa_attention_bwd_atomic", "ms": ms1, "TFLOP_per_s": tf,
+                    "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+                    "executed_flops_per_call": flops, "launches_per_call": 3,
+                    "deterministic": det})
+    else:
+        out.update(det)
+    return out
 
 
 def time_fp8(fa, w, dev, reps, peaks, clocks):
