@@ -248,6 +248,32 @@ FA_API int fa_attention_bwd_atomic(const void *Q, const void *K, const void *V, 
 FA_API int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * fa_attention_bwd_atomic for packed sequences ("第二十二课…" §三十五 with
+ * "少搬一趟…" §3.3): each sequence's gradients are those of its own attention.
+ *   Q, K, V, O, dO, dQ, dK, dV: bf16 [total, H, d]; lse and D_buf: fp32
+ *   [H, total]; cu_seqlens: DEVICE int32 [B + 1], non-decreasing from 0 to
+ *   total; N: the longest sequence (an upper bound is fine); d: 128 only.
+ *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
+ *   fa_attention_bwd_atomic_varlen_workspace_bytes(B, H, N, total, d) bytes:
+ *   the fp32 dQ accumulator [H, total + 64, d], then fp32 (lse log2 e, D)
+ *   pairs [H, B, n_pad] (n_pad = N rounded up to 64); contents on entry are
+ *   ignored.  A sequence longer than N is not computed and sets
+ *   FA_DEVERR_BAD_SEQLENS.  dQ's last bits may differ from run to run.
+ * Errors: as fa_attention_bwd_atomic, and FA_ERR_NULL_POINTER for a NULL
+ * cu_seqlens.
+ */
+FA_API int fa_attention_bwd_atomic_varlen(const void *Q, const void *K, const void *V,
+                                          const void *O, const void *dO, const float *lse,
+                                          void *dQ, void *dK, void *dV, float *D_buf, int B,
+                                          int H, int N, int64_t total, int d, float scale,
+                                          int causal, const int32_t *cu_seqlens, void *workspace,
+                                          int64_t workspace_bytes);
+
+/* Workspace bytes fa_attention_bwd_atomic_varlen needs, or a negative FA_ERR_* code. */
+FA_API int64_t fa_attention_bwd_atomic_varlen_workspace_bytes(int B, int H, int N, int64_t total,
+                                                              int d);
+
+/*
  * FP8 attention forward ("少搬一趟…" §4.6: FP8 with blockwise quantisation and
  * incoherent processing), for bf16 inputs on dense batches:
  *   1. Q and K rows are multiplied by M = diag(signs) H_d / sqrt(d) (H_d the

@@ -11,6 +11,7 @@ Raw C-ABI names (same names, same argument order, ints and pointers only):
 ``fa_attention_fwd_splitkv``, ``fa_attention_fwd_splitkv_varlen``, ``fa_splitkv_num_splits``, ``fa_attention_fwd_splitkv_noalloc``,
 ``fa_attention_fwd_f32``, ``fa_attention_bwd``, ``fa_attention_bwd_varlen``,
 ``fa_attention_bwd_atomic``, ``fa_attention_bwd_atomic_workspace_bytes``,
+``fa_attention_bwd_atomic_varlen``, ``fa_attention_bwd_atomic_varlen_workspace_bytes``,
 ``fa_attention_fwd_fp8``, ``fa_attention_fwd_fp8_varlen``,
 ``fa_attention_fp8_workspace_bytes``, ``fa_attention_fwd_host``,
 ``fa_attention_host_workspace_bytes``,
@@ -98,6 +99,10 @@ def lib():
                                               i32, i32, f32, i32, vp, i64]
         L.fa_attention_bwd_atomic_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.fa_attention_bwd_atomic_workspace_bytes.restype = i64
+        L.fa_attention_bwd_atomic_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                     i32, i32, i64, i32, f32, i32, vp, vp, i64]
+        L.fa_attention_bwd_atomic_varlen_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
+        L.fa_attention_bwd_atomic_varlen_workspace_bytes.restype = i64
         L.fa_set_stream.argtypes = [vp]
         L.fa_get_stream.argtypes = []
         L.fa_get_stream.restype = vp
@@ -110,6 +115,7 @@ def lib():
                      "fa_attention_fwd_f32", "fa_attention_fwd_splitkv", "fa_splitkv_num_splits",
                      "fa_attention_fwd_splitkv_noalloc", "fa_attention_bwd",
                      "fa_attention_bwd_varlen", "fa_attention_bwd_atomic",
+                     "fa_attention_bwd_atomic_varlen",
                      "fa_attention_fwd_splitkv_varlen",
                      "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
                      "fa_attention_fwd_host",
@@ -224,6 +230,17 @@ def fa_attention_bwd_atomic(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, d, 
 
 def fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) -> int:
     return lib().fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
+
+
+def fa_attention_bwd_atomic_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N, total, d,
+                                   scale, causal, cu_seqlens, workspace, workspace_bytes) -> int:
+    return lib().fa_attention_bwd_atomic_varlen(q, k, v, o, do, lse, dq, dk, dv, d_buf, B, H, N,
+                                                total, d, scale, causal, cu_seqlens, workspace,
+                                                workspace_bytes)
+
+
+def fa_attention_bwd_atomic_varlen_workspace_bytes(B, H, N, total, d) -> int:
+    return lib().fa_attention_bwd_atomic_varlen_workspace_bytes(B, H, N, total, d)
 
 
 def fa_set_stream(stream_ptr) -> int:
@@ -517,8 +534,8 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
     with ``cu_seqlens`` (int32 CUDA [B+1]) and ``max_seqlen``, lse [H, total].
     ``o`` and ``lse`` are the forward's outputs for the same inputs.  The fp32
     D scratch (lse's shape) is allocated here (torch).  ``deterministic=False``
-    calls the one-pass form with atomic dQ sums (``fa_attention_bwd_atomic``:
-    dense, d = 128; its fp32 workspace is allocated here).  Returns (dq, dk, dv).
+    calls the one-pass form with atomic dQ sums (``fa_attention_bwd_atomic`` /
+    ``_varlen``, d = 128; its workspace is allocated here).  Returns (dq, dk, dv).
     """
     import torch
     for t in (q, k, v, o, do):
@@ -546,15 +563,20 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
     d_buf = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
             _ptr(d_buf))
-    if not deterministic:
-        if cu_seqlens is not None:
-            raise ValueError("the one-pass backward takes dense batches")
+    if not deterministic and cu_seqlens is None:
         nbytes = fa_attention_bwd_atomic_workspace_bytes(B, H, N, d)
         _check(int(min(nbytes, 0)), "fa_attention_bwd_atomic_workspace_bytes")
         ws = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
         rc = fa_attention_bwd_atomic(*ptrs, B, H, N, d, float(scale), int(bool(causal)), _ptr(ws),
                                      nbytes)
         _check(rc, "fa_attention_bwd_atomic")
+    elif not deterministic:
+        nbytes = fa_attention_bwd_atomic_varlen_workspace_bytes(B, H, N, q.shape[0], d)
+        _check(int(min(nbytes, 0)), "fa_attention_bwd_atomic_varlen_workspace_bytes")
+        ws = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=q.device)
+        rc = fa_attention_bwd_atomic_varlen(*ptrs, B, H, N, q.shape[0], d, float(scale),
+                                            int(bool(causal)), _ptr(cu_seqlens), _ptr(ws), nbytes)
+        _check(rc, "fa_attention_bwd_atomic_varlen")
     elif cu_seqlens is None:
         rc = fa_attention_bwd(*ptrs, B, H, N, d, float(scale), int(bool(causal)))
         _check(rc, "fa_attention_bwd")
@@ -572,7 +594,8 @@ __all__ = [
     "fa_splitkv_num_splits",
     "fa_attention_fwd_splitkv_noalloc", "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
     "attention_bwd", "fa_attention_bwd", "fa_attention_bwd_varlen", "fa_attention_bwd_atomic",
-    "fa_attention_bwd_atomic_workspace_bytes", "attention_fwd_fp8",
+    "fa_attention_bwd_atomic_workspace_bytes", "fa_attention_bwd_atomic_varlen",
+    "fa_attention_bwd_atomic_varlen_workspace_bytes", "attention_fwd_fp8",
     "fa_attention_fwd_fp8", "fa_attention_fwd_fp8_varlen",
     "fa_attention_fp8_workspace_bytes",
     "fa_softmax_rows", "fa_attention_fwd", "fa_attention_fwd_varlen", "fa_attention_fwd_f32",

@@ -124,9 +124,12 @@ struct BwdParams {
     int *err_word;
     const int32_t *cu_seqlens;       // packed batches: [B + 1] prefix sums (else nullptr)
     int64_t total;                   // rows of the tensors
-    float *dq_acc;                   // one-pass kernel: fp32 [B * H, n_pad, d]
-    const float2 *stat2;             // one-pass kernel: [B * H, n_pad] of (lse log2 e, D)
+    float *dq_acc;                   // one-pass kernel: fp32 [B * H, n_pad, d] (packed:
+                                     // [H, total_pad, d])
+    const float2 *stat2;             // one-pass kernel: (lse log2 e, D) pairs [B * H, n_pad]
+                                     // (packed: [H, B, n_pad])
     int64_t n_pad;                   // N rounded up to 64
+    int64_t total_pad;               // packed: total + 64 (a last sub-tile's reach)
 };
 
 // Rows of sequence b: its first row, its length and the index of its first
@@ -1120,7 +1123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tma_load_3d(tile_v + c * kResChunkBytes, &p.tm_a1, a_full, c * 64, h,
                                  int(row0 + int64_t(kt) * BT));
             }
-            const float2 *stat_src = p.stat2 + int64_t(bh) * p.n_pad;
+            const int64_t stat_row = PACKED ? int64_t(h) * p.B + b : int64_t(bh);
+            const float2 *stat_src = p.stat2 + stat_row * p.n_pad;
             int issued = 0;
             for (int s = 0; s < n_q; ++s) {
                 const int stage = s % C::kStages;
@@ -1280,7 +1284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ^T of step t: load this thread's 32 queries of head-dim row r,
         // free the columns, and add them into the accumulator (a warp's 32
         // lanes hold one query's 32 consecutive head-dim entries: one 128-byte
-        // row per atomic instruction)
+        // row per atomic instruction).  Queries past the sequence's end add
+        // zeros (their dS is 0), into rows that belong to no query of it.
+        const int64_t acc_row0 = PACKED ? int64_t(h) * p.total_pad + row0 : int64_t(bh) * p.n_pad;
         auto drain_dq = [&](int t) -> bool {
             if (!row_wait(dq_full, uint32_t(t) & 1u, abort_flag, p.err_word))
                 return false;
@@ -1292,7 +1298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(dq_free);
-            float *dst = p.dq_acc + (int64_t(bh) * p.n_pad + (i0 + t) * BS + col0) * D + r;
+            float *dst = p.dq_acc + (acc_row0 + (i0 + t) * BS + col0) * D + r;
 #pragma unroll
             for (int c = 0; c < 32; ++c)
                 ptx::red_add_f32(dst + c * D, __uint_as_float(v[c]));
@@ -1497,6 +1503,117 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *acc, 
     }
 }
 
+// The prep kernel for packed batches ([total, H, 128] tensors, lse and D in
+// [H, total]): D_i as above, the pairs in [H, B, n_pad] (sequence b's query q
+// at (h B + b) n_pad + q, zero pairs past its length), the accumulator
+// [H, total_pad, 128] set to zero.  A row's sequence is found by binary search
+// in cu_seqlens; rows outside every sequence, or past n_pad, write no pair.
+__global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
+    const __nv_bfloat16 *O, const __nv_bfloat16 *dO, const float *lse, float *Dv, float2 *stat2,
+    float4 *acc, int64_t acc_vec, const int32_t *cu_seqlens, int B, int H, int64_t total,
+    int64_t n_pad)
+{
+    constexpr int kRowsPerWarp = 8;
+    const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = tid; i < acc_vec; i += nthreads)
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t n_pairs = int64_t(H) * B * n_pad;
+    for (int64_t i = tid; i < n_pairs; i += nthreads) {
+        const int b = int((i / n_pad) % B);
+        const int64_t q = i % n_pad;
+        if (q >= int64_t(cu_seqlens[b + 1]) - cu_seqlens[b])
+            stat2[i] = make_float2(0.f, 0.f);
+    }
+    const int64_t rows = total * H;
+    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
+         base += (nthreads >> 5) * kRowsPerWarp) {
+        uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+            const int64_t row = base + 2 * u + half;
+            o[u] = make_uint4(0, 0, 0, 0);
+            g[u] = o[u];
+            if (row < rows) {
+                o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
+                g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o[u]);
+            const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g[u]);
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = __bfloat1622float2(o2[e]), c = __bfloat1622float2(g2[e]);
+                sum = fmaf(a.x, c.x, sum);
+                sum = fmaf(a.y, c.y, sum);
+            }
+#pragma unroll
+            for (int m = 8; m > 0; m >>= 1)
+                sum += __shfl_xor_sync(0xffffffffu, sum, m);
+            const int64_t row = base + 2 * u + half;
+            if (l16 == 0 && row < rows) {
+                const int64_t token = row / H;
+                const int hh = int(row % H);
+                Dv[int64_t(hh) * total + token] = sum;
+                int lo = 0, hi = B;                  // largest b with cu_seqlens[b] <= token
+                while (hi - lo > 1) {
+                    const int mid = (lo + hi) >> 1;
+                    if (cu_seqlens[mid] <= token)
+                        lo = mid;
+                    else
+                        hi = mid;
+                }
+                const int64_t q = token - cu_seqlens[lo];
+                if (q >= 0 && token < cu_seqlens[lo + 1] && q < n_pad)
+                    stat2[(int64_t(hh) * B + lo) * n_pad + q] =
+                        make_float2(lse[int64_t(hh) * total + token] * kLog2e, sum);
+            }
+        }
+    }
+}
+
+// The conversion for packed batches: dQ[t, h, :] = bf16(scale *
+// acc[h, t, :]) for t < total.
+__global__ void __launch_bounds__(256) bwd_dq_convert_packed_kernel(const float4 *acc, uint4 *dQ,
+                                                                    int H, int64_t total,
+                                                                    int64_t total_pad, float scale)
+{
+    constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    const int64_t n = int64_t(H) * total * kVec;      // (h, t, 8-element group)
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
+         i0 += stride * kUnroll) {
+        float4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t row = i / kVec, hh = row / total, t = row % total;
+                const float4 *src = acc + (hh * total_pad + t) * (D / 4) + 2 * (i % kVec);
+                a[u] = src[0];
+                b[u] = src[1];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i < n) {
+                const int64_t row = i / kVec, hh = row / total, t = row % total;
+                uint4 w;
+                w.x = ptx::pack_bf16x2(scale * a[u].x, scale * a[u].y);
+                w.y = ptx::pack_bf16x2(scale * a[u].z, scale * a[u].w);
+                w.z = ptx::pack_bf16x2(scale * b[u].x, scale * b[u].y);
+                w.w = ptx::pack_bf16x2(scale * b[u].z, scale * b[u].w);
+                dQ[(t * H + hh) * kVec + i % kVec] = w;
+            }
+        }
+    }
+}
+
 template <int D, bool PACKED>
 int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t stream)
 {
@@ -1566,10 +1683,11 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
 
 int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
 {
-    if (a.d != 128 || a.cu_seqlens != nullptr || a.dq_acc == nullptr)
+    if (a.d != 128 || a.dq_acc == nullptr)
         return FA_ERR_UNSUPPORTED;
+    const bool packed = a.cu_seqlens != nullptr;
     BwdParams p;
-    const int64_t total = int64_t(a.B) * a.N;
+    const int64_t total = packed ? a.total : int64_t(a.B) * a.N;
     const int64_t n_pad = bwd_atomic_n_pad(a.N);
     p.O = static_cast<const __nv_bfloat16 *>(a.O);
     p.dO = static_cast<const __nv_bfloat16 *>(a.dO);
@@ -1587,16 +1705,18 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     p.scale_log2 = float(double(a.scale) * 1.4426950408889634);
     p.causal = a.causal;
     p.err_word = a.err_word;
-    p.cu_seqlens = nullptr;
+    p.cu_seqlens = a.cu_seqlens;
     p.total = total;
     p.dq_acc = a.dq_acc;
     p.n_pad = n_pad;
+    p.total_pad = total + 64;
     // workspace: the accumulator, then the (lse log2 e, D) pairs
-    p.stat2 = reinterpret_cast<const float2 *>(a.dq_acc + int64_t(a.B) * a.H * n_pad * 128);
+    const int64_t acc_floats = packed ? int64_t(a.H) * p.total_pad * 128
+                                      : int64_t(a.B) * a.H * n_pad * 128;
+    p.stat2 = reinterpret_cast<const float2 *>(a.dq_acc + acc_floats);
     const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
-    if (blocks == 0)
+    if (blocks == 0 || total == 0)
         return FA_OK;
-    const int64_t acc_rows = int64_t(a.B) * a.H * 128;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
     if (!make_tmap_bf16(&p.tm_a0, a.K, total, a.H, a.d, BT) ||
@@ -1604,26 +1724,37 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
         !make_tmap_bf16(&p.tm_s0, a.Q, total, a.H, a.d, BS) ||
         !make_tmap_bf16(&p.tm_s1, a.dO, total, a.H, a.d, BS))
         return FA_ERR_CUDA;
-    static PerDeviceOnce once_fused;
-    auto kf = attn_bwd_fused_kernel<false>;
-    if (!set_max_dynamic_smem(once_fused, reinterpret_cast<const void *>(kf),
-                              int(CfgF::kSmemBytes)))
+    static PerDeviceOnce once_fused, once_fused_packed;
+    auto kf = packed ? attn_bwd_fused_kernel<true> : attn_bwd_fused_kernel<false>;
+    if (!set_max_dynamic_smem(packed ? once_fused_packed : once_fused,
+                              reinterpret_cast<const void *>(kf), int(CfgF::kSmemBytes)))
         return FA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
-    bwd_prep_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-        p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2), reinterpret_cast<float4 *>(a.dq_acc),
-        acc_rows * n_pad / 4, total * a.H, a.H, a.N, n_pad);
+    if (packed)
+        bwd_prep_packed_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
+            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, a.cu_seqlens, a.B, a.H, total,
+            n_pad);
+    else
+        bwd_prep_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
+            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, total * a.H, a.H, a.N, n_pad);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
     kf<<<dim3(unsigned(blocks)), dim3(kThreads), CfgF::kSmemBytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    bwd_dq_convert_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-        reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ),
-        int64_t(a.B) * a.H, a.H, a.N, n_pad, a.scale);
+    if (packed)
+        bwd_dq_convert_packed_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ), a.H,
+            total, p.total_pad, a.scale);
+    else
+        bwd_dq_convert_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ),
+            int64_t(a.B) * a.H, a.H, a.N, n_pad, a.scale);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -387,7 +387,8 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
     if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
         total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
-    if (one_pass && workspace_bytes < bwd_atomic_workspace_bytes(B, H, N))
+    if (one_pass && workspace_bytes < (cu_seqlens ? bwd_atomic_varlen_workspace_bytes(B, H, N, total)
+                                                  : bwd_atomic_workspace_bytes(B, H, N)))
         return FA_ERR_BAD_SIZE;
     DeviceInfo *dev = current_device();
     if (dev == nullptr)
@@ -505,6 +506,27 @@ int fa_attention_bwd_atomic(const void *Q, const void *K, const void *V, const v
     return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N,
                                     int64_t(B) * N, d, scale, causal, nullptr, true, workspace,
                                     workspace_bytes);
+}
+
+int fa_attention_bwd_atomic_varlen(const void *Q, const void *K, const void *V, const void *O,
+                                   const void *dO, const float *lse, void *dQ, void *dK,
+                                   void *dV, float *D_buf, int B, int H, int N, int64_t total,
+                                   int d, float scale, int causal, const int32_t *cu_seqlens,
+                                   void *workspace, int64_t workspace_bytes)
+{
+    if (cu_seqlens == nullptr)
+        return FA_ERR_NULL_POINTER;
+    return fa::attention_bwd_common(Q, K, V, O, dO, lse, dQ, dK, dV, D_buf, B, H, N, total, d,
+                                    scale, causal, cu_seqlens, true, workspace, workspace_bytes);
+}
+
+int64_t fa_attention_bwd_atomic_varlen_workspace_bytes(int B, int H, int N, int64_t total, int d)
+{
+    if (B < 0 || H < 0 || N < 0 || total < 0)
+        return FA_ERR_BAD_SIZE;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    return fa::bwd_atomic_varlen_workspace_bytes(B, H, N, total);
 }
 
 int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d)

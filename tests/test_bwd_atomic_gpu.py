@@ -159,8 +159,79 @@ def test_bwd_atomic_bad_arguments(dev):
     assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 128, 0.1, 0, w + 16, need) == \
         fa.FA_ERR_MISALIGNED
     assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 0, 128, 0.1, 0, None, 0) == 0
-    q3 = q.reshape(128, 1, 128)
-    with pytest.raises(ValueError, match="dense"):
-        fa.attention_bwd(q3, q3, q3, q3, q3, lse.reshape(1, 128), causal=False,
-                         cu_seqlens=torch.tensor([0, 128], dtype=torch.int32, device=dev),
-                         max_seqlen=128, deterministic=False)
+
+
+def run_gpu_packed(Q, K, V, dO, cu, max_len, causal, dev):
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    cu_d = torch.from_numpy(np.asarray(cu, np.int32)).to(dev)
+    o, lse = fa.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu_d, max_seqlen=max_len)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, do, lse, causal=causal, cu_seqlens=cu_d,
+                                  max_seqlen=max_len, deterministic=False)
+    torch.cuda.synchronize(dev)
+    return [t.float().cpu().numpy() for t in (dq, dk, dv)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lens", [[1, 129, 300, 64, 257, 0, 128, 700], [1000, 3]])
+def test_bwd_atomic_packed_matches_oracle(dev, lens, causal):
+    """Packed sequences (ragged lengths, an empty one, one token, a long one
+    whose ring wraps): every gradient against the oracle's per-sequence
+    backward."""
+    import workloads
+    d, H = 128, 3
+    cu = workloads.cu_seqlens_of(lens)
+    total = int(cu[-1])
+    rng = np.random.default_rng(sum(lens) + 11 * causal)
+    Q, K, V, dO = (torch.from_numpy(rng.standard_normal((total, H, d)).astype(np.float32))
+                   .to(torch.bfloat16) for _ in range(4))
+    dq, dk, dv = run_gpu_packed(Q, K, V, dO, cu, max(lens), causal, dev)
+    ref = oracle.attention_bwd_packed(*(t.float().numpy() for t in (Q, K, V, dO)), cu,
+                                      1 / math.sqrt(d), causal)
+    errs = {name: normwise(g, ref[name], ZERO_FLOOR)
+            for name, g in (("dQ", dq), ("dK", dk), ("dV", dv))}
+    print(f"one-pass packed {lens} causal={causal}: normwise errors {errs}")
+    for name, e in errs.items():
+        assert e <= BWD_TOL, f"{name}: {e}"
+    device_error_clear()
+
+
+def test_bwd_atomic_packed_equal_lengths_is_the_dense_call(dev):
+    """Packed sequences of one length: dK and dV equal the dense one-pass
+    call's bits (the same arithmetic on the same rows); dQ's sums may be
+    added in another order."""
+    B, H, N, d = 2, 2, 300, 128
+    Q, K, V, dO = make_inputs(B, H, N, d, seed=29)
+    dense = run_gpu(Q, K, V, dO, True, dev)
+    cu = np.arange(B + 1, dtype=np.int32) * N
+    packed = run_gpu_packed(*(t.reshape(B * N, H, d) for t in (Q, K, V, dO)), cu, N, True, dev)
+    dense = [x.reshape(B * N, H, d) for x in dense]
+    assert np.array_equal(dense[1], packed[1]) and np.array_equal(dense[2], packed[2])
+    assert normwise(packed[0], dense[0]) <= 2.0 ** -8
+
+
+def test_bwd_atomic_packed_length_over_n_is_flagged(dev):
+    """A sequence longer than N is flagged in the device error word and not
+    computed (no access past the tensors or the workspace)."""
+    H, d = 1, 128
+    q = torch.zeros((300, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros((H, 300), dtype=torch.float32, device=dev)
+    cu = torch.tensor([0, 300], dtype=torch.int32, device=dev)
+    nbytes = fa.fa_attention_bwd_atomic_varlen_workspace_bytes(1, H, 200, 300, d)
+    assert nbytes == H * (300 + 64) * d * 4 + H * 1 * 256 * 8
+    ws = torch.empty((nbytes // 4,), dtype=torch.float32, device=dev)
+    fa.fa_set_stream(torch.cuda.current_stream(dev).cuda_stream)
+    p, l, w = q.data_ptr(), lse.data_ptr(), ws.data_ptr()
+    call = fa.fa_attention_bwd_atomic_varlen
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1, cu.data_ptr(), w,
+                nbytes) == 0
+    torch.cuda.synchronize(dev)
+    assert fa.fa_get_device_error() == fa.FA_DEVERR_BAD_SEQLENS
+    assert fa.fa_get_device_error() == 0
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1, None, w,
+                nbytes) == fa.FA_ERR_NULL_POINTER
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1, cu.data_ptr(), w,
+                nbytes - 8) == fa.FA_ERR_BAD_SIZE
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, 64, 0.125, 1, cu.data_ptr(), w,
+                nbytes) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_attention_bwd_atomic_varlen_workspace_bytes(1, H, 200, 300, 64) == \
+        fa.FA_ERR_UNSUPPORTED
