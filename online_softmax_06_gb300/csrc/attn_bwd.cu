@@ -1428,15 +1428,40 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
     const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
          base += (nthreads >> 5) * kRowsPerWarp) {
+        // every load of the 8 rows first (the statistic's index and its lse
+        // too, in the row's leading lane), then the dot products
         uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
+        int64_t bhq[kRowsPerWarp / 2], sq[kRowsPerWarp / 2];
+        float lv[kRowsPerWarp / 2];
+        // (b, q, h) of the group's first row by division, the others by carry
+        const int64_t token0 = base / H;
+        const int h0 = int(base - token0 * H);
+        const int64_t b0 = token0 / N, q0 = token0 - b0 * N;
 #pragma unroll
         for (int u = 0; u < kRowsPerWarp / 2; ++u) {
             const int64_t row = base + 2 * u + half;
             o[u] = make_uint4(0, 0, 0, 0);
             g[u] = o[u];
+            lv[u] = 0.f;
+            bhq[u] = sq[u] = 0;
             if (row < rows) {
                 o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
                 g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+                if (l16 == 0) {
+                    int hh = h0 + 2 * u + half;
+                    int64_t q = q0, bb = b0;
+                    while (hh >= H) {
+                        hh -= H;
+                        if (++q == N) {
+                            q = 0;
+                            ++bb;
+                        }
+                    }
+                    const int64_t bh = bb * H + hh;
+                    bhq[u] = bh * N + q;
+                    sq[u] = bh * n_pad + q;
+                    lv[u] = lse[bhq[u]];
+                }
             }
         }
 #pragma unroll
@@ -1453,12 +1478,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
 #pragma unroll
             for (int m = 8; m > 0; m >>= 1)
                 sum += __shfl_xor_sync(0xffffffffu, sum, m);
-            const int64_t row = base + 2 * u + half;
-            if (l16 == 0 && row < rows) {
-                const int64_t token = row / H;
-                const int64_t bh = token / N * H + row % H, q = token % N;
-                Dv[bh * N + q] = sum;
-                stat2[bh * n_pad + q] = make_float2(lse[bh * N + q] * kLog2e, sum);
+            if (l16 == 0 && base + 2 * u + half < rows) {
+                Dv[bhq[u]] = sum;
+                stat2[sq[u]] = make_float2(lv[u] * kLog2e, sum);
             }
         }
     }
@@ -1529,15 +1551,47 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
     const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
          base += (nthreads >> 5) * kRowsPerWarp) {
+        // every load of the 8 rows first (the row's sequence, found by binary
+        // search in cu_seqlens, and its lse too, in the row's leading lane),
+        // then the dot products
         uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
+        int64_t dq_[kRowsPerWarp / 2], sq[kRowsPerWarp / 2];
+        float lv[kRowsPerWarp / 2];
+        // (token, h) of the group's first row by division, the others by carry
+        const int64_t token0 = base / H;
+        const int h0 = int(base - token0 * H);
 #pragma unroll
         for (int u = 0; u < kRowsPerWarp / 2; ++u) {
             const int64_t row = base + 2 * u + half;
             o[u] = make_uint4(0, 0, 0, 0);
             g[u] = o[u];
+            lv[u] = 0.f;
+            dq_[u] = 0;
+            sq[u] = -1;                              // no pair for this row
             if (row < rows) {
                 o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
                 g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+                if (l16 == 0) {
+                    int hh = h0 + 2 * u + half;
+                    int64_t token = token0;
+                    while (hh >= H) {
+                        hh -= H;
+                        ++token;
+                    }
+                    dq_[u] = int64_t(hh) * total + token;
+                    lv[u] = lse[dq_[u]];
+                    int lo = 0, hi = B;              // largest b with cu_seqlens[b] <= token
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (cu_seqlens[mid] <= token)
+                            lo = mid;
+                        else
+                            hi = mid;
+                    }
+                    const int64_t q = token - cu_seqlens[lo];
+                    if (q >= 0 && token < cu_seqlens[lo + 1] && q < n_pad)
+                        sq[u] = (int64_t(hh) * B + lo) * n_pad + q;
+                }
             }
         }
 #pragma unroll
@@ -1554,23 +1608,10 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
 #pragma unroll
             for (int m = 8; m > 0; m >>= 1)
                 sum += __shfl_xor_sync(0xffffffffu, sum, m);
-            const int64_t row = base + 2 * u + half;
-            if (l16 == 0 && row < rows) {
-                const int64_t token = row / H;
-                const int hh = int(row % H);
-                Dv[int64_t(hh) * total + token] = sum;
-                int lo = 0, hi = B;                  // largest b with cu_seqlens[b] <= token
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (cu_seqlens[mid] <= token)
-                        lo = mid;
-                    else
-                        hi = mid;
-                }
-                const int64_t q = token - cu_seqlens[lo];
-                if (q >= 0 && token < cu_seqlens[lo + 1] && q < n_pad)
-                    stat2[(int64_t(hh) * B + lo) * n_pad + q] =
-                        make_float2(lse[int64_t(hh) * total + token] * kLog2e, sum);
+            if (l16 == 0 && base + 2 * u + half < rows) {
+                Dv[dq_[u]] = sum;
+                if (sq[u] >= 0)
+                    stat2[sq[u]] = make_float2(lv[u] * kLog2e, sum);
             }
         }
     }
