@@ -1125,6 +1125,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int64_t stat_row = PACKED ? int64_t(h) * p.B + b : int64_t(bh);
             const float2 *stat_src = p.stat2 + stat_row * p.n_pad;
+            // Launched as a programmatic dependent of the prep kernel: the
+            // resident K, V (inputs) are requested above; the statistics and
+            // the zeroed accumulator are that kernel's output, so the copies
+            // below wait for it to complete.  Every other role reaches them
+            // only through the ring barriers filled after this wait (the rows'
+            // atomic adds follow their first kv_full wait).
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             int issued = 0;
             for (int s = 0; s < n_q; ++s) {
                 const int stage = s % C::kStages;
@@ -1494,6 +1501,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *acc, 
                                                              int64_t n_pad, float scale)
 {
     constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the pass's sums are complete
     const int64_t n = bh_count * N * kVec;            // (b h, q < N, 8-element group)
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
@@ -1624,6 +1632,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_packed_kernel(const float4
                                                                     int64_t total_pad, float scale)
 {
     constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the pass's sums are complete
     const int64_t n = int64_t(H) * total * kVec;      // (h, t, 8-element group)
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n;
@@ -1785,18 +1794,34 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
             reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, total * a.H, a.H, a.N, n_pad);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    kf<<<dim3(unsigned(blocks)), dim3(kThreads), CfgF::kSmemBytes, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess)
+    // the pass and the conversion are programmatic dependents of the kernel
+    // before them (no early trigger: each may start as the previous one's
+    // CTAs exit, and waits for its completion before reading its output)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CfgF::kSmemBytes;
+    if (cudaLaunchKernelEx(&cfg, kf, p) != cudaSuccess || cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    if (packed)
-        bwd_dq_convert_packed_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-            reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ), a.H,
-            total, p.total_pad, a.scale);
-    else
-        bwd_dq_convert_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-            reinterpret_cast<const float4 *>(a.dq_acc), reinterpret_cast<uint4 *>(p.dQ),
-            int64_t(a.B) * a.H, a.H, a.N, n_pad, a.scale);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    cfg.gridDim = dim3(unsigned(sms * 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    const cudaError_t e =
+        packed ? cudaLaunchKernelEx(&cfg, bwd_dq_convert_packed_kernel,
+                                    reinterpret_cast<const float4 *>(a.dq_acc),
+                                    reinterpret_cast<uint4 *>(p.dQ), a.H, total, p.total_pad,
+                                    a.scale)
+               : cudaLaunchKernelEx(&cfg, bwd_dq_convert_kernel,
+                                    reinterpret_cast<const float4 *>(a.dq_acc),
+                                    reinterpret_cast<uint4 *>(p.dQ), int64_t(a.B) * a.H, a.H,
+                                    a.N, n_pad, a.scale);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace fa
