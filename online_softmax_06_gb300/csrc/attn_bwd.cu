@@ -771,6 +771,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         const int64_t stat0 = sq.stat0;
+        // Launched as a programmatic dependent of the dQ kernel: K and V
+        // (inputs) are requested above; D is that kernel's output, and every
+        // lane of this warp loads it, so all of them wait for its completion.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int s = 0; s < n_q; ++s) {
             const int i = i0 + s;
             // the step's statistics: global loads in flight during the slot wait
@@ -1679,8 +1683,21 @@ int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t st
     kdq<<<dim3(unsigned(blocks)), dim3(kThreads), CfgQ<D>::kSmemBytes, stream>>>(p_dq);
     if (cudaGetLastError() != cudaSuccess)
         return FA_ERR_CUDA;
-    kdkdv<<<dim3(unsigned(blocks)), dim3(kThreads), Cfg<D>::kSmemBytes, stream>>>(p_dkdv);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    // the dK/dV kernel is a programmatic dependent of the dQ kernel (no early
+    // trigger: it may start as the dQ kernel's CTAs exit; it waits for its
+    // completion before reading D)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<D>::kSmemBytes;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kdkdv, p_dkdv);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
