@@ -220,9 +220,9 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  * one block per CTA, and the blocks' overlapping contributions to dQ are
  * summed with atomic additions; §5.6).  Each CTA forms dK and dV of its 128
  * keys and its share dS K of dQ for every 64 queries it sees; the shares are
- * added in fp32 into `workspace` by TMA reduce-adds in L2, and a last kernel
- * writes dQ = scale * sum in bf16.  S and dP are formed once (five products
- * instead of fa_attention_bwd's seven).
+ * added in fp32 into `workspace` by atomic adds (performed in L2), and a last
+ * kernel writes dQ = scale * sum in bf16.  S and dP are formed once (five
+ * products instead of fa_attention_bwd's seven).
  *   Arguments, layouts and the result's definition: as fa_attention_bwd
  *   (dense batches; D_buf receives D_i).  d: 128 only.
  *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
@@ -230,7 +230,7 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  *   accumulator [B * H, n_pad, d], then fp32 (lse log2 e, D) pairs [B * H,
  *   n_pad], n_pad = N rounded up to 64; contents on entry are ignored (the
  *   first kernel writes all of it).
- * The order of the reduce-adds is not fixed, so dQ may differ from run to run
+ * The order of the atomic adds is not fixed, so dQ may differ from run to run
  * in its last bits; dK and dV are reproducible.  fa_attention_bwd is the
  * deterministic form ("少搬一趟…" §5.6 offers one for the same reason).
  * Three kernels run on the library stream (D_i and zeroing, the pass, the dQ

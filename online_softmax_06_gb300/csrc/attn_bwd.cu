@@ -1008,11 +1008,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =============================================================================
-// One-pass backward (d = 128, dense): dK, dV and each key tile's share of dQ
+// One-pass backward (d = 128, dense or packed): dK, dV and each key tile's
+// share of dQ
 // =============================================================================
 // One CTA per (sequence, head, 128-key tile), as the dK/dV kernel, that also
 // forms dQ^T_s = K^T dS^T_s for each 64-query sub-step and adds it into an
-// fp32 accumulator [B*H, n_pad, d] in global memory with atomic adds: the
+// fp32 accumulator ([B*H, n_pad, d]; packed: [H, total + 64, d]) in global
+// memory with atomic adds: the
 // contributions of the key tiles are summed in L2 ("少搬一趟…" §3.3: the
 // column blocks' dQ shares summed with atomic adds; §5.6). The order of those
 // adds varies from run to run, so dQ's rounding may too; dK and dV do not.
