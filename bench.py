@@ -189,10 +189,26 @@ def cpu_baseline(w, seconds: float):
     per_row = max(dt / 64, 1e-6)
     n = int(min(max(seconds / per_row, 256), w.total * w.H))
     dt, flops = time_oracle(w, Qp, Kp, Vp, n, seed=2)
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": f"{n} (token, head) query rows of {w.name} drawn uniformly with seed 2 "
-                      f"(fp64, {dt:.1f} s); flops = 4 * visible keys * d per row"}
+    cores = oracle.num_threads()
+    out = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": f"{n} (token, head) query rows of {w.name} drawn uniformly with seed 2 "
+                     f"(fp64, {dt:.1f} s); flops = 4 * visible keys * d per row"}
+    # per-core speed: every query row of the first sequence's first head on one thread
+    L0 = int(w.cu_seqlens()[1])
+    tok = np.arange(L0, dtype=np.int64)
+    head = np.zeros(L0, dtype=np.int64)
+    vis = (tok + 1) if w.causal else np.full(L0, L0)
+    flops1 = float(np.sum(4.0 * vis * w.d))
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.attention_rows(Qp, Kp, Vp, w.cu_seqlens(), w.scale, w.causal, tok, head)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(cores)
+    out["one_thread"] = {"value": flops1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                         "sample": f"all {L0} query rows of (sequence 0, head 0) ({dt1:.1f} s)"}
+    return out
 
 
 def run_reference(args, rank: int):

@@ -82,6 +82,8 @@ def _bind(lib):
     lib.oracle_attention_bwd_head.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
+    lib.oracle_set_num_threads.argtypes = [c_int]
+    lib.oracle_set_num_threads.restype = None
     return lib
 
 
@@ -110,6 +112,11 @@ def _f32(a) -> np.ndarray:
 
 def num_threads(lib=None) -> int:
     return (lib or load()).oracle_num_threads()
+
+
+def set_num_threads(n: int, lib=None) -> None:
+    """Thread count of the oracle's parallel loops from now on (for timing)."""
+    (lib or load()).oracle_set_num_threads(int(n))
 
 
 def softmax_rows(x, lib=None) -> np.ndarray:

@@ -571,3 +571,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Sets the thread count of the parallel loops that follow (n >= 1); for
+ * timing the oracle on one core. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
