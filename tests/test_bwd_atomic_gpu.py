@@ -235,3 +235,34 @@ def test_bwd_atomic_packed_length_over_n_is_flagged(dev):
                 nbytes) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_attention_bwd_atomic_varlen_workspace_bytes(1, H, 200, 300, 64) == \
         fa.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_atomic_full_size_every_element_matches_two_pass(dev):
+    """Every gradient element of the benchmark's backward workload (causal
+    B=2 H=32 N=4096 d=128, all 64 heads) from the one-pass form against the
+    two-pass form.  dK and dV are formed the same way in both (D_i summed in
+    the same order: 16 lanes of 8 elements, then the same shuffle tree; the
+    same products in the same K-step order), so their bits must be equal.
+    dQ is summed in another order (fp32 atomic adds over the key tiles
+    against one accumulator per query tile), so it may differ by a few units
+    in the last place of its bf16 result: bound 2^-9 of the largest |dQ|
+    (observed 5.9e-4).  The oracle checks of both forms fix correctness;
+    this one makes a fault confined to some heads or tiles of the full grid
+    show."""
+    B, H, N, d = 2, 32, 4096, 128
+    g = torch.Generator(device=dev).manual_seed(7)
+    q, k, v, do = (torch.randn((B, N, H, d), generator=g, device=dev).to(torch.bfloat16)
+                   for _ in range(4))
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    one = fa.attention_bwd(q, k, v, o, do, lse, causal=True, deterministic=False)
+    two = fa.attention_bwd(q, k, v, o, do, lse, causal=True, deterministic=True)
+    torch.cuda.synchronize(dev)
+    assert torch.equal(one[1], two[1]), "dK differs from the two-pass form"
+    assert torch.equal(one[2], two[2]), "dV differs from the two-pass form"
+    a, b = one[0].float(), two[0].float()
+    assert torch.isfinite(a).all()
+    per_head = (a - b).abs().amax(dim=(1, 3)) / b.abs().amax().item()   # [B, H]
+    worst = per_head.max().item()
+    print(f"full size, every element, one-pass vs two-pass: dK, dV equal; dQ max {worst:.2e} "
+          f"of max |dQ| (per head: min {per_head.min().item():.2e})")
+    assert worst <= 2.0 ** -9, f"dQ: {worst}"
