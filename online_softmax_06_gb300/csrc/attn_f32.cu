@@ -2,12 +2,16 @@
 //
 // The same online-softmax recurrence as the tensor-core path ("第二十二课…"
 // §三十二 pseudo-code; "少搬一趟：FlashAttention 四代进化史" §2.2), kept in fp32 so the
-// output meets fp32 accuracy: one thread owns one query row (its running max m,
-// running sum l and unnormalised output accumulator in registers); a CTA of 128
-// threads covers 128 consecutive query rows of one (sequence, head) and walks
-// the keys in tiles of 32 that all its threads read from shared memory.  The
-// key loop stops at the last key any row of the CTA can see (causal), and key
-// positions past the sequence end are masked ([L22] §三十四–§三十五).
+// output meets fp32 accuracy.  Eight threads share one query row: each holds
+// d / 8 of its head-dim columns of q and of the unnormalised output
+// accumulator in registers; a score is the sum of their eight partial dot
+// products (a three-step shuffle tree within the row's lanes), and each of
+// them keeps the row's running max m and sum l (the same values in all
+// eight) and updates its own columns.  A CTA of 128 threads covers 16
+// consecutive query rows of one (sequence, head) and walks the keys in tiles
+// of 32 that all its threads read from shared memory.  The key loop stops at
+// the last key any row of the CTA can see (causal), and key positions past
+// the sequence end are masked ([L22] §三十四–§三十五).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -21,8 +25,10 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 128;   // query rows per CTA (one per thread)
-constexpr int kKeys = 32;    // keys per shared-memory tile
+constexpr int kThreads = 128;
+constexpr int kGroup = 8;                    // threads per query row
+constexpr int kRows = kThreads / kGroup;     // query rows per CTA
+constexpr int kKeys = 32;                    // keys per shared-memory tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -39,9 +45,9 @@ struct F32Params {
 
 // DMAX: compile-time bound on d (32, 64 or 128); d itself may be smaller.
 template <int DMAX>
-__global__ void __launch_bounds__(kRows) attn_fwd_f32_kernel(const F32Params p)
+__global__ void __launch_bounds__(kThreads) attn_fwd_f32_kernel(const F32Params p)
 {
-    __shared__ float q_s[kRows][DMAX + 1];   // +1: conflict-free per-row access
+    constexpr int kCols = DMAX / kGroup;     // head-dim columns per thread
     __shared__ float k_s[kKeys][DMAX];
     __shared__ float v_s[kKeys][DMAX];
 
@@ -65,41 +71,51 @@ __global__ void __launch_bounds__(kRows) attn_fwd_f32_kernel(const F32Params p)
     if (q0 >= L)
         return;
     const int d = p.d, H = p.H;
-    const int r = threadIdx.x;
-    const int i = q0 + r;             // query position in the sequence
+    const int r = threadIdx.x / kGroup;      // row in the CTA
+    const int g = threadIdx.x % kGroup;      // column group: columns g kCols ..
+    const int c0 = g * kCols;
+    const int i = q0 + r;                    // query position in the sequence
     const bool row_ok = i < L;
 
-    // Stage this CTA's query rows (coalesced over d).
-    for (int idx = threadIdx.x; idx < kRows * DMAX; idx += kRows) {
-        const int rr = idx / DMAX, c = idx % DMAX;
-        float v = 0.f;
-        if (q0 + rr < L && c < d)
-            v = p.Q[((start + q0 + rr) * H + h) * d + c];
-        q_s[rr][c] = v;
-    }
-
-    float acc[DMAX];
+    float q[kCols], acc[kCols];
 #pragma unroll
-    for (int c = 0; c < DMAX; ++c)
+    for (int c = 0; c < kCols; ++c) {
+        q[c] = (row_ok && c0 + c < d) ? p.Q[((start + i) * H + h) * d + c0 + c] : 0.f;
         acc[c] = 0.f;
-    float m = -INFINITY, l = 0.f;     // m in log2 units of the scaled score
+    }
+    float m = -INFINITY, l = 0.f;            // m in log2 units of the scaled score
 
     const int last_q = min(q0 + kRows, L) - 1;
     const int n_keys = p.causal ? last_q + 1 : L;
-    for (int j0 = 0; j0 < n_keys; j0 += kKeys) {
-        __syncthreads();  // previous tile fully consumed (and q_s staged)
-        for (int idx = threadIdx.x; idx < kKeys * DMAX; idx += kRows) {
+    // the next tile's K and V are loaded into registers while this one is
+    // used, so the loads' latency overlaps the arithmetic
+    constexpr int kPer = kKeys * DMAX / kThreads;   // elements per thread and tile
+    float kr[kPer], vr[kPer];
+    auto load_tile = [&](int j0) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int idx = threadIdx.x + u * kThreads;
             const int jj = idx / DMAX, c = idx % DMAX;
-            float kv = 0.f, vv = 0.f;
+            kr[u] = vr[u] = 0.f;
             if (j0 + jj < L && c < d) {
                 const int64_t off = ((start + j0 + jj) * H + h) * d + c;
-                kv = p.K[off];
-                vv = p.V[off];
+                kr[u] = p.K[off];
+                vr[u] = p.V[off];
             }
-            k_s[jj][c] = kv;
-            v_s[jj][c] = vv;
+        }
+    };
+    load_tile(0);
+    for (int j0 = 0; j0 < n_keys; j0 += kKeys) {
+        __syncthreads();                     // the previous tile is fully consumed
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int idx = threadIdx.x + u * kThreads;
+            k_s[idx / DMAX][idx % DMAX] = kr[u];
+            v_s[idx / DMAX][idx % DMAX] = vr[u];
         }
         __syncthreads();
+        if (j0 + kKeys < n_keys)
+            load_tile(j0 + kKeys);
 
         float s[kKeys];
         float tmax = -INFINITY;
@@ -107,8 +123,12 @@ __global__ void __launch_bounds__(kRows) attn_fwd_f32_kernel(const F32Params p)
         for (int jj = 0; jj < kKeys; ++jj) {
             float dot = 0.f;
 #pragma unroll
-            for (int c = 0; c < DMAX; ++c)
-                dot = fmaf(q_s[r][c], k_s[jj][c], dot);
+            for (int c = 0; c < kCols; ++c)
+                dot = fmaf(q[c], k_s[jj][c0 + c], dot);
+            // the row's eight partial sums (lanes 8 r' .. 8 r' + 7 of the warp)
+            dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+            dot += __shfl_xor_sync(0xffffffffu, dot, 4);
             const int j = j0 + jj;
             const bool vis = j < L && (!p.causal || j <= i);
             s[jj] = vis ? dot * p.scale_log2 : -INFINITY;
@@ -116,19 +136,19 @@ __global__ void __launch_bounds__(kRows) attn_fwd_f32_kernel(const F32Params p)
         }
         const float m_new = fmaxf(m, tmax);
         if (m_new == -INFINITY)
-            continue;  // nothing visible yet for this row
+            continue;                        // nothing visible yet for this row
         const float corr = ptx::ex2(m - m_new);   // 0 on the first visible tile
         l *= corr;
 #pragma unroll
-        for (int c = 0; c < DMAX; ++c)
+        for (int c = 0; c < kCols; ++c)
             acc[c] *= corr;
 #pragma unroll
         for (int jj = 0; jj < kKeys; ++jj) {
             const float pj = ptx::ex2(s[jj] - m_new);
             l += pj;
 #pragma unroll
-            for (int c = 0; c < DMAX; ++c)
-                acc[c] = fmaf(pj, v_s[jj][c], acc[c]);
+            for (int c = 0; c < kCols; ++c)
+                acc[c] = fmaf(pj, v_s[jj][c0 + c], acc[c]);
         }
         m = m_new;
     }
@@ -138,14 +158,16 @@ __global__ void __launch_bounds__(kRows) attn_fwd_f32_kernel(const F32Params p)
     const float inv = 1.f / l;
     float *o = p.O + ((start + i) * H + h) * d;
 #pragma unroll
-    for (int c = 0; c < DMAX; ++c)
-        if (c < d)
-            o[c] = acc[c] * inv;
-    const float lse = (m + log2f(l)) * kLn2;
-    if (p.cu_seqlens)
-        p.lse[int64_t(h) * p.total + start + i] = lse;
-    else
-        p.lse[(int64_t(b) * H + h) * p.N + i] = lse;
+    for (int c = 0; c < kCols; ++c)
+        if (c0 + c < d)
+            o[c0 + c] = acc[c] * inv;
+    if (g == 0) {
+        const float lse = (m + log2f(l)) * kLn2;
+        if (p.cu_seqlens)
+            p.lse[int64_t(h) * p.total + start + i] = lse;
+        else
+            p.lse[(int64_t(b) * H + h) * p.N + i] = lse;
+    }
 }
 
 }  // namespace
@@ -169,11 +191,11 @@ int launch_attention_f32(const AttnArgs &a, cudaStream_t stream)
     p.err_word = a.err_word;
     const dim3 grid((a.N + kRows - 1) / kRows, a.H, a.B);
     if (a.d <= 32)
-        attn_fwd_f32_kernel<32><<<grid, kRows, 0, stream>>>(p);
+        attn_fwd_f32_kernel<32><<<grid, kThreads, 0, stream>>>(p);
     else if (a.d <= 64)
-        attn_fwd_f32_kernel<64><<<grid, kRows, 0, stream>>>(p);
+        attn_fwd_f32_kernel<64><<<grid, kThreads, 0, stream>>>(p);
     else
-        attn_fwd_f32_kernel<128><<<grid, kRows, 0, stream>>>(p);
+        attn_fwd_f32_kernel<128><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
