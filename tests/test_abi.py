@@ -95,6 +95,37 @@ def test_host_validation_without_gpu(lib):
     assert nl(None, None, None, None, None, 0, 1, 8, 8, 64, 1.0, 0, 0) == 0
 
 
+def test_one_pass_backward_host_checks_without_gpu(lib):
+    """The one-pass backward's workspace sizes and its argument checks that
+    return before any CUDA call."""
+    wb = fa.fa_attention_bwd_atomic_workspace_bytes
+    assert wb(-1, 1, 8, 128) == fa.FA_ERR_BAD_SIZE
+    assert wb(1, 1, 8, 64) == fa.FA_ERR_UNSUPPORTED
+    # accumulator [B H, n_pad, 128] fp32 and (lse, D) pairs [B H, n_pad], n_pad = 64
+    assert wb(2, 3, 50, 128) == 2 * 3 * 64 * (128 + 2) * 4
+    assert wb(2, 3, 64, 128) == wb(2, 3, 50, 128)
+    assert wb(2, 3, 65, 128) == 2 * 3 * 128 * (128 + 2) * 4
+    vb = fa.fa_attention_bwd_atomic_varlen_workspace_bytes
+    assert vb(2, 3, 50, -1, 128) == fa.FA_ERR_BAD_SIZE
+    assert vb(2, 3, 50, 90, 64) == fa.FA_ERR_UNSUPPORTED
+    # accumulator [H, total + 64, 128] fp32 and pairs [H, B, n_pad]
+    assert vb(2, 3, 50, 90, 128) == 3 * (90 + 64) * 128 * 4 + 3 * 2 * 64 * 8
+    call = fa.fa_attention_bwd_atomic
+    p = [None] * 10
+    assert call(*p, 1, 1, -1, 128, 1.0, 0, None, 0) == fa.FA_ERR_BAD_SIZE
+    assert call(*p, 1, 1, 8, 64, 1.0, 0, None, 0) == fa.FA_ERR_UNSUPPORTED
+    assert call(*p, 0, 1, 8, 128, 1.0, 0, None, 0) == 0
+    assert call(*p, 1, 1, 8, 128, 1.0, 0, None, 0) == fa.FA_ERR_NULL_POINTER
+    assert call(*p, 1, 1, 8, 128, 1.0, 0, None, -1) == fa.FA_ERR_BAD_SIZE
+    ptrs = [256] * 10
+    assert call(*ptrs, 1, 1, 8, 128, 1.0, 0, 16, 1 << 20) == fa.FA_ERR_MISALIGNED
+    assert call(*ptrs, 1, 1, 8, 128, 1.0, 0, 256, wb(1, 1, 8, 128) - 4) == fa.FA_ERR_BAD_SIZE
+    vcall = fa.fa_attention_bwd_atomic_varlen
+    assert vcall(*p, 1, 1, 8, 8, 128, 1.0, 0, None, None, 0) == fa.FA_ERR_NULL_POINTER
+    assert vcall(*ptrs, 1, 1, 8, 8, 128, 1.0, 0, 256, 256,
+                 vb(1, 1, 8, 8, 128) - 8) == fa.FA_ERR_BAD_SIZE
+
+
 def test_expire_wait_argument_range(lib):
     """The failure-detection switch takes 0 (off) .. 10^9 ns and is checked on
     the host (no device needed)."""
