@@ -224,7 +224,7 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  * kernel writes dQ = scale * sum in bf16.  S and dP are formed once (five
  * products instead of fa_attention_bwd's seven).
  *   Arguments, layouts and the result's definition: as fa_attention_bwd
- *   (dense batches; D_buf receives D_i).  d: 128 only.
+ *   (dense batches; D_buf receives D_i).  d: 64 or 128.
  *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
  *   fa_attention_bwd_atomic_workspace_bytes(B, H, N, d) bytes: the fp32 dQ
  *   accumulator [B * H, n_pad, d], then fp32 (lse log2 e, D) pairs [B * H,
@@ -235,8 +235,8 @@ FA_API int fa_attention_bwd_varlen(const void *Q, const void *K, const void *V, 
  * deterministic form ("少搬一趟…" §5.6 offers one for the same reason).
  * Three kernels run on the library stream (D_i and zeroing, the pass, the dQ
  * conversion); no synchronisation.
- * Errors: as fa_attention_bwd; FA_ERR_UNSUPPORTED for d != 128;
- * FA_ERR_BAD_SIZE also for a workspace that is too small.
+ * Errors: as fa_attention_bwd; FA_ERR_BAD_SIZE also for a workspace that is
+ * too small.
  */
 FA_API int fa_attention_bwd_atomic(const void *Q, const void *K, const void *V, const void *O,
                                    const void *dO, const float *lse, void *dQ, void *dK,
@@ -252,7 +252,7 @@ FA_API int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int 
  * "少搬一趟…" §3.3): each sequence's gradients are those of its own attention.
  *   Q, K, V, O, dO, dQ, dK, dV: bf16 [total, H, d]; lse and D_buf: fp32
  *   [H, total]; cu_seqlens: DEVICE int32 [B + 1], non-decreasing from 0 to
- *   total; N: the longest sequence (an upper bound is fine); d: 128 only.
+ *   total; N: the longest sequence (an upper bound is fine); d: 64 or 128.
  *   workspace: DEVICE scratch owned by the caller, 256-byte aligned, at least
  *   fa_attention_bwd_atomic_varlen_workspace_bytes(B, H, N, total, d) bytes:
  *   the fp32 dQ accumulator [H, total + 64, d], then fp32 (lse log2 e, D)

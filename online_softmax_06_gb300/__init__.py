@@ -535,7 +535,7 @@ def attention_bwd(q, k, v, o, do, lse, causal: bool = False, scale: float | None
     ``o`` and ``lse`` are the forward's outputs for the same inputs.  The fp32
     D scratch (lse's shape) is allocated here (torch).  ``deterministic=False``
     calls the one-pass form with atomic dQ sums (``fa_attention_bwd_atomic`` /
-    ``_varlen``, d = 128; its workspace is allocated here).  Returns (dq, dk, dv).
+    ``_varlen``; its workspace is allocated here).  Returns (dq, dk, dv).
     """
     import torch
     for t in (q, k, v, o, do):

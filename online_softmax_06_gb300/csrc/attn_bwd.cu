@@ -1025,17 +1025,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 16 KB buffers (row = key, 64 queries = 128 bytes, 128-byte swizzle), which
 // is both the K-major A operand of dK += dS^T Q_s and the MN-major B operand
 // of dQ^T = K^T dS^T.
+template <int D_>
 struct CfgF {
-    static constexpr int D = 128;
+    static constexpr int D = D_;
     static constexpr int kChunks = D / 64;
     static constexpr uint32_t kResBytes = BT * D * 2;
     static constexpr uint32_t kSubBytes = BS * D * 2;
     static constexpr int kStages = 3;
     static constexpr uint32_t kStageBytes = 2 * kSubBytes;
     static constexpr uint32_t kDsBytes = BT * BS * 2;
+    // K^T is the A operand of dQ^T with M = 128 head-dim rows in two 64-row
+    // blocks 16 KB apart: at d = 128 the second block is K's second chunk; at
+    // d = 64 it is a zero tile placed there, so the operand and its descriptor
+    // are the same for both head dims (the padded rows of dQ^T are zeros)
     static constexpr uint32_t kOffA0 = 0;
-    static constexpr uint32_t kOffA1 = kResBytes;
-    static constexpr uint32_t kOffRing = 2 * kResBytes;
+    static constexpr uint32_t kOffZero = kResChunkBytes;      // d = 64 only
+    static constexpr uint32_t kOffA1 = 2 * kResChunkBytes;    // V
+    static constexpr uint32_t kOffRing = kOffA1 + kResBytes;
     static constexpr uint32_t kOffDs = kOffRing + kStages * kStageBytes;
     static constexpr uint32_t kOffStat = kOffDs + 2 * kDsBytes;
     static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;   // (lse log2 e, D) pairs
@@ -1046,14 +1052,14 @@ struct CfgF {
     static constexpr uint32_t kSmemBytes = kOffBar + 8 * kBars + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
-constexpr uint32_t kFColDP = 128, kFColDQ = 192, kFColDV = 256, kFColDK = 384;
+constexpr uint32_t kFColDP = 128, kFColDQ = 192, kFColDV = 256;   // dK from 256 + d
 
-template <bool PACKED>
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_fused_kernel(const __grid_constant__ BwdParams p)
 {
-    using C = CfgF;
-    constexpr int D = C::D;
+    using C = CfgF<D>;
+    constexpr uint32_t kFColDK = kFColDV + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1107,6 +1113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&p.tm_a1);
         ptx::prefetch_tmap(&p.tm_s0);
         ptx::prefetch_tmap(&p.tm_s1);
+    }
+    if constexpr (D < 128) {
+        // the zero rows of the K^T operand (see CfgF)
+        for (int i = threadIdx.x; i < int(kResChunkBytes / 16); i += kThreads)
+            reinterpret_cast<uint4 *>(smem + C::kOffZero)[i] = make_uint4(0, 0, 0, 0);
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
@@ -1179,7 +1191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (once the rows have read dQ^T_{s-1}).  One elected lane issues.
         constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BS, false);
         constexpr uint32_t idesc_acc = ptx::idesc_bf16_f32(BT, D, true);          // B MN-major
-        constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32_mn(D, BS, true, true);  // both MN-major
+        constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32_mn(BT, BS, true, true); // both MN-major
         constexpr uint64_t desc_kmajor = ptx::smem_desc_base(16, 1024);
         constexpr uint64_t desc_mn_sub = ptx::smem_desc_base(kSubChunkBytes, 1024);
         constexpr uint64_t desc_mn_res = ptx::smem_desc_base(kResChunkBytes, 1024);
@@ -1300,21 +1312,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // row per atomic instruction).  Queries past the sequence's end add
         // zeros (their dS is 0), into rows that belong to no query of it.
         const int64_t acc_row0 = PACKED ? int64_t(h) * p.total_pad + row0 : int64_t(bh) * p.n_pad;
+        // (at d = 64 the warps of lanes 64 .. 127 hold the zero rows: they
+        // only keep the barrier protocol)
+        const bool has_d = (warp & 3) * 32 < D;
         auto drain_dq = [&](int t) -> bool {
             if (!row_wait(dq_full, uint32_t(t) & 1u, abort_flag, p.err_word))
                 return false;
             ptx::tc_fence_after_sync();
-            uint32_t v[32];
-            ptx::tmem_ld32(tmem + lane_bits + kFColDQ + col0, v);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(dq_free);
-            float *dst = p.dq_acc + (acc_row0 + (i0 + t) * BS + col0) * D + r;
+            if (has_d) {
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + lane_bits + kFColDQ + col0, v);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(dq_free);
+                float *dst = p.dq_acc + (acc_row0 + (i0 + t) * BS + col0) * D + r;
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                ptx::red_add_f32(dst + c * D, __uint_as_float(v[c]));
+                for (int c = 0; c < 32; ++c)
+                    ptx::red_add_f32(dst + c * D, __uint_as_float(v[c]));
+            } else {
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(dq_free);
+            }
             return true;
         };
         for (int s = 0; s < n_q; ++s) {
@@ -1417,10 +1439,11 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // Before the one-pass kernel: D_i = dO_i . O_i for every (token, head) row of a
-// dense [B, N, H, 128] batch, stored [B, H, N] and, with lse_i log2 e, as pairs
+// dense [B, N, H, D] batch, stored [B, H, N] and, with lse_i log2 e, as pairs
 // [B * H, n_pad] (zero pairs past N); and the dQ accumulator set to zero.
-// Half a warp takes a row (16 bytes a lane); a warp keeps 8 rows' loads in
-// flight.
+// D / 8 lanes take a row (16 bytes a lane; the same sum order as the dQ
+// kernel's D); a warp keeps 8 rows' loads in flight.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
                                                        const __nv_bfloat16 *dO, const float *lse,
                                                        float *Dv, float2 *stat2, float4 *acc,
@@ -1428,6 +1451,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
                                                        int N, int64_t n_pad)
 {
     constexpr int kRowsPerWarp = 8;
+    constexpr int kLanes = D / 8, kRowsPerInst = 32 / kLanes, kU = kRowsPerWarp / kRowsPerInst;
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = tid; i < acc_vec; i += nthreads)
@@ -1438,30 +1462,30 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
         const int64_t bh = i / (n_pad - N), q = N + i % (n_pad - N);
         stat2[bh * n_pad + q] = make_float2(0.f, 0.f);
     }
-    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    const int lane = threadIdx.x & 31, sub = lane / kLanes, l16 = lane % kLanes;
     for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
          base += (nthreads >> 5) * kRowsPerWarp) {
         // every load of the 8 rows first (the statistic's index and its lse
         // too, in the row's leading lane), then the dot products
-        uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
-        int64_t bhq[kRowsPerWarp / 2], sq[kRowsPerWarp / 2];
-        float lv[kRowsPerWarp / 2];
+        uint4 o[kU], g[kU];
+        int64_t bhq[kU], sq[kU];
+        float lv[kU];
         // (b, q, h) of the group's first row by division, the others by carry
         const int64_t token0 = base / H;
         const int h0 = int(base - token0 * H);
         const int64_t b0 = token0 / N, q0 = token0 - b0 * N;
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
-            const int64_t row = base + 2 * u + half;
+        for (int u = 0; u < kU; ++u) {
+            const int64_t row = base + u * kRowsPerInst + sub;
             o[u] = make_uint4(0, 0, 0, 0);
             g[u] = o[u];
             lv[u] = 0.f;
             bhq[u] = sq[u] = 0;
             if (row < rows) {
-                o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
-                g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+                o[u] = reinterpret_cast<const uint4 *>(O + row * D)[l16];
+                g[u] = reinterpret_cast<const uint4 *>(dO + row * D)[l16];
                 if (l16 == 0) {
-                    int hh = h0 + 2 * u + half;
+                    int hh = h0 + u * kRowsPerInst + sub;
                     int64_t q = q0, bb = b0;
                     while (hh >= H) {
                         hh -= H;
@@ -1478,7 +1502,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
             }
         }
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+        for (int u = 0; u < kU; ++u) {
             const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o[u]);
             const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g[u]);
             float sum = 0.f;
@@ -1489,9 +1513,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
                 sum = fmaf(a.y, c.y, sum);
             }
 #pragma unroll
-            for (int m = 8; m > 0; m >>= 1)
+            for (int m = kLanes / 2; m > 0; m >>= 1)
                 sum += __shfl_xor_sync(0xffffffffu, sum, m);
-            if (l16 == 0 && base + 2 * u + half < rows) {
+            if (l16 == 0 && base + u * kRowsPerInst + sub < rows) {
                 Dv[bhq[u]] = sum;
                 stat2[sq[u]] = make_float2(lv[u] * kLog2e, sum);
             }
@@ -1502,11 +1526,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *O,
 // After it: dQ[b, q, h, :] = bf16(scale * acc[b H + h, q, :]), 8 elements per
 // thread and iteration (two 16-byte loads, one 16-byte store), four iterations'
 // loads in flight.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *acc, uint4 *dQ,
                                                              int64_t bh_count, int H, int N,
                                                              int64_t n_pad, float scale)
 {
-    constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    constexpr int kVec = D / 8, kUnroll = 4;
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the pass's sums are complete
     const int64_t n = bh_count * N * kVec;            // (b h, q < N, 8-element group)
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -1539,17 +1564,19 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4 *acc, 
     }
 }
 
-// The prep kernel for packed batches ([total, H, 128] tensors, lse and D in
+// The prep kernel for packed batches ([total, H, D] tensors, lse and D in
 // [H, total]): D_i as above, the pairs in [H, B, n_pad] (sequence b's query q
 // at (h B + b) n_pad + q, zero pairs past its length), the accumulator
-// [H, total_pad, 128] set to zero.  A row's sequence is found by binary search
+// [H, total_pad, D] set to zero.  A row's sequence is found by binary search
 // in cu_seqlens; rows outside every sequence, or past n_pad, write no pair.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
     const __nv_bfloat16 *O, const __nv_bfloat16 *dO, const float *lse, float *Dv, float2 *stat2,
     float4 *acc, int64_t acc_vec, const int32_t *cu_seqlens, int B, int H, int64_t total,
     int64_t n_pad)
 {
     constexpr int kRowsPerWarp = 8;
+    constexpr int kLanes = D / 8, kRowsPerInst = 32 / kLanes, kU = kRowsPerWarp / kRowsPerInst;
     const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthreads = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = tid; i < acc_vec; i += nthreads)
@@ -1562,31 +1589,31 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
             stat2[i] = make_float2(0.f, 0.f);
     }
     const int64_t rows = total * H;
-    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    const int lane = threadIdx.x & 31, sub = lane / kLanes, l16 = lane % kLanes;
     for (int64_t base = (tid >> 5) * kRowsPerWarp; base < rows;
          base += (nthreads >> 5) * kRowsPerWarp) {
         // every load of the 8 rows first (the row's sequence, found by binary
         // search in cu_seqlens, and its lse too, in the row's leading lane),
         // then the dot products
-        uint4 o[kRowsPerWarp / 2], g[kRowsPerWarp / 2];
-        int64_t dq_[kRowsPerWarp / 2], sq[kRowsPerWarp / 2];
-        float lv[kRowsPerWarp / 2];
+        uint4 o[kU], g[kU];
+        int64_t dq_[kU], sq[kU];
+        float lv[kU];
         // (token, h) of the group's first row by division, the others by carry
         const int64_t token0 = base / H;
         const int h0 = int(base - token0 * H);
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
-            const int64_t row = base + 2 * u + half;
+        for (int u = 0; u < kU; ++u) {
+            const int64_t row = base + u * kRowsPerInst + sub;
             o[u] = make_uint4(0, 0, 0, 0);
             g[u] = o[u];
             lv[u] = 0.f;
             dq_[u] = 0;
             sq[u] = -1;                              // no pair for this row
             if (row < rows) {
-                o[u] = reinterpret_cast<const uint4 *>(O + row * 128)[l16];
-                g[u] = reinterpret_cast<const uint4 *>(dO + row * 128)[l16];
+                o[u] = reinterpret_cast<const uint4 *>(O + row * D)[l16];
+                g[u] = reinterpret_cast<const uint4 *>(dO + row * D)[l16];
                 if (l16 == 0) {
-                    int hh = h0 + 2 * u + half;
+                    int hh = h0 + u * kRowsPerInst + sub;
                     int64_t token = token0;
                     while (hh >= H) {
                         hh -= H;
@@ -1609,7 +1636,7 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
             }
         }
 #pragma unroll
-        for (int u = 0; u < kRowsPerWarp / 2; ++u) {
+        for (int u = 0; u < kU; ++u) {
             const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&o[u]);
             const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g[u]);
             float sum = 0.f;
@@ -1620,9 +1647,9 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
                 sum = fmaf(a.y, c.y, sum);
             }
 #pragma unroll
-            for (int m = 8; m > 0; m >>= 1)
+            for (int m = kLanes / 2; m > 0; m >>= 1)
                 sum += __shfl_xor_sync(0xffffffffu, sum, m);
-            if (l16 == 0 && base + 2 * u + half < rows) {
+            if (l16 == 0 && base + u * kRowsPerInst + sub < rows) {
                 Dv[dq_[u]] = sum;
                 if (sq[u] >= 0)
                     stat2[sq[u]] = make_float2(lv[u] * kLog2e, sum);
@@ -1633,11 +1660,12 @@ __global__ void __launch_bounds__(256) bwd_prep_packed_kernel(
 
 // The conversion for packed batches: dQ[t, h, :] = bf16(scale *
 // acc[h, t, :]) for t < total.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_packed_kernel(const float4 *acc, uint4 *dQ,
                                                                     int H, int64_t total,
                                                                     int64_t total_pad, float scale)
 {
-    constexpr int D = 128, kVec = D / 8, kUnroll = 4;
+    constexpr int kVec = D / 8, kUnroll = 4;
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the pass's sums are complete
     const int64_t n = int64_t(H) * total * kVec;      // (h, t, 8-element group)
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -1750,9 +1778,64 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
                      : launch_bwd_d<128, false>(p_dq, p_dkdv, stream);
 }
 
+namespace {
+// The one-pass form's three launches at head dim D.
+template <int D>
+int launch_bwd_atomic_d(const AttnBwdArgs &a, BwdParams &p, int64_t blocks, int64_t acc_floats,
+                        int sms, cudaStream_t stream)
+{
+    const bool packed = a.cu_seqlens != nullptr;
+    static PerDeviceOnce once_fused, once_fused_packed;
+    auto kf = packed ? attn_bwd_fused_kernel<D, true> : attn_bwd_fused_kernel<D, false>;
+    if (!set_max_dynamic_smem(packed ? once_fused_packed : once_fused,
+                              reinterpret_cast<const void *>(kf), int(CfgF<D>::kSmemBytes)))
+        return FA_ERR_CUDA;
+    if (packed)
+        bwd_prep_packed_kernel<D><<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
+            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, a.cu_seqlens, a.B, a.H,
+            p.total, p.n_pad);
+    else
+        bwd_prep_kernel<D><<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
+            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
+            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, p.total * a.H, a.H, a.N,
+            p.n_pad);
+    if (cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    // the pass and the conversion are programmatic dependents of the kernel
+    // before them (no early trigger: each may start as the previous one's
+    // CTAs exit, and waits for its completion before reading its output)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CfgF<D>::kSmemBytes;
+    if (cudaLaunchKernelEx(&cfg, kf, p) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+        return FA_ERR_CUDA;
+    cfg.gridDim = dim3(unsigned(sms * 8));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    const cudaError_t e =
+        packed ? cudaLaunchKernelEx(&cfg, bwd_dq_convert_packed_kernel<D>,
+                                    reinterpret_cast<const float4 *>(a.dq_acc),
+                                    reinterpret_cast<uint4 *>(p.dQ), a.H, p.total, p.total_pad,
+                                    a.scale)
+               : cudaLaunchKernelEx(&cfg, bwd_dq_convert_kernel<D>,
+                                    reinterpret_cast<const float4 *>(a.dq_acc),
+                                    reinterpret_cast<uint4 *>(p.dQ), int64_t(a.B) * a.H, a.H,
+                                    a.N, p.n_pad, a.scale);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+}  // namespace
+
 int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
 {
-    if (a.d != 128 || a.dq_acc == nullptr)
+    if ((a.d != 64 && a.d != 128) || a.dq_acc == nullptr)
         return FA_ERR_UNSUPPORTED;
     const bool packed = a.cu_seqlens != nullptr;
     BwdParams p;
@@ -1780,8 +1863,8 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     p.n_pad = n_pad;
     p.total_pad = total + 64;
     // workspace: the accumulator, then the (lse log2 e, D) pairs
-    const int64_t acc_floats = packed ? int64_t(a.H) * p.total_pad * 128
-                                      : int64_t(a.B) * a.H * n_pad * 128;
+    const int64_t acc_floats = packed ? int64_t(a.H) * p.total_pad * a.d
+                                      : int64_t(a.B) * a.H * n_pad * a.d;
     p.stat2 = reinterpret_cast<const float2 *>(a.dq_acc + acc_floats);
     const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
     if (blocks == 0 || total == 0)
@@ -1793,54 +1876,12 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
         !make_tmap_bf16(&p.tm_s0, a.Q, total, a.H, a.d, BS) ||
         !make_tmap_bf16(&p.tm_s1, a.dO, total, a.H, a.d, BS))
         return FA_ERR_CUDA;
-    static PerDeviceOnce once_fused, once_fused_packed;
-    auto kf = packed ? attn_bwd_fused_kernel<true> : attn_bwd_fused_kernel<false>;
-    if (!set_max_dynamic_smem(packed ? once_fused_packed : once_fused,
-                              reinterpret_cast<const void *>(kf), int(CfgF::kSmemBytes)))
-        return FA_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
-    if (packed)
-        bwd_prep_packed_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
-            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, a.cu_seqlens, a.B, a.H, total,
-            n_pad);
-    else
-        bwd_prep_kernel<<<dim3(unsigned(sms * 8)), dim3(256), 0, stream>>>(
-            p.O, p.dO, a.lse, a.D, const_cast<float2 *>(p.stat2),
-            reinterpret_cast<float4 *>(a.dq_acc), acc_floats / 4, total * a.H, a.H, a.N, n_pad);
-    if (cudaGetLastError() != cudaSuccess)
-        return FA_ERR_CUDA;
-    // the pass and the conversion are programmatic dependents of the kernel
-    // before them (no early trigger: each may start as the previous one's
-    // CTAs exit, and waits for its completion before reading its output)
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(unsigned(blocks));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = CfgF::kSmemBytes;
-    if (cudaLaunchKernelEx(&cfg, kf, p) != cudaSuccess || cudaGetLastError() != cudaSuccess)
-        return FA_ERR_CUDA;
-    cfg.gridDim = dim3(unsigned(sms * 8));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    const cudaError_t e =
-        packed ? cudaLaunchKernelEx(&cfg, bwd_dq_convert_packed_kernel,
-                                    reinterpret_cast<const float4 *>(a.dq_acc),
-                                    reinterpret_cast<uint4 *>(p.dQ), a.H, total, p.total_pad,
-                                    a.scale)
-               : cudaLaunchKernelEx(&cfg, bwd_dq_convert_kernel,
-                                    reinterpret_cast<const float4 *>(a.dq_acc),
-                                    reinterpret_cast<uint4 *>(p.dQ), int64_t(a.B) * a.H, a.H,
-                                    a.N, n_pad, a.scale);
-    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return a.d == 64 ? launch_bwd_atomic_d<64>(a, p, blocks, acc_floats, sms, stream)
+                     : launch_bwd_atomic_d<128>(a, p, blocks, acc_floats, sms, stream);
 }
 
 }  // namespace fa

@@ -370,8 +370,6 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
         return FA_ERR_BAD_SIZE;
     if (d != 64 && d != 128)
         return FA_ERR_UNSUPPORTED;
-    if (one_pass && d != 128)
-        return FA_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || N == 0 || total == 0)
         return FA_OK;
     if (!Q || !K || !V || !O || !dO || !lse || !dQ || !dK || !dV || !D_buf ||
@@ -387,8 +385,8 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
     if (total > (int64_t(1) << 31) - 512 || int64_t(N) > (int64_t(1) << 31) - 512 ||
         total * int64_t(H) * int64_t(d) > (int64_t(1) << 56))
         return FA_ERR_TOO_LARGE;
-    if (one_pass && workspace_bytes < (cu_seqlens ? bwd_atomic_varlen_workspace_bytes(B, H, N, total)
-                                                  : bwd_atomic_workspace_bytes(B, H, N)))
+    if (one_pass && workspace_bytes < (cu_seqlens ? bwd_atomic_varlen_workspace_bytes(B, H, N, total, d)
+                                                  : bwd_atomic_workspace_bytes(B, H, N, d)))
         return FA_ERR_BAD_SIZE;
     DeviceInfo *dev = current_device();
     if (dev == nullptr)
@@ -524,18 +522,18 @@ int64_t fa_attention_bwd_atomic_varlen_workspace_bytes(int B, int H, int N, int6
 {
     if (B < 0 || H < 0 || N < 0 || total < 0)
         return FA_ERR_BAD_SIZE;
-    if (d != 128)
+    if (d != 64 && d != 128)
         return FA_ERR_UNSUPPORTED;
-    return fa::bwd_atomic_varlen_workspace_bytes(B, H, N, total);
+    return fa::bwd_atomic_varlen_workspace_bytes(B, H, N, total, d);
 }
 
 int64_t fa_attention_bwd_atomic_workspace_bytes(int B, int H, int N, int d)
 {
     if (B < 0 || H < 0 || N < 0)
         return FA_ERR_BAD_SIZE;
-    if (d != 128)
+    if (d != 64 && d != 128)
         return FA_ERR_UNSUPPORTED;
-    return fa::bwd_atomic_workspace_bytes(B, H, N);
+    return fa::bwd_atomic_workspace_bytes(B, H, N, d);
 }
 
 }  // extern "C"

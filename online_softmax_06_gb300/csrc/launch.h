@@ -123,20 +123,20 @@ struct AttnBwdArgs {
     float *dq_acc = nullptr;              // one-pass form: the workspace (see below)
 };
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
-// One-pass backward (d = 128, dense or packed): dQ summed over the key tiles
+// One-pass backward (d = 64 or 128, dense or packed): dQ summed over the key tiles
 // by fp32 atomic adds into the workspace a.dq_acc, then converted.
 int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream);
 inline int64_t bwd_atomic_n_pad(int N) { return (int64_t(N) + 63) / 64 * 64; }
-// Workspace of the one-pass form (d = 128): the fp32 dQ accumulator [B H,
-// n_pad, 128], then (lse log2 e, D) pairs [B H, n_pad]; packed batches: the
-// accumulator [H, total + 64, 128], then the pairs [H, B, n_pad].
-inline int64_t bwd_atomic_workspace_bytes(int B, int H, int N)
+// Workspace of the one-pass form (d = 64, 128): the fp32 dQ accumulator [B H,
+// n_pad, d], then (lse log2 e, D) pairs [B H, n_pad]; packed batches: the
+// accumulator [H, total + 64, d], then the pairs [H, B, n_pad].
+inline int64_t bwd_atomic_workspace_bytes(int B, int H, int N, int d)
 {
-    return int64_t(B) * H * bwd_atomic_n_pad(N) * (128 + 2) * 4;
+    return int64_t(B) * H * bwd_atomic_n_pad(N) * (d + 2) * 4;
 }
-inline int64_t bwd_atomic_varlen_workspace_bytes(int B, int H, int N, int64_t total)
+inline int64_t bwd_atomic_varlen_workspace_bytes(int B, int H, int N, int64_t total, int d)
 {
-    return int64_t(H) * (total + 64) * 128 * 4 + int64_t(H) * B * bwd_atomic_n_pad(N) * 8;
+    return int64_t(H) * (total + 64) * d * 4 + int64_t(H) * B * bwd_atomic_n_pad(N) * 8;
 }
 
 // Quantisation pass of the FP8 forward (dense [B, N, H, d] bf16 inputs).

@@ -100,20 +100,22 @@ def test_one_pass_backward_host_checks_without_gpu(lib):
     return before any CUDA call."""
     wb = fa.fa_attention_bwd_atomic_workspace_bytes
     assert wb(-1, 1, 8, 128) == fa.FA_ERR_BAD_SIZE
-    assert wb(1, 1, 8, 64) == fa.FA_ERR_UNSUPPORTED
-    # accumulator [B H, n_pad, 128] fp32 and (lse, D) pairs [B H, n_pad], n_pad = 64
+    assert wb(1, 1, 8, 96) == fa.FA_ERR_UNSUPPORTED
+    # accumulator [B H, n_pad, d] fp32 and (lse, D) pairs [B H, n_pad], n_pad = 64
     assert wb(2, 3, 50, 128) == 2 * 3 * 64 * (128 + 2) * 4
+    assert wb(2, 3, 50, 64) == 2 * 3 * 64 * (64 + 2) * 4
     assert wb(2, 3, 64, 128) == wb(2, 3, 50, 128)
     assert wb(2, 3, 65, 128) == 2 * 3 * 128 * (128 + 2) * 4
     vb = fa.fa_attention_bwd_atomic_varlen_workspace_bytes
     assert vb(2, 3, 50, -1, 128) == fa.FA_ERR_BAD_SIZE
-    assert vb(2, 3, 50, 90, 64) == fa.FA_ERR_UNSUPPORTED
-    # accumulator [H, total + 64, 128] fp32 and pairs [H, B, n_pad]
+    assert vb(2, 3, 50, 90, 96) == fa.FA_ERR_UNSUPPORTED
+    # accumulator [H, total + 64, d] fp32 and pairs [H, B, n_pad]
     assert vb(2, 3, 50, 90, 128) == 3 * (90 + 64) * 128 * 4 + 3 * 2 * 64 * 8
+    assert vb(2, 3, 50, 90, 64) == 3 * (90 + 64) * 64 * 4 + 3 * 2 * 64 * 8
     call = fa.fa_attention_bwd_atomic
     p = [None] * 10
     assert call(*p, 1, 1, -1, 128, 1.0, 0, None, 0) == fa.FA_ERR_BAD_SIZE
-    assert call(*p, 1, 1, 8, 64, 1.0, 0, None, 0) == fa.FA_ERR_UNSUPPORTED
+    assert call(*p, 1, 1, 8, 96, 1.0, 0, None, 0) == fa.FA_ERR_UNSUPPORTED
     assert call(*p, 0, 1, 8, 128, 1.0, 0, None, 0) == 0
     assert call(*p, 1, 1, 8, 128, 1.0, 0, None, 0) == fa.FA_ERR_NULL_POINTER
     assert call(*p, 1, 1, 8, 128, 1.0, 0, None, -1) == fa.FA_ERR_BAD_SIZE

@@ -52,28 +52,31 @@ def normwise(g, ref, floor=1e-30):
 ZERO_FLOOR = 1e-3
 
 
-@pytest.mark.parametrize("B,H,N,causal", [
-    (1, 2, 128, False),
-    (2, 2, 256, True),
-    (1, 3, 300, True),       # ragged last key tile and query sub-tile
-    (2, 2, 200, False),      # ragged: a tile's last key rows are the next sequence's
-    (3, 1, 170, True),       # the same, causal, three sequences
-    (1, 1, 1, True),         # one token
-    (1, 2, 385, False),
-    (1, 2, 192, True),       # last key tile of one 64-row sub-tile
-    (1, 1, 65, True),        # two sub-tiles, one tile
-    (1, 2, 1000, True),      # 16 sub-steps: the 3-stage ring and both dS buffers wrap
-    (2, 1, 900, False),
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (1, 2, 128, 64, False),
+    (2, 2, 200, 64, False),      # d = 64: ragged, a tile's last key rows are the next sequence's
+    (1, 2, 1000, 64, True),      # d = 64: ring and dS buffers wrap
+    (1, 1, 1, 64, True),
+    (1, 2, 128, 128, False),
+    (2, 2, 256, 128, True),
+    (1, 3, 300, 128, True),  # ragged last key tile and query sub-tile
+    (2, 2, 200, 128, False), # ragged: a tile's last key rows are the next sequence's
+    (3, 1, 170, 128, True),  # the same, causal, three sequences
+    (1, 1, 1, 128, True),    # one token
+    (1, 2, 385, 128, False),
+    (1, 2, 192, 128, True),  # last key tile of one 64-row sub-tile
+    (1, 1, 65, 128, True),   # two sub-tiles, one tile
+    (1, 2, 1000, 128, True), # 16 sub-steps: the 3-stage ring and both dS buffers wrap
+    (2, 1, 900, 128, False),
 ])
-def test_bwd_atomic_matches_oracle(dev, B, H, N, causal):
-    d = 128
+def test_bwd_atomic_matches_oracle(dev, B, H, N, d, causal):
     Q, K, V, dO = make_inputs(B, H, N, d, seed=N * 11 + B)
     dq, dk, dv = run_gpu(Q, K, V, dO, causal, dev)
     ref = oracle.attention_bwd(*(t.float().numpy() for t in (Q, K, V, dO)), 1 / math.sqrt(d),
                                causal)
     errs = {name: normwise(g, ref[name], ZERO_FLOOR)
             for name, g in (("dQ", dq), ("dK", dk), ("dV", dv))}
-    print(f"one-pass B{B} H{H} N{N} causal={causal}: normwise errors {errs}")
+    print(f"one-pass B{B} H{H} N{N} d{d} causal={causal}: normwise errors {errs}")
     for name, e in errs.items():
         assert e <= BWD_TOL, f"{name}: {e}"
     device_error_clear()
@@ -147,10 +150,11 @@ def test_bwd_atomic_bad_arguments(dev):
     p, l, w = q.data_ptr(), lse.data_ptr(), ws.data_ptr()
     need = fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 128)
     assert need == 128 * 130 * 4
-    assert fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 64) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 96) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_attention_bwd_atomic_workspace_bytes(1, 1, 128, 64) == 128 * 66 * 4
     assert fa.fa_attention_bwd_atomic_workspace_bytes(-1, 1, 128, 128) == fa.FA_ERR_BAD_SIZE
     call = fa.fa_attention_bwd_atomic
-    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 64, 0.1, 0, w, need) == \
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 96, 0.1, 0, w, need) == \
         fa.FA_ERR_UNSUPPORTED
     assert call(p, p, p, p, p, l, p, p, p, l, 1, 1, 128, 128, 0.1, 0, None, need) == \
         fa.FA_ERR_NULL_POINTER
@@ -171,14 +175,15 @@ def run_gpu_packed(Q, K, V, dO, cu, max_len, causal, dev):
     return [t.float().cpu().numpy() for t in (dq, dk, dv)]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("lens", [[1, 129, 300, 64, 257, 0, 128, 700], [1000, 3]])
-def test_bwd_atomic_packed_matches_oracle(dev, lens, causal):
+def test_bwd_atomic_packed_matches_oracle(dev, lens, causal, d):
     """Packed sequences (ragged lengths, an empty one, one token, a long one
     whose ring wraps): every gradient against the oracle's per-sequence
     backward."""
     import workloads
-    d, H = 128, 3
+    H = 3
     cu = workloads.cu_seqlens_of(lens)
     total = int(cu[-1])
     rng = np.random.default_rng(sum(lens) + 11 * causal)
@@ -189,7 +194,7 @@ def test_bwd_atomic_packed_matches_oracle(dev, lens, causal):
                                       1 / math.sqrt(d), causal)
     errs = {name: normwise(g, ref[name], ZERO_FLOOR)
             for name, g in (("dQ", dq), ("dK", dk), ("dV", dv))}
-    print(f"one-pass packed {lens} causal={causal}: normwise errors {errs}")
+    print(f"one-pass packed {lens} d{d} causal={causal}: normwise errors {errs}")
     for name, e in errs.items():
         assert e <= BWD_TOL, f"{name}: {e}"
     device_error_clear()
@@ -231,9 +236,9 @@ def test_bwd_atomic_packed_length_over_n_is_flagged(dev):
                 nbytes) == fa.FA_ERR_NULL_POINTER
     assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, d, 0.125, 1, cu.data_ptr(), w,
                 nbytes - 8) == fa.FA_ERR_BAD_SIZE
-    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, 64, 0.125, 1, cu.data_ptr(), w,
+    assert call(p, p, p, p, p, l, p, p, p, l, 1, H, 200, 300, 96, 0.125, 1, cu.data_ptr(), w,
                 nbytes) == fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_attention_bwd_atomic_varlen_workspace_bytes(1, H, 200, 300, 64) == \
+    assert fa.fa_attention_bwd_atomic_varlen_workspace_bytes(1, H, 200, 300, 96) == \
         fa.FA_ERR_UNSUPPORTED
 
 
