@@ -101,6 +101,8 @@ struct Bf16Params {
     int H_row;                       // heads per token row of Q/K/V/O and per (b) in lse
     int Nk;                          // keys per sequence (dense); packed batches use L
     int n_pairs;                     // Q-tile pairs per (sequence, head) at length N
+    int head_groups;                 // the (sequence, head) pairs in this many consecutive
+                                     // groups, heaviest Q-tile pairs first within each
     int64_t total;                   // query rows of Q / O
     float scale_log2;                // scale * log2(e)
     int causal;
@@ -164,14 +166,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     // ---- work item: (sequence b, head h, Q-tile pair, key split), heaviest
-    //      pairs first ------------------------------------------------------------
+    //      pairs first within each group of (sequence, head) pairs (the
+    //      groups run one after another, so only a group's K/V compete for
+    //      L2) ----------------------------------------------------------------------
     const int bh_count = p.B * p.H;
     const int n_splits = SPLIT ? p.splits : 1;
     int kv_off = SPLIT ? p.kv_off : 0;
     const int split = SPLIT ? int(blockIdx.x % unsigned(n_splits)) : 0;
     const int rest = SPLIT ? int(blockIdx.x / unsigned(n_splits)) : int(blockIdx.x);
-    const int pair = p.n_pairs - 1 - rest / bh_count;
-    const int bh = rest % bh_count;
+    int pair, bh;
+    if (SPLIT || FP8 || p.head_groups <= 1) {   // (FP8: K', V' are small enough for L2)
+        pair = p.n_pairs - 1 - rest / bh_count;
+        bh = rest % bh_count;
+    } else {
+        const int gsz = bh_count / p.head_groups;           // pairs per group
+        const int grp = rest / (p.n_pairs * gsz);
+        const int in_grp = rest - grp * (p.n_pairs * gsz);
+        pair = p.n_pairs - 1 - in_grp / gsz;
+        bh = grp * gsz + in_grp % gsz;
+    }
     const int b = bh / p.H, h = bh % p.H;
     int64_t start, start_k;    // first query row / first key row of the sequence
     int L, Lk;                 // query and key counts of the sequence
@@ -856,6 +869,39 @@ int launch_d(const Bf16Params &p, int64_t blocks, cudaStream_t stream)
 
 }  // namespace
 
+namespace {
+// Groups of (sequence, head) pairs for a dense, unsplit launch.  With every
+// head's heaviest Q-tile pairs first, all heads' K and V are read at once;
+// when they exceed what L2 holds, tiles are evicted between the Q-tile pairs
+// that share them and read again from DRAM.  Past half of L2 (64 MB) the
+// heads are therefore taken in consecutive groups, each small enough (about
+// 32 MB of K and V) to stay in L2, as long as every group still fills the GPU
+// (at least 1.5 waves of CTAs); below it one group (grouping then only adds
+// the tails of the group boundaries).  1: one group.
+int choose_head_groups(int bh, int n_pairs, int64_t kv_bytes_per_head)
+{
+    constexpr int64_t kGroupBytes = int64_t(32) << 20, kOneGroupBytes = int64_t(64) << 20;
+    if (kv_bytes_per_head * bh <= kOneGroupBytes)
+        return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return 1;
+    int best = 1;
+    for (int g = 2; g <= bh; ++g) {
+        if (bh % g != 0)
+            continue;
+        if (2 * int64_t(n_pairs) * (bh / g) < 3 * int64_t(sms))
+            break;                       // fewer CTAs per group than 1.5 waves
+        best = g;
+        if (kv_bytes_per_head * (bh / g) <= kGroupBytes)
+            break;
+    }
+    return best;
+}
+}  // namespace
+
 int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
 {
     Bf16Params p;
@@ -895,6 +941,11 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
     const bool split = p.splits > 1 || p.kv_off != 0 || Nk != a.N || a.cu_seqlens_k != nullptr;
+    // dense, unsplit launches take the heads in L2-sized groups (packed
+    // batches keep one group: a late group of long sequences would be a tail)
+    p.head_groups = split || a.cu_seqlens != nullptr
+                        ? 1
+                        : choose_head_groups(a.B * a.H, p.n_pairs, int64_t(4) * a.N * a.d);
     int rc;
     if (a.d == 64)
         rc = split ? launch_d<64, true>(p, blocks, stream) : launch_d<64, false>(p, blocks, stream);
@@ -904,6 +955,7 @@ int launch_attention_bf16(const AttnArgs &a, cudaStream_t stream)
         return rc;
     return launch_attention_combine(a, stream);
 }
+
 
 int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
 {
@@ -945,6 +997,7 @@ int launch_attention_fp8(const AttnFp8Args &a, cudaStream_t stream)
         return FA_OK;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
+    p.head_groups = 1;                // K' and V'^T, one byte per element, stay in L2
     auto kern = attn_fwd_bf16_kernel<128, false, true>;
     static PerDeviceOnce once;
     if (!set_max_dynamic_smem(once, reinterpret_cast<const void *>(kern),
