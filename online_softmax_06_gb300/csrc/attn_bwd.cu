@@ -130,6 +130,8 @@ struct BwdParams {
                                      // (packed: [H, B, n_pad])
     int64_t n_pad;                   // N rounded up to 64
     int64_t total_pad;               // packed: total + 64 (a last sub-tile's reach)
+    int head_groups;                 // one-pass kernel: the (sequence, head) pairs in this
+                                     // many consecutive groups, heaviest key tiles first
 };
 
 // Rows of sequence b: its first row, its length and the index of its first
@@ -1072,9 +1074,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    // work item (sequence, head, key tile): low key tiles (the most query
+    // steps when causal) first within each group of (sequence, head) pairs;
+    // the groups run one after another so that a group's Q, dO and dQ sums
+    // stay in L2
     const int bh_count = p.B * p.H;
-    const int kt = int(blockIdx.x) / bh_count;       // causal: low key tiles see most
-    const int bh = int(blockIdx.x) % bh_count;
+    int kt, bh;
+    if (p.head_groups <= 1) {
+        kt = int(blockIdx.x) / bh_count;
+        bh = int(blockIdx.x) % bh_count;
+    } else {
+        const int gsz = bh_count / p.head_groups;
+        const int grp = int(blockIdx.x) / (p.n_tiles * gsz);
+        const int in_grp = int(blockIdx.x) - grp * (p.n_tiles * gsz);
+        kt = in_grp / gsz;
+        bh = grp * gsz + in_grp % gsz;
+    }
     const int b = bh / p.H, h = bh % p.H;
     SeqRows sq;
     if (!seq_rows<PACKED>(p, b, h, sq) || kt * BT >= sq.L)
@@ -1880,6 +1895,23 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
+    // Every key-tile CTA of a head streams the head's Q and dO and adds into
+    // its dQ sums (8 N d bytes a head).  Past half of L2 the heads run in
+    // consecutive groups of about 32 MB, each keeping at least 1.5 waves of
+    // CTAs; packed batches keep one group.
+    p.head_groups = 1;
+    const int bh = a.B * a.H;
+    const int64_t per_head = int64_t(8) * a.N * a.d;
+    if (!packed && per_head * bh > (int64_t(64) << 20))
+        for (int g = 2; g <= bh; ++g) {
+            if (bh % g != 0)
+                continue;
+            if (2 * int64_t(p.n_tiles) * (bh / g) < 3 * int64_t(sms))
+                break;
+            p.head_groups = g;
+            if (per_head * (bh / g) <= (int64_t(32) << 20))
+                break;
+        }
     return a.d == 64 ? launch_bwd_atomic_d<64>(a, p, blocks, acc_floats, sms, stream)
                      : launch_bwd_atomic_d<128>(a, p, blocks, acc_floats, sms, stream);
 }
