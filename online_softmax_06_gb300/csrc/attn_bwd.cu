@@ -355,9 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    // work item (sequence, head, query tile), the heaviest query tiles first
+    // within each group of (sequence, head) pairs (see bwd_head_groups)
     const int bh_count = p.B * p.H;
-    const int qt = p.n_tiles - 1 - int(blockIdx.x) / bh_count;
-    const int bh = int(blockIdx.x) % bh_count;
+    int qt, bh;
+    if (p.head_groups <= 1) {
+        qt = p.n_tiles - 1 - int(blockIdx.x) / bh_count;
+        bh = int(blockIdx.x) % bh_count;
+    } else {
+        const int gsz = bh_count / p.head_groups;
+        const int grp = int(blockIdx.x) / (p.n_tiles * gsz);
+        const int in_grp = int(blockIdx.x) - grp * (p.n_tiles * gsz);
+        qt = p.n_tiles - 1 - in_grp / gsz;
+        bh = grp * gsz + in_grp % gsz;
+    }
     const int b = bh / p.H, h = bh % p.H;
     SeqRows sq;
     if (!seq_rows<PACKED>(p, b, h, sq) || qt * BT >= sq.L)
@@ -733,9 +744,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + C::kBarBytes);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    // work item (sequence, head, key tile): low key tiles (the most query
+    // steps when causal) first within each group of (sequence, head) pairs
     const int bh_count = p.B * p.H;
-    const int kt = int(blockIdx.x) / bh_count;       // causal: low key tiles see most
-    const int bh = int(blockIdx.x) % bh_count;
+    int kt, bh;
+    if (p.head_groups <= 1) {
+        kt = int(blockIdx.x) / bh_count;
+        bh = int(blockIdx.x) % bh_count;
+    } else {
+        const int gsz = bh_count / p.head_groups;
+        const int grp = int(blockIdx.x) / (p.n_tiles * gsz);
+        const int in_grp = int(blockIdx.x) - grp * (p.n_tiles * gsz);
+        kt = in_grp / gsz;
+        bh = grp * gsz + in_grp % gsz;
+    }
     const int b = bh / p.H, h = bh % p.H;
     SeqRows sq;
     if (!seq_rows<PACKED>(p, b, h, sq) || kt * BT >= sq.L)
@@ -1747,6 +1769,32 @@ int launch_bwd_d(const BwdParams &p_dq, const BwdParams &p_dkdv, cudaStream_t st
 
 }  // namespace
 
+namespace {
+// Groups of (sequence, head) pairs for a dense launch in which every tile CTA
+// of a head streams `per_head` bytes of that head (the other side's tiles,
+// and the dQ sums).  With all heads' heaviest tiles first, those bytes exceed
+// L2 and are read again from DRAM; past half of L2 (64 MB) the heads run in
+// consecutive groups of about 32 MB, as long as every group keeps at least
+// 1.5 waves of CTAs.  1: one group.
+int bwd_head_groups(int bh, int n_tiles, int64_t per_head, int sms)
+{
+    int best = 1;
+    if (per_head * bh <= (int64_t(64) << 20) || sms <= 0)
+        return best;
+    for (int g = 2; g <= bh; ++g) {
+        if (bh % g != 0)
+            continue;
+        if (2 * int64_t(n_tiles) * (bh / g) < 3 * int64_t(sms))
+            break;
+        best = g;
+        if (per_head * (bh / g) <= (int64_t(32) << 20))
+            break;
+    }
+    return best;
+}
+
+}  // namespace
+
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
 {
     BwdParams p;
@@ -1774,6 +1822,15 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
         return FA_OK;
     if (blocks > 0x7fffffffLL)
         return FA_ERR_TOO_LARGE;
+    // the dQ kernel streams each head's K and V, the dK/dV kernel its Q and
+    // dO: 4 N d bytes a head each
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FA_ERR_CUDA;
+    p.head_groups = a.cu_seqlens != nullptr
+                        ? 1
+                        : bwd_head_groups(a.B * a.H, p.n_tiles, int64_t(4) * a.N * a.d, sms);
     BwdParams p_dq = p, p_dkdv = p;
     if (!make_tmap_bf16(&p_dq.tm_a0, a.Q, total, a.H, a.d, BT) ||
         !make_tmap_bf16(&p_dq.tm_a1, a.dO, total, a.H, a.d, BT) ||
@@ -1895,23 +1952,9 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return FA_ERR_CUDA;
-    // Every key-tile CTA of a head streams the head's Q and dO and adds into
-    // its dQ sums (8 N d bytes a head).  Past half of L2 the heads run in
-    // consecutive groups of about 32 MB, each keeping at least 1.5 waves of
-    // CTAs; packed batches keep one group.
-    p.head_groups = 1;
-    const int bh = a.B * a.H;
-    const int64_t per_head = int64_t(8) * a.N * a.d;
-    if (!packed && per_head * bh > (int64_t(64) << 20))
-        for (int g = 2; g <= bh; ++g) {
-            if (bh % g != 0)
-                continue;
-            if (2 * int64_t(p.n_tiles) * (bh / g) < 3 * int64_t(sms))
-                break;
-            p.head_groups = g;
-            if (per_head * (bh / g) <= (int64_t(32) << 20))
-                break;
-        }
+    // every key-tile CTA of a head streams the head's Q and dO and adds into
+    // its dQ sums: 8 N d bytes a head
+    p.head_groups = packed ? 1 : bwd_head_groups(a.B * a.H, p.n_tiles, int64_t(8) * a.N * a.d, sms);
     return a.d == 64 ? launch_bwd_atomic_d<64>(a, p, blocks, acc_floats, sms, stream)
                      : launch_bwd_atomic_d<128>(a, p, blocks, acc_floats, sms, stream);
 }
