@@ -448,14 +448,17 @@ FA_API int fa_set_stream(void *stream);
 
 /*
  * Failure detection, for tests: arms a wait that cannot complete in the next
- * bf16 attention forward (fa_attention_fwd / fa_attention_fwd_varlen) launched
- * from this host thread.  In that launch the warp that issues the tensor-core
- * instructions first waits, bounded by `ns` nanoseconds, on a barrier that
- * nothing arrives at.  The wait runs out, sets FA_DEVERR_WAIT_TIMEOUT in the
- * device error word and raises the CTA's abort flag, and every CTA winds down
- * the way it does after any timed-out wait: the other roles leave their loops,
- * copies already issued are waited for, tensor memory is freed, and O and lse
- * are left unwritten.  The launch returns FA_OK; the error shows in
+ * bf16 attention forward (fa_attention_fwd / fa_attention_fwd_varlen) or
+ * one-pass backward (fa_attention_bwd_atomic / fa_attention_bwd_atomic_varlen)
+ * launched from this host thread, whichever comes first.  In that launch the
+ * warp that issues the tensor-core instructions first waits, bounded by `ns`
+ * nanoseconds, on a barrier that nothing arrives at.  The wait runs out, sets
+ * FA_DEVERR_WAIT_TIMEOUT in the device error word and raises the CTA's abort
+ * flag, and every CTA winds down the way it does after any timed-out wait: the
+ * other roles leave their loops, copies already issued are waited for, tensor
+ * memory is freed, and O and lse (forward) or dK and dV (backward) are left
+ * unwritten; the backward's dQ is converted from an accumulator that received
+ * nothing, so it reads zero.  The launch returns FA_OK; the error shows in
  * fa_get_device_error.  One-shot: the setting is consumed by that launch.  The
  * kernels' own waits keep their bound (2 s), so the device stays usable and the
  * next call runs normally.  ns: 1 .. 10^9 arms, 0 disarms.

@@ -132,6 +132,7 @@ struct BwdParams {
     int64_t total_pad;               // packed: total + 64 (a last sub-tile's reach)
     int head_groups;                 // one-pass kernel: the (sequence, head) pairs in this
                                      // many consecutive groups, heaviest key tiles first
+    uint32_t expire_wait_ns;         // one-pass kernel, failure-detection test only (0: off)
 };
 
 // Rows of sequence b: its first row, its length and the index of its first
@@ -1071,8 +1072,8 @@ struct CfgF {
     static constexpr uint32_t kStatBytes = kStages * 2 * BS * 4;   // (lse log2 e, D) pairs
     static constexpr uint32_t kOffBar = kOffStat + kStatBytes;
     // a_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], dp_read, dq_full,
-    // dq_free, o_full, drain
-    static constexpr int kBars = 1 + 2 * kStages + 9;
+    // dq_free, o_full, drain, never (nothing arrives: failure-detection test)
+    static constexpr int kBars = 1 + 2 * kStages + 10;
     static constexpr uint32_t kSmemBytes = kOffBar + 8 * kBars + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -1092,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = bars + 1 + 2 * C::kStages;          // [2]
     uint64_t *p_full = s_full + 2;                          // [2]
     uint64_t *dp_read = s_full + 4, *dq_full = s_full + 5, *dq_free = s_full + 6,
-             *o_full = s_full + 7, *drain = s_full + 8;
+             *o_full = s_full + 7, *drain = s_full + 8, *never = s_full + 9;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + 8 * C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -1138,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(dq_free, kRowWarps);
         ptx::mbar_init(o_full, 1);
         ptx::mbar_init(drain, 1);
+        ptx::mbar_init(never, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -1212,13 +1214,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 issued = s + 1;
             }
-            if (*abort_flag) {
-                // wait (bounded) for the copies in flight before the CTA ends:
-                // the last step issued into each stage
-                drain_wait(a_full, 0);
-                for (int s = issued - C::kStages > 0 ? issued - C::kStages : 0; s < issued; ++s)
-                    drain_wait(&kv_full[s % C::kStages], uint32_t(s / C::kStages) & 1u);
-            }
+            // wait (bounded) for the copies in flight before the CTA ends: the
+            // last step issued into each stage.  Done whether or not the flag
+            // is up yet: a short test timeout can raise it after this point,
+            // and without an abort these phases have completed or are about to.
+            drain_wait(a_full, 0);
+            for (int s = issued - C::kStages > 0 ? issued - C::kStages : 0; s < issued; ++s)
+                drain_wait(&kv_full[s % C::kStages], uint32_t(s / C::kStages) & 1u);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -1267,8 +1269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
+        // Failure-detection test: a wait on a barrier that nothing arrives at
+        // runs out after expire_wait_ns; it raises the error bit and the abort
+        // flag, and the CTA winds down as after any timed-out wait.
+        if (p.expire_wait_ns != 0u &&
+            !__all_sync(0xffffffffu, ptx::mbar_wait_limited(never, 0, abort_flag, p.err_word,
+                                                            p.expire_wait_ns)))
+            aborted = true;
         do {
-            if (!ptx::mbar_wait_warp(a_full, 0, abort_flag, p.err_word) || !issue_s(0)) {
+            if (aborted || !ptx::mbar_wait_warp(a_full, 0, abort_flag, p.err_word) ||
+                !issue_s(0)) {
                 aborted = true;
                 break;
             }
@@ -1817,6 +1827,7 @@ int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream)
     p.err_word = a.err_word;
     p.cu_seqlens = a.cu_seqlens;
     p.total = total;
+    p.expire_wait_ns = 0;
     const int64_t blocks = int64_t(p.n_tiles) * a.B * a.H;
     if (blocks == 0)
         return FA_OK;
@@ -1955,6 +1966,7 @@ int launch_attention_bwd_atomic(const AttnBwdArgs &a, cudaStream_t stream)
     // every key-tile CTA of a head streams the head's Q and dO and adds into
     // its dQ sums: 8 N d bytes a head
     p.head_groups = packed ? 1 : bwd_head_groups(a.B * a.H, p.n_tiles, int64_t(8) * a.N * a.d, sms);
+    p.expire_wait_ns = a.expire_wait_ns;
     return a.d == 64 ? launch_bwd_atomic_d<64>(a, p, blocks, acc_floats, sms, stream)
                      : launch_bwd_atomic_d<128>(a, p, blocks, acc_floats, sms, stream);
 }

@@ -18,7 +18,8 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 thread_local cudaStream_t t_stream = nullptr;
-// fa_debug_expire_next_wait: armed for the next bf16 forward from this thread
+// fa_debug_expire_next_wait: armed for the next bf16 forward or one-pass
+// backward from this thread
 thread_local uint32_t t_expire_wait_ns = 0;
 
 struct DeviceInfo {
@@ -413,6 +414,8 @@ int attention_bwd_common(const void *Q, const void *K, const void *V, const void
     a.total = total;
     if (one_pass) {
         a.dq_acc = static_cast<float *>(workspace);
+        a.expire_wait_ns = t_expire_wait_ns;
+        t_expire_wait_ns = 0;
         return launch_attention_bwd_atomic(a, t_stream);
     }
     return launch_attention_bwd(a, t_stream);

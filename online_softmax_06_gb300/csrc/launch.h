@@ -121,6 +121,10 @@ struct AttnBwdArgs {
     const int32_t *cu_seqlens = nullptr;  // packed: device [B + 1] prefix sums
     int64_t total = 0;                    // packed: rows of the tensors
     float *dq_acc = nullptr;              // one-pass form: the workspace (see below)
+    // failure-detection test (fa_debug_expire_next_wait), one-pass form only:
+    // nonzero makes the tensor-core warp wait that long on a barrier that
+    // nothing arrives at, so that the timeout path runs
+    uint32_t expire_wait_ns = 0;
 };
 int launch_attention_bwd(const AttnBwdArgs &a, cudaStream_t stream);
 // One-pass backward (d = 64 or 128, dense or packed): dQ summed over the key tiles
