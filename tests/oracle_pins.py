@@ -742,6 +742,41 @@ def pin_fp8_blockwise_scales(lib):
         assert np.all((rel <= 2.0 ** -4 + 1e-12) | tiny)
 
 
+def pin_fp8_inputs_are_blockwise_codes(lib):
+    """The method's inputs ([FG] §4.6, rotation then blockwise quantisation),
+    read from the format and an independent Hadamard matrix: Q' and K' are
+    e4m3 values times one scale per (sequence, head, 128-row tile) of the
+    rotated tensor (scipy's Hadamard matrix, the signs on its rows, over
+    sqrt d); V' is e4m3 values times one scale per (sequence, head), V not
+    rotated.  A block's scale is its largest magnitude over 448, so that
+    magnitude is kept."""
+    from scipy.linalg import hadamard
+    from oracle import fp8
+    vals = np.unique(np.abs(_e4m3_table()[0]))
+    rng = np.random.default_rng(46)
+    B, N, H, d = 2, 300, 3, 64
+    Q, K, V = (rng.standard_normal((B, N, H, d)) * rng.uniform(0.2, 5.0, (1, 1, H, 1))
+               for _ in range(3))
+    signs = rng.choice([-1.0, 1.0], size=d)
+    M = signs[:, None] * hadamard(d).astype(np.float64) / math.sqrt(d)
+    Qd, Kd, Vd = fp8.fp8_inputs(Q, K, V, signs)
+
+    def on_codes(deq, src, what):
+        s = np.abs(src).max() / 448.0
+        c = np.abs(deq / s).ravel()
+        nearest = vals[np.abs(c[:, None] - vals[None, :]).argmin(axis=1)]
+        assert np.all(np.abs(c - nearest) <= 1e-12 * np.maximum(c, 1.0)), what + ": not e4m3 codes"
+        assert abs(c.max() - 448.0) <= 1e-12 * 448.0, what + ": amax not kept"
+
+    for b in range(B):
+        for h in range(H):
+            on_codes(Vd[b, :, h], V[b, :, h], f"V' b={b} h={h}")
+            for X, Xd, name in ((Q, Qd, "Q'"), (K, Kd, "K'")):
+                for t in range(0, N, 128):
+                    rows = slice(t, min(t + 128, N))
+                    on_codes(Xd[b, rows, h], X[b, rows, h] @ M, f"{name} b={b} h={h} tile {t}")
+
+
 def pin_fp8_incoherent_processing_helps(lib):
     """The pages' claim ([FG] §4.6, a test with outliers: per-tensor FP8 RMSE
     2.4e-2 against 9.1e-3 with blockwise scales and the rotation).  Reading of

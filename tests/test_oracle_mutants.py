@@ -7,6 +7,7 @@ operand).  It is compiled on the CPU into a temporary library and the pins of
 would mean the pins cannot see that kind of mistake.
 """
 import os
+import shutil
 import subprocess
 import sys
 
@@ -56,6 +57,31 @@ MUTANTS = [
 ]
 
 
+# Mistakes planted in copies of ``oracle/fp8.py`` (the FP8 method's rotation
+# and quantisation), run against the FP8 pins.
+FP8_MUTANTS = [
+    ("fp8_hadamard_block_sign", "H = np.block([[H, H], [H, -H]])", "H = np.block([[H, H], [-H, H]])", 0),
+    ("fp8_rotation_unnormalised", "return (s[:, None] * sylvester_hadamard(d)) / math.sqrt(d)",
+     "return s[:, None] * sylvester_hadamard(d)", 0),
+    ("fp8_rotation_signs_on_columns", "(s[:, None] * sylvester_hadamard(d))",
+     "(sylvester_hadamard(d) * s[None, :])", 0),
+    ("fp8_e4m3_truncates", "np.round(a / ulp)", "np.floor(a / ulp)", 0),
+    ("fp8_e4m3_max_240", "E4M3_MAX = 448.0", "E4M3_MAX = 240.0", 0),
+    ("fp8_e4m3_subnormal_binade", "e = np.maximum(ex - 1, -6)", "e = np.maximum(ex - 1, -7)", 0),
+    ("fp8_e4m3_two_fraction_bits", "ulp = np.ldexp(1.0, e - 3)", "ulp = np.ldexp(1.0, e - 2)", 0),
+    ("fp8_scale_over_256", "amax / E4M3_MAX, 1.0", "amax / 256.0, 1.0", 0),
+    ("fp8_tile_64_rows", "TILE_ROWS = 128", "TILE_ROWS = 64", 0),
+    ("fp8_block_amax_signed", "sc = _scale_of(np.abs(blk).max(axis=(1, 3)))",
+     "sc = _scale_of(blk.max(axis=(1, 3)))", 0),
+    ("fp8_v_unquantised", "blockwise_qk(Kr)[0], per_head_v(V)[0]",
+     "blockwise_qk(Kr)[0], np.asarray(V, dtype=np.float64)", 0),
+    ("fp8_v_per_tensor", "blockwise_qk(Kr)[0], per_head_v(V)[0]",
+     "blockwise_qk(Kr)[0], per_tensor(V)[0]", 0),
+    ("fp8_q_unrotated", "Qr = rotate(Q, signs) if rotate_qk", "Qr = np.asarray(Q, dtype=np.float64) if rotate_qk", 0),
+    ("fp8_k_unrotated", "Kr = rotate(K, signs) if rotate_qk", "Kr = np.asarray(K, dtype=np.float64) if rotate_qk", 0),
+]
+
+
 def _mutate(src, old, new, occ):
     idx = -1
     for _ in range(occ + 1):
@@ -67,11 +93,13 @@ def _mutate(src, old, new, occ):
 
 _RUNNER = r"""
 import sys
-sys.path[:0] = [sys.argv[1], sys.argv[2]]
+sys.path[:0] = [p for p in sys.argv[1].split("|") if p] + [sys.argv[2]]
 import oracle, oracle_pins
+print("ORACLE_PACKAGE", oracle.__file__)
 lib = oracle.load(sys.argv[3])
+prefix = sys.argv[4] if len(sys.argv) > 4 else "pin_"
 failed = []
-for pin in oracle_pins.PINS:
+for pin in [p for p in oracle_pins.PINS if p.__name__.startswith(prefix)]:
     try:
         pin(lib)
     except Exception as e:
@@ -96,3 +124,24 @@ def test_mutant_is_caught(tmp_path, name, old, new, occ):
     r = subprocess.run([sys.executable, "-c", _RUNNER, root, tests, so],
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 3, f"mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name,old,new,occ", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_mutant_is_caught(tmp_path, name, old, new, occ):
+    """The same for the FP8 method's Python steps: a copy of the oracle
+    package whose ``fp8.py`` holds the mistake is put first on the path, and
+    the FP8 pins run against it."""
+    pkg = os.path.dirname(oracle.__file__)
+    dst = tmp_path / "oracle"
+    dst.mkdir()
+    for f in ("__init__.py", "oracle.c"):
+        shutil.copy(os.path.join(pkg, f), dst / f)
+    src = open(os.path.join(pkg, "fp8.py"), encoding="utf-8").read()
+    (dst / "fp8.py").write_text(_mutate(src, old, new, occ), encoding="utf-8")
+    so = oracle.compile_oracle(SRC, str(tmp_path / "liboracle.so"))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    tests = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _RUNNER, f"{tmp_path}|{root}", tests, so,
+                        "pin_fp8"], capture_output=True, text=True, timeout=300)
+    assert f"ORACLE_PACKAGE {dst / '__init__.py'}" in r.stdout, (r.stdout, r.stderr[-2000:])
+    assert r.returncode != 3, f"mutant {name} passed every FP8 pin"
