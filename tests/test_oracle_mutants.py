@@ -82,6 +82,20 @@ FP8_MUTANTS = [
 ]
 
 
+# Mistakes planted in copies of ``oracle/__init__.py``: the Python layer that
+# lays out the C oracle's results and slices packed batches per sequence.
+PY_MUTANTS = [
+    ("dense_lse_layout", "lse.reshape(H, B, N).transpose(1, 0, 2).copy()", "lse.reshape(B, H, N).copy()", 0),
+    ("qk_lse_layout", "lse.reshape(B, Nq, H).transpose(0, 2, 1).copy()", "lse.reshape(B, H, Nq).copy()", 0),
+    ("qk_packed_keys_at_query_offsets", "K[None, k0:k1], V[None, k0:k1]", "K[None, q0:q1], V[None, q0:q1]", 0),
+    ("qk_packed_values_at_query_offsets", "K[None, k0:k1], V[None, k0:k1]", "K[None, k0:k1], V[None, q0:q1]", 0),
+    ("bwd_packed_d_from_lse", 'out["D"][:, s0:s1] = g["D"][0]', 'out["D"][:, s0:s1] = g["lse"][0]', 0),
+    ("bwd_packed_v_and_do_swapped", "for X in (Q, K, V, dO)), scale", "for X in (Q, K, dO, V)), scale", 0),
+    ("bwd_packed_skips_last_sequence", "    for b in range(cu.size - 1):\n        s0, s1 = int(cu[b]), int(cu[b + 1])\n        if s1 == s0:\n            continue\n        g =",
+     "    for b in range(cu.size - 2):\n        s0, s1 = int(cu[b]), int(cu[b + 1])\n        if s1 == s0:\n            continue\n        g =", 0),
+]
+
+
 def _mutate(src, old, new, occ):
     idx = -1
     for _ in range(occ + 1):
@@ -126,22 +140,33 @@ def test_mutant_is_caught(tmp_path, name, old, new, occ):
     assert r.returncode != 3, f"mutant {name} passed every pin"
 
 
-@pytest.mark.parametrize("name,old,new,occ", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
-def test_fp8_mutant_is_caught(tmp_path, name, old, new, occ):
-    """The same for the FP8 method's Python steps: a copy of the oracle
-    package whose ``fp8.py`` holds the mistake is put first on the path, and
-    the FP8 pins run against it."""
+def _run_package_mutant(tmp_path, fname, name, old, new, occ, prefix):
+    """A copy of the oracle package whose ``fname`` holds the mistake, first on
+    the path of a child process that runs the pins named ``prefix*``."""
     pkg = os.path.dirname(oracle.__file__)
     dst = tmp_path / "oracle"
     dst.mkdir()
-    for f in ("__init__.py", "oracle.c"):
-        shutil.copy(os.path.join(pkg, f), dst / f)
-    src = open(os.path.join(pkg, "fp8.py"), encoding="utf-8").read()
-    (dst / "fp8.py").write_text(_mutate(src, old, new, occ), encoding="utf-8")
+    for f in ("__init__.py", "fp8.py", "oracle.c"):
+        text = open(os.path.join(pkg, f), encoding="utf-8").read()
+        (dst / f).write_text(_mutate(text, old, new, occ) if f == fname else text,
+                             encoding="utf-8")
     so = oracle.compile_oracle(SRC, str(tmp_path / "liboracle.so"))
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     tests = os.path.dirname(os.path.abspath(__file__))
-    r = subprocess.run([sys.executable, "-c", _RUNNER, f"{tmp_path}|{root}", tests, so,
-                        "pin_fp8"], capture_output=True, text=True, timeout=300)
+    r = subprocess.run([sys.executable, "-c", _RUNNER, f"{tmp_path}|{root}", tests, so, prefix],
+                       capture_output=True, text=True, timeout=300)
     assert f"ORACLE_PACKAGE {dst / '__init__.py'}" in r.stdout, (r.stdout, r.stderr[-2000:])
-    assert r.returncode != 3, f"mutant {name} passed every FP8 pin"
+    assert r.returncode != 3, f"mutant {name} passed every pin named {prefix}*"
+
+
+@pytest.mark.parametrize("name,old,new,occ", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_mutant_is_caught(tmp_path, name, old, new, occ):
+    """The same for the FP8 method's Python steps, against the FP8 pins."""
+    _run_package_mutant(tmp_path, "fp8.py", name, old, new, occ, "pin_fp8")
+
+
+@pytest.mark.parametrize("name,old,new,occ", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_binding_mutant_is_caught(tmp_path, name, old, new, occ):
+    """The same for the oracle's Python layer (layouts of the row statistics,
+    per-sequence slicing of packed batches), against every pin."""
+    _run_package_mutant(tmp_path, "__init__.py", name, old, new, occ, "pin_")
