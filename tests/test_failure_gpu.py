@@ -68,19 +68,18 @@ def _normwise(g, ref):
     return float(np.abs(g - ref).max() / max(np.abs(ref).max(), 1e-3))
 
 
-@pytest.mark.parametrize("lens,d,causal", [
-    ((256, 256), 128, True),        # dense, two steps per CTA at most: the ring never wraps
-    ((300, 300), 64, False),        # dense, d = 64 (zero rows of K^T)
-    ((1000, 1000), 128, True),      # dense, the producer waits for ring stages to free
-    ((1, 129, 700, 0, 64), 128, True),   # packed: ragged, one token, an empty sequence
+@pytest.mark.parametrize("packed,lens,d,causal", [
+    (False, (256, 256), 128, True),       # dense B=2: two or four 64-query steps per CTA
+    (False, (300, 300), 64, False),       # dense B=2, d = 64 (zero rows of K^T)
+    (False, (1000, 1000), 128, True),     # dense B=2: up to 16 steps, the 3-stage ring wraps
+    (True, (1, 129, 700, 0, 64), 128, True),   # packed: ragged, one token, an empty sequence
 ])
-def test_expired_wait_in_one_pass_backward(dev, lens, d, causal):
+def test_expired_wait_in_one_pass_backward(dev, packed, lens, d, causal):
     """The same switch on the one-pass backward: its tensor-core warp gives up,
     the row warps and the copy warp leave their loops, dK and dV stay
     unwritten, dQ is converted from an accumulator that received nothing
     (zero), and the next call matches the oracle."""
     H = 3
-    packed = len(set(lens)) > 1
     B, N = len(lens), max(lens)
     cu = workloads.cu_seqlens_of(lens)
     total = int(cu[-1])
